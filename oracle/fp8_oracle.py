@@ -1,0 +1,257 @@
+"""CPU oracle for the block-scaled FP8 linear layer.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain reference that the
+CUDA library is checked against.  Only the test suite, the package's smoke
+entry point and the benchmark's CPU-baseline leg may import it; the product
+path never does, and it shares no code, tables or helpers with the CUDA
+kernels.
+
+What it computes, and where each step comes from:
+
+* The element format is FP8 E4M3 and the blocks are 1x128 for activations and
+  128x128 for weights -- page "NVIDIA NeMo RL достигает ускорения на 48%
+  благодаря сквозному обучению с точностью FP8" (greentreeone.com),
+  §Технический прорыв.  The pages do not spell out the bit layout; it is taken
+  from the public OCP 8-bit Floating Point specification (OFP8, 2023), E4M3:
+  1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+  S.1111.111 is NaN, largest finite magnitude 448.
+* A power-of-two scale option -- page "NVIDIA NeMo RL FP8" (upppp.jp),
+  §設定方法, and the greentreeone.com page, §Почему это важно.
+* Scales are recomputed from the current tensor on every call (weights are
+  re-quantised after each optimizer step) -- upppp.jp page,
+  §KVキャッシュとAttentionにも拡張; greentreeone.com page,
+  §Реальные прирост производительности.
+* Linear layers do their arithmetic on the FP8 codes with higher-precision
+  accumulation -- page "エンドツーエンドFP8精度で実現する高スループット強化学習
+  トレーニング" (ai.warp-studio.com), §FP8強化学習における精度と安定性の確保.
+
+Readings where the pages are silent (each also listed in the design notes):
+scale = amax/448 rounded to fp32; an all-zero block gets scale 1; the cast
+divides by the scale (x/s, IEEE fp32) before rounding to E4M3 with
+round-to-nearest-even and saturation at +-448; the power-of-two scale is
+2**ceil(log2(amax/448)) with the exponent clamped to [-127, 127]; the GEMM
+reference is dequantise-then-multiply in fp64.
+
+Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
+against facts that do not come from this file (the OCP code table, library
+casts, exact rational arithmetic, brute force and closed forms).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0        # largest finite E4M3 magnitude (OCP OFP8, E4M3 row)
+QBLOCK = 128            # block edge: 1x128 activations, 128x128 weights
+
+__all__ = [
+    "E4M3_MAX", "QBLOCK",
+    "e4m3_decode", "e4m3_encode", "bf16_bits_to_f32",
+    "block_amax_act", "block_amax_weight",
+    "scale_from_amax_fp32", "scale_from_amax_pow2", "scale_from_amax",
+    "quant_act_1x128", "quant_weight_128x128",
+    "dequant_act", "dequant_weight",
+    "gemm_ref", "gemm_ref_rows", "grouped_gemm_ref",
+]
+
+
+# --------------------------------------------------------------------------
+# Element format
+# --------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 byte as float64 (NaN for the two NaN codes).
+
+    OCP OFP8 E4M3: sign = bit 7, exponent field E = bits 6..3 (bias 7),
+    mantissa m = bits 2..0.  E == 0 is subnormal, value m * 2**-9; otherwise
+    (1 + m/8) * 2**(E-7).  E == 15 with m == 7 is NaN; there is no infinity.
+    """
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((b >> 7) & 1, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    sub = m.astype(np.float64) * 2.0 ** -9
+    nrm = (1.0 + m.astype(np.float64) / 8.0) * np.exp2((e - 7).astype(np.float64))
+    val = sign * np.where(e == 0, sub, nrm)
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+# The 127 non-negative finite codes 0x00..0x7E; their values increase with the
+# code, so a sorted search over this table finds the two neighbours of |y|.
+_POS_CODES = np.arange(0x7F, dtype=np.uint8)
+_POS_VALUES = e4m3_decode(_POS_CODES)
+
+
+def e4m3_encode(y) -> np.ndarray:
+    """E4M3 code of each finite float32 value: round to nearest, ties to the
+    even code, magnitudes at or above 448 saturate to 448 (code 0x7E).
+
+    The sign bit of the input becomes the sign bit of the code, so -0.0 maps
+    to 0x80.  Between two neighbouring representable values lo <= |y| < hi the
+    nearer one wins; on an exact tie the code whose last bit is 0 wins (the
+    even mantissa).  The distances are exact in float64 because |y| is a
+    float32 and lo, hi are E4M3 values.  Non-finite inputs are outside the
+    contract.
+    """
+    y = np.asarray(y, dtype=np.float32)
+    neg = np.signbit(y)
+    a = np.abs(y.astype(np.float64))
+    sat = a >= E4M3_MAX
+    a_in = np.where(sat, 0.0, a)
+    lo_idx = np.searchsorted(_POS_VALUES, a_in, side="right") - 1
+    lo_idx = np.clip(lo_idx, 0, 125)
+    hi_idx = lo_idx + 1
+    d_lo = a_in - _POS_VALUES[lo_idx]
+    d_hi = _POS_VALUES[hi_idx] - a_in
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi_idx % 2 == 0))
+    mag = np.where(pick_hi, hi_idx, lo_idx)
+    mag = np.where(sat, 0x7E, mag).astype(np.uint8)
+    return (mag | (neg.astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) to the float32 values they denote (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Block statistics and scales
+# --------------------------------------------------------------------------
+def _check_mult(n, what):
+    if n % QBLOCK:
+        raise ValueError(f"{what}={n} is not a multiple of {QBLOCK}")
+
+
+def block_amax_act(x: np.ndarray) -> np.ndarray:
+    """max |x| over each 1x128 block of a [M, K] float32 matrix -> [M, K/128]."""
+    M, K = x.shape
+    _check_mult(K, "K")
+    return np.abs(x).reshape(M, K // QBLOCK, QBLOCK).max(axis=2).astype(np.float32)
+
+
+def block_amax_weight(w: np.ndarray) -> np.ndarray:
+    """max |w| over each 128x128 tile of a [N, K] float32 matrix -> [N/128, K/128]."""
+    N, K = w.shape
+    _check_mult(N, "N")
+    _check_mult(K, "K")
+    t = np.abs(w).reshape(N // QBLOCK, QBLOCK, K // QBLOCK, QBLOCK)
+    return t.max(axis=(1, 3)).astype(np.float32)
+
+
+def scale_from_amax_fp32(amax) -> np.ndarray:
+    """fp32 scale s = amax / 448 (IEEE float32 division); s = 1 for amax == 0."""
+    amax = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = amax / np.float32(E4M3_MAX)
+    return np.where(amax > 0, s, np.float32(1.0)).astype(np.float32)
+
+
+def scale_from_amax_pow2(amax) -> np.ndarray:
+    """Power-of-two scale 2**e with e = ceil(log2(amax / 448)).
+
+    amax = F * 2**E with F in [1, 2) (frexp, which also normalises
+    subnormals).  Because 448 = 1.75 * 2**8, amax / 448 = (F / 1.75) * 2**(E-8)
+    with F / 1.75 in [4/7, 8/7), so the ceiling of its log2 is E - 8 when
+    F <= 1.75 and E - 7 when F > 1.75.  e is clamped to [-127, 127] (the range
+    an 8-bit power-of-two exponent can hold); amax == 0 gives e = 0.
+    """
+    amax = np.asarray(amax, dtype=np.float32).astype(np.float64)
+    f, E = np.frexp(amax)          # amax = f * 2**E, f in [0.5, 1)
+    F = 2.0 * f
+    E = E - 1
+    e = E - 8 + (F > 1.75).astype(np.int64)
+    e = np.clip(e, -127, 127)
+    e = np.where(amax > 0, e, 0)
+    return np.ldexp(np.float64(1.0), e).astype(np.float32)
+
+
+def scale_from_amax(amax, pow2: bool) -> np.ndarray:
+    return scale_from_amax_pow2(amax) if pow2 else scale_from_amax_fp32(amax)
+
+
+# --------------------------------------------------------------------------
+# Quantisers
+# --------------------------------------------------------------------------
+def _cast(x: np.ndarray, s_broadcast: np.ndarray) -> np.ndarray:
+    """codes = e4m3(RN_fp32(x / s)) elementwise (IEEE float32 division)."""
+    q32 = (x.astype(np.float32) / s_broadcast.astype(np.float32)).astype(np.float32)
+    return e4m3_encode(q32)
+
+
+def quant_act_1x128(x: np.ndarray, pow2: bool = False):
+    """1x128 activation quantisation.
+
+    x: float32 [M, K] (bf16 values).  Returns (q uint8 [M, K],
+    s float32 [M, K/128]) where s[m, kb] is the scale of row m, columns
+    kb*128 .. kb*128+127, and q = e4m3(x / s).  (The library stores the
+    scales K-block-major, s[kb][m]; that is a layout choice, the values are
+    these.)
+    """
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    s = scale_from_amax(block_amax_act(x), pow2)
+    sb = np.repeat(s, QBLOCK, axis=1)
+    return _cast(x, sb), s
+
+
+def quant_weight_128x128(w: np.ndarray, pow2: bool = False):
+    """128x128 weight quantisation.
+
+    w: float32 [N, K] (bf16 values).  Returns (q uint8 [N, K],
+    s float32 [N/128, K/128]) with q = e4m3(w / s) tile by tile.
+    """
+    w = np.asarray(w, dtype=np.float32)
+    s = scale_from_amax(block_amax_weight(w), pow2)
+    sb = np.repeat(np.repeat(s, QBLOCK, axis=0), QBLOCK, axis=1)
+    return _cast(w, sb), s
+
+
+# --------------------------------------------------------------------------
+# GEMM reference: dequantise, then multiply in fp64
+# --------------------------------------------------------------------------
+def dequant_act(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """dec(q[m, k]) * s[m, k // 128] in float64 (exact: <= 4 + 24 bits)."""
+    return e4m3_decode(q) * np.repeat(np.asarray(s, np.float64), QBLOCK, axis=1)
+
+
+def dequant_weight(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """dec(q[n, k]) * s[n // 128, k // 128] in float64 (exact)."""
+    sb = np.repeat(np.repeat(np.asarray(s, np.float64), QBLOCK, axis=0), QBLOCK, axis=1)
+    return e4m3_decode(q) * sb
+
+
+def gemm_ref(qa, sa, qw, sw) -> np.ndarray:
+    """C[m, n] = sum_k deqA[m, k] * deqW[n, k] in float64 (C = A W^T).
+
+    Equal, up to fp64 rounding order, to sum over K-blocks kb of
+    sA[m, kb] * sW[n/128, kb] * sum_{k in kb} dec(qA[m, k]) dec(qW[n, k]).
+    """
+    return dequant_act(qa, sa) @ dequant_weight(qw, sw).T
+
+
+def gemm_ref_rows(qa, sa, qw, sw, rows) -> np.ndarray:
+    """gemm_ref restricted to the given output rows (for sampled checks)."""
+    rows = np.asarray(rows)
+    return dequant_act(qa[rows], sa[rows]) @ dequant_weight(qw, sw).T
+
+
+def grouped_gemm_ref(qa, sa, offsets, qw_groups, sw_groups, rows=None) -> np.ndarray:
+    """Per-expert GEMM: rows offsets[g] .. offsets[g+1]-1 of A times W_g^T.
+
+    qw_groups: uint8 [G, N, K]; sw_groups: float32 [G, N/128, K/128].
+    Empty groups contribute no rows.  With `rows`, only those output rows are
+    computed (returned in the order given).
+    """
+    offsets = np.asarray(offsets, dtype=np.int64)
+    G = len(offsets) - 1
+    N = qw_groups.shape[1]
+    M = qa.shape[0]
+    want = np.arange(M) if rows is None else np.asarray(rows)
+    out = np.zeros((len(want), N), dtype=np.float64)
+    grp = np.searchsorted(offsets, want, side="right") - 1
+    for g in range(G):
+        sel = np.nonzero(grp == g)[0]
+        if sel.size == 0:
+            continue
+        r = want[sel]
+        out[sel] = dequant_act(qa[r], sa[r]) @ dequant_weight(qw_groups[g], sw_groups[g]).T
+    return out
