@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled FP8 linear layer at Llama-3.1-8B shapes.
+
+One step = the whole hot path over one batch: for each of the three linear
+layers of a Llama-3.1-8B block at M = 4096 tokens (QKV K=4096 N=6144,
+gate+up K=4096 N=28672, down K=14336 N=4096): 1x128 activation quantisation,
+128x128 weight re-quantisation (weights change every optimizer step) and the
+block-scaled FP8 GEMM, all in libfp8bs.so's kernels, fp32 amax/448 scales.
+
+metric: quant+GEMM TFLOP/s = sum(2 M N K) / (t_quantA + t_quantW + t_gemm).
+
+Timing: W untimed warm-up steps, then exactly K steps, each preceded (outside
+its CUDA-event interval) by a 256 MB write that flushes the 129 MB L2;
+barrier + synchronize around the timed region; max over ranks.  N > 1 runs
+independent replicas (the path has no exchange step): value is the work of
+all ranks divided by the slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the
+same workload instead; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 quant+GEMM TFLOP/s at Llama-8B shapes; % FP8 peak / HBM"
+UNIT = "TFLOP/s"
+WORKLOAD = "llama3.1-8b linear layers, M=4096 tokens: qkv(K4096,N6144) gate_up(K4096,N28672) down(K14336,N4096)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20
+# bounded oracle sample per layer: rows of A and rows of W
+CPU_SAMPLE_ROWS_A = 128
+CPU_SAMPLE_ROWS_W = 512
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    a = p.parse_args(argv)
+    a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
+    return a
+
+
+# ------------------------------------------------------------------ peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs") or 0) or None
+        bf16 = float(d.get("bf16_tflops") or 0) or None
+        bf16_s = float(d.get("bf16_tflops_sustained") or 0) or None
+        if hbm and bf16:
+            return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_s or bf16,
+                    "source": "measured"}
+    except (OSError, ValueError, TypeError):
+        pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ dist
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle sample
+def oracle_sample(layers, rows_a=CPU_SAMPLE_ROWS_A, rows_w=CPU_SAMPLE_ROWS_W):
+    """Time the CPU oracle on a bounded sample of each layer (first rows_a rows
+    of A, first rows_w rows of W): quant A, quant W, GEMM.  Returns
+    (flops of the sample, seconds)."""
+    import numpy as np
+    import oracle.fp8_oracle as O
+    flops = 0.0
+    t0 = time.perf_counter()
+    for a, w in layers:
+        xa = a[:rows_a].float().numpy()
+        xw = w[:rows_w].float().numpy()
+        qa, sa = O.quant_act_1x128(xa)
+        qw, sw = O.quant_weight_128x128(xw)
+        c = O.gemm_ref(qa, sa, qw, sw)
+        assert np.isfinite(c).all()
+        flops += 2.0 * xa.shape[0] * xw.shape[0] * xa.shape[1]
+    return flops, time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def sample_desc():
+    return (f"oracle (numpy, fp64 GEMM) on the first {CPU_SAMPLE_ROWS_A} rows of A and first "
+            f"{CPU_SAMPLE_ROWS_W} rows of W of each of the 3 layers (quant A + quant W + GEMM); "
+            f"value = sample FLOPs / sample time")
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from fp8_block_scaled_05_gb300 import inputs as I
+    layers = [(c.a, c.w) for c in I.llama8b_layers(args.seed)]
+    for _ in range(args.warmup):
+        oracle_sample(layers)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(layers)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample_desc()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample_desc()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def traffic_for(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        from fp8_block_scaled_05_gb300 import build as B
+        if d.get("source_stamp") != B.source_stamp():
+            return None
+        return d.get("kernels", {}).get(kernel)
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from fp8_block_scaled_05_gb300 import build as B
+    from fp8_block_scaled_05_gb300 import inputs as I
+    from fp8_block_scaled_05_gb300 import ops
+
+    B.build()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    stream = torch.cuda.Stream(device=dev)
+    cases = I.llama8b_layers(args.seed)
+
+    layers = []
+    for c in cases:
+        M, N, K = c.shape
+        a = c.a.to(dev)
+        w = c.w.to(dev)
+        L = dict(name=c.name.split(".")[1], M=M, N=N, K=K, a=a, w=w,
+                 qa=torch.empty((M, K), dtype=torch.uint8, device=dev),
+                 sa=torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev),
+                 qw=torch.empty((N, K), dtype=torch.uint8, device=dev),
+                 sw=torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
+                 c=torch.empty((M, N), dtype=torch.bfloat16, device=dev))
+        layers.append(L)
+    flops_step = sum(2.0 * L["M"] * L["N"] * L["K"] for L in layers)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = 3 * len(layers)
+
+    def step(events=None):
+        for i, L in enumerate(layers):
+            if events is not None:
+                events[3 * i].record(stream)
+            ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
+            if events is not None:
+                events[3 * i + 1].record(stream)
+            ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
+            if events is not None:
+                events[3 * i + 2].record(stream)
+            ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, None, stream)
+        if events is not None:
+            events[3 * len(layers)].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize(dev)
+    st = ops.fp8_last_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {ops.status_string(st)}")
+
+    nev = 3 * len(layers) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush.zero_()
+            step(evs[k])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+
+    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
+    kern = {}
+    for i, L in enumerate(layers):
+        for j, kname in enumerate(("quant_act", "quant_weight", "gemm")):
+            ms = [evs[k][3 * i + j].elapsed_time(evs[k][3 * i + j + 1]) for k in range(args.steps)]
+            kern[f"{L['name']}.{kname}"] = sum(ms) / len(ms)
+    total_ms = reduce_max(sum(step_ms), world, dev)
+    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # dominant kernel: the GEMM with the largest time share
+    gemms = {L["name"]: (kern[f"{L['name']}.gemm"], 2.0 * L["M"] * L["N"] * L["K"]) for L in layers}
+    dom = max(gemms, key=lambda n: gemms[n][0])
+    dom_ms, dom_flops = gemms[dom]
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    traffic = traffic_for(f"gemm.{dom}")
+    kernels_out = {}
+    for L in layers:
+        n = L["name"]
+        qa_bytes = 2 * L["M"] * L["K"] + L["M"] * L["K"] + 4 * L["M"] * L["K"] // 128
+        qw_bytes = 2 * L["N"] * L["K"] + L["N"] * L["K"] + 4 * (L["N"] // 128) * (L["K"] // 128)
+        kernels_out[f"{n}.quant_act"] = {"ms": kern[f"{n}.quant_act"],
+                                         "GB/s": qa_bytes / kern[f"{n}.quant_act"] / 1e6,
+                                         "frac_hbm": qa_bytes / kern[f"{n}.quant_act"] / 1e6 / peaks["hbm_gbs"]}
+        kernels_out[f"{n}.quant_weight"] = {"ms": kern[f"{n}.quant_weight"],
+                                            "GB/s": qw_bytes / kern[f"{n}.quant_weight"] / 1e6,
+                                            "frac_hbm": qw_bytes / kern[f"{n}.quant_weight"] / 1e6 / peaks["hbm_gbs"]}
+        gf = 2.0 * L["M"] * L["N"] * L["K"]
+        kernels_out[f"{n}.gemm"] = {"ms": kern[f"{n}.gemm"], "TFLOP/s": gf / kern[f"{n}.gemm"] / 1e9,
+                                    "frac_fp8": gf / kern[f"{n}.gemm"] / 1e9 / fp8_peak}
+    gemm_ms = sum(kern[f"{L['name']}.gemm"] for L in layers)
+
+    # ---------------- end to end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host = [(L["a"].cpu().pin_memory(), L["w"].cpu().pin_memory(),
+                 torch.empty((L["M"], L["N"]), dtype=torch.bfloat16).pin_memory()) for L in layers]
+        h2d = sum(a.numel() * 2 + w.numel() * 2 for a, w, _ in host)
+        d2h = sum(c.numel() * 2 for _, _, c in host)
+        e2e_steps = max(3, args.steps // 4)
+
+        def e2e_step():
+            for L, (ah, wh, ch) in zip(layers, host):
+                L["a"].copy_(ah, non_blocking=True)
+                L["w"].copy_(wh, non_blocking=True)
+                ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
+                ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
+                ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, None, stream)
+                ch.copy_(L["c"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_step()
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": e2e_ms / e2e_steps}
+
+    st = ops.fp8_last_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status after the timed region: {ops.status_string(st)}")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        layers_cpu = [(c.a, c.w) for c in cases]
+        f, s = oracle_sample(layers_cpu)
+        cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": sample_desc(), "seconds": s}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate, bf16 out",
+            "data": "synthetic (seeded numpy PCG64: A ~ N(0,1) with 1% outlier channels x30, W ~ N(0,0.02))",
+            "config": {"workload": WORKLOAD, "M": 4096, "scale": "fp32 amax/448",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed before every timed step (256 MB write outside the step's events)"},
+            "roofline": {"bound": "tensor", "kernel": f"gemm.{dom}", "achieved": achieved, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
+                         "peak_source": f"{peaks['source']}: bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
+                                        f"(fp8/bf16 nominal ratio)",
+                         "hbm_peak_gbs": peaks["hbm_gbs"]},
+            "gemm_only_tflops": sum(g[1] for g in gemms.values()) / (gemm_ms / 1e3) / 1e12,
+            "kernels": kernels_out,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

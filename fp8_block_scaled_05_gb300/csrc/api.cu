@@ -1,0 +1,333 @@
+// C-ABI entry points (include/fp8bs.h): argument validation, per-device
+// state, TMA descriptor cache and kernel dispatch.  Host code only.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "fp8bs.h"
+#include "internal.h"
+
+namespace fp8bs {
+namespace {
+
+// First error recorded by any kernel on this device (0 = none).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+fp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+// Current device, checked to be sm_103, with its SM count and status word.
+fp8_status current_device(DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FP8_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.device < 0) {
+        int major = 0, minor = 0, sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8_ERR_ARCH;
+        }
+        if (major != 10 || minor != 3) return FP8_ERR_ARCH;
+        void* sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8_ERR_CUDA;
+        }
+        if (cudaMemset(sym, 0, sizeof(int)) != cudaSuccess) return FP8_ERR_CUDA;
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn) {
+                cudaGetLastError();
+                return FP8_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.sm_count = sms;
+        d.max_smem_optin = smem;
+        d.status = static_cast<int*>(sym);
+        d.device = dev;
+    }
+    *out = &d;
+    return FP8_OK;
+}
+
+// ------------------------------------------------------------ TMA descriptors
+struct TmKey {
+    uint64_t ptr, d0, d1, pitch;
+    uint32_t b0, b1;
+    int dtype, swizzle;
+    bool operator==(const TmKey& o) const { return std::memcmp(this, &o, sizeof(TmKey)) == 0; }
+};
+struct TmKeyHash {
+    size_t operator()(const TmKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+        for (size_t i = 0; i < sizeof(TmKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+        return (size_t)h;
+    }
+};
+std::mutex g_tm_mu;
+std::unordered_map<TmKey, CUtensorMap, TmKeyHash> g_tm_cache;
+
+// 2-D row-major tensor [d1 rows][d0 elements], row pitch in bytes, box
+// {b0, b1}.  Descriptors are cached by all of these; entries stay valid
+// because a descriptor depends on nothing else.
+fp8_status tensor_map(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t pitch_bytes,
+                      uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz, const CUtensorMap** out) {
+    TmKey key;
+    std::memset(&key, 0, sizeof(key));
+    key.ptr = reinterpret_cast<uint64_t>(ptr);
+    key.d0 = d0;
+    key.d1 = d1;
+    key.pitch = pitch_bytes;
+    key.b0 = b0;
+    key.b1 = b1;
+    key.dtype = (int)dtype;
+    key.swizzle = (int)swz;
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    auto it = g_tm_cache.find(key);
+    if (it != g_tm_cache.end()) {
+        *out = &it->second;
+        return FP8_OK;
+    }
+    if (g_tm_cache.size() > 4096) g_tm_cache.clear();
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {b0, b1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FP8_ERR_CUDA;
+    auto ins = g_tm_cache.emplace(key, m);
+    *out = &ins.first->second;
+    return FP8_OK;
+}
+
+fp8_status check_mode(int mode) { return (mode == FP8_SCALE_FP32_AMAX || mode == FP8_SCALE_POW2) ? FP8_OK : FP8_ERR_SCALE_MODE; }
+
+constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_MASK;
+
+uint32_t plan_path(int64_t M, uint32_t flags) {
+    const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
+    if (forced != FP8_GEMM_PATH_AUTO) return forced;
+    if (M <= 256) return FP8_GEMM_PATH_SKINNY;
+    return FP8_GEMM_PATH_PROMOTE;
+}
+
+// Shared validation of the GEMM operands (both forms).
+fp8_status check_gemm_common(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                             const float* sb, const void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                             uint32_t flags) {
+    if (M < 0 || N <= 0 || K <= 0 || (N % 128) || (K % 128)) return FP8_ERR_SHAPE;
+    if (M > INT32_MAX / 2 || N > (1ll << 24) || K > (1ll << 24)) return FP8_ERR_SHAPE;
+    if (flags & ~kKnownFlags) return FP8_ERR_SCALE_MODE;
+    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
+    if (path > FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
+    if (path == FP8_GEMM_PATH_MX && !(flags & FP8_GEMM_SCALES_POW2)) return FP8_ERR_SCALE_MODE;
+    if (M == 0) return FP8_OK;
+    if (!qa || !sa || !qb || !sb || !c) return FP8_ERR_NULL;
+    if (lda < K || ldc < N || ldsa < M) return FP8_ERR_SHAPE;
+    if ((lda % 16) || (ldsa % 4) || (ldc % 8)) return FP8_ERR_ALIGN;
+    if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(c)) return FP8_ERR_ALIGN;
+    return FP8_OK;
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" {
+
+const char* fp8_status_string(fp8_status st) {
+    switch (st) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_NULL: return "FP8_ERR_NULL: a required pointer is NULL";
+        case FP8_ERR_SHAPE: return "FP8_ERR_SHAPE: sizes out of range or leading dimension too small";
+        case FP8_ERR_ALIGN: return "FP8_ERR_ALIGN: pointer or row pitch not 16-byte aligned";
+        case FP8_ERR_SCALE_MODE: return "FP8_ERR_SCALE_MODE: unknown scale mode or flags";
+        case FP8_ERR_WORKSPACE: return "FP8_ERR_WORKSPACE: workspace missing or too small";
+        case FP8_ERR_ARCH: return "FP8_ERR_ARCH: no sm_103 CUDA device is current";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA: a CUDA call failed";
+        case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT: a kernel wait ran out of time";
+        case FP8_ERR_NOT_IMPLEMENTED: return "FP8_ERR_NOT_IMPLEMENTED: path not built";
+    }
+    return "unknown fp8_status";
+}
+
+fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq, float* s,
+                               int64_t lds, fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 21) || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x || !q || !s) return FP8_ERR_NULL;
+    if (ldx < K || ldq < K || lds < M) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldq % 16) || (lds % 4) || !aligned16(x) || !aligned16(q) || !aligned16(s)) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_act_1x128(x, M, K, ldx, q, ldq, s, lds, mode == FP8_SCALE_POW2,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                                    float* s, fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (N <= 0 || K <= 0 || (N % 128) || (K % 128) || N / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (!w || !q || !s) return FP8_ERR_NULL;
+    if (ldw < K || ldq < K) return FP8_ERR_SHAPE;
+    if ((ldw % 8) || (ldq % 16) || !aligned16(w) || !aligned16(q) || !aligned16(s)) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_weight_128x128(w, N, K, ldw, q, ldq, s, mode == FP8_SCALE_POW2,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t* splits) {
+    const uint32_t path = plan_path(M, flags);
+    int32_t sp = 1;
+    if (path == FP8_GEMM_PATH_SKINNY) {
+        int sms = 152;
+        DeviceInfo* d;
+        if (current_device(&d) == FP8_OK) sms = d->sm_count;
+        sp = skinny_splits(M, N, K, sms);
+    }
+    if (splits) *splits = sp;
+    return path;
+}
+
+size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t G) {
+    if (G != 1 || M <= 0 || N <= 0 || K <= 0) return 0;
+    int32_t sp = 1;
+    const uint32_t path = fp8_gemm_plan(M, N, K, FP8_GEMM_PATH_AUTO, &sp);
+    if (path != FP8_GEMM_PATH_SKINNY) return 0;
+    return skinny_workspace_bytes(M, N, K, sp);
+}
+
+fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa, const uint8_t* qb,
+                                int64_t ldb, const float* sb, void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                uint32_t flags, void* workspace, size_t ws_bytes, fp8_stream_t stream) {
+    if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M, N, K, flags)) return e;
+    if (M == 0) return FP8_OK;
+    if (ldb < K) return FP8_ERR_SHAPE;
+    if (ldb % 16) return FP8_ERR_ALIGN;
+    const uint32_t path = plan_path(M, flags);
+    if (path == FP8_GEMM_PATH_MX) return FP8_ERR_NOT_IMPLEMENTED;
+    if (path == FP8_GEMM_PATH_SKINNY && M > 256) return FP8_ERR_SHAPE;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+
+    GemmArgs a{};
+    a.sa = sa;
+    a.ldsa = ldsa;
+    a.sb = sb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.offsets = nullptr;
+    a.G = 1;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = 1;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    if (path == FP8_GEMM_PATH_SKINNY) {
+        const int nt = skinny_tile_n(M);
+        a.splits = skinny_splits(M, N, K, d->sm_count);
+        const size_t need = skinny_workspace_bytes(M, N, K, a.splits);
+        if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace))) return FP8_ERR_WORKSPACE;
+        a.workspace = workspace;
+        a.ws_bytes = ws_bytes;
+        if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, nt,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+            return e;
+        if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, 128,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+            return e;
+        if (fp8_status e = tensor_map(sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, M, K / 128, ldsa * 4, nt, 1,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE, &a.tm_sa))
+            return e;
+        return cuda_status(launch_gemm_skinny(a, st));
+    }
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, kPromoteBN,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+        return e;
+    return cuda_status(launch_gemm_promote(a, st));
+}
+
+fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                        const int32_t* offsets, int32_t G, int64_t M_total, const uint8_t* qb,
+                                        const float* sb, void* c, int64_t ldc, int64_t N, int64_t K, uint32_t flags,
+                                        void* workspace, size_t ws_bytes, fp8_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (G < 1 || G > 1024) return FP8_ERR_SHAPE;
+    if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M_total, N, K, flags)) return e;
+    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
+    if (path != FP8_GEMM_PATH_AUTO && path != FP8_GEMM_PATH_PROMOTE) return FP8_ERR_NOT_IMPLEMENTED;
+    if (M_total == 0) return FP8_OK;
+    if (!offsets) return FP8_ERR_NULL;
+    if ((int64_t)G * N > INT32_MAX) return FP8_ERR_SHAPE;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    GemmArgs a{};
+    a.sa = sa;
+    a.ldsa = ldsa;
+    a.sb = sb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M_total;
+    a.N = N;
+    a.K = K;
+    a.offsets = offsets;
+    a.G = G;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = 1;
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M_total, lda, 128, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, (uint64_t)G * N, K, 128, kPromoteBN,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+        return e;
+    return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_last_device_status(fp8_stream_t stream) {
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
+    if (v != 0 && cudaMemset(d->status, 0, sizeof(int)) != cudaSuccess) return FP8_ERR_CUDA;
+    return static_cast<fp8_status>(v);
+}
+
+}  // extern "C"

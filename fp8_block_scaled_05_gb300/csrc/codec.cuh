@@ -1,0 +1,140 @@
+// Device-side pieces of the block quantisers: bf16 unpacking, block amax,
+// the two scale rules, the per-element division and the E4M3 conversion.
+//
+// Method (page "NVIDIA NeMo RL достигает ускорения на 48% благодаря
+// сквозному обучению с точностью FP8", greentreeone.com, §Технический
+// прорыв; power-of-two option: upppp.jp NeMo RL FP8 article, §設定方法):
+//   s = RN_fp32(amax / 448)   or   s = 2^ceil(log2(amax / 448)) (clamped to
+//   [2^-127, 2^127]); s = 1 for an all-zero block;
+//   q = e4m3_RNE_satfinite( RN_fp32(x / s) ).
+#pragma once
+#include <cstdint>
+
+namespace fp8bs {
+
+// Two bf16 values packed in a 32-bit word (element 2i in the low half) to fp32.
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Element-wise max of the magnitudes of two bf16 pairs, as bf16 bit patterns.
+// For non-NaN bf16, |x| ordered as floats equals its bits ordered as
+// unsigned integers, so a packed unsigned 16-bit max gives the amax.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+    uint32_t r;
+    const uint32_t a = w & 0x7FFF7FFFu;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(a));
+    return r;
+}
+
+// Larger of the two halves, as the fp32 value of that bf16.
+__device__ __forceinline__ float absmax_pair_to_f32(uint32_t m) {
+    const uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+    return __uint_as_float((lo > hi ? lo : hi) << 16);
+}
+
+// Power-of-two exponent e = ceil(log2(amax / 448)), clamped to [-127, 127];
+// 0 for amax == 0.  448 = 1.75 * 2^8: with amax = F * 2^E, F in [1, 2),
+// e = E - 8 when F <= 1.75 and E - 7 when F > 1.75.
+__device__ __forceinline__ int pow2_exponent(float amax) {
+    const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (b == 0) return 0;
+    int E;
+    uint32_t mant;                       // 23-bit fraction of F
+    const uint32_t ef = b >> 23;
+    if (ef != 0) {
+        E = (int)ef - 127;
+        mant = b & 0x7FFFFFu;
+    } else {                             // fp32 subnormal: normalise
+        const int lz = __clz(b) - 8;     // leading zeros inside the 23-bit field (+1 for the hidden bit)
+        E = -126 - lz;
+        mant = (b << lz) & 0x7FFFFFu;
+    }
+    int e = E - 8 + (mant > 0x600000u ? 1 : 0);   // F > 1.75  <=>  fraction > 0.75
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    return e;
+}
+
+// 2^e as fp32 for e in [-127, 127] (2^-127 is subnormal, exact).
+__device__ __forceinline__ float exp2_int(int e) {
+    return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Per-block constants for the cast x -> x / s.
+struct BlockScale {
+    float s;         // the stored scale
+    float r;         // RN(1 / s) (fp32 mode) or 2^-e exactly (pow2 mode)
+    int mode;        // 0: two-step corrected quotient, 1: exact product, 2: IEEE division
+};
+
+__device__ __forceinline__ BlockScale make_scale(float amax, bool pow2) {
+    BlockScale bs;
+    if (pow2) {
+        const int e = pow2_exponent(amax);
+        bs.s = exp2_int(e);
+        bs.r = exp2_int(-e);             // exact; x * 2^-e == x / 2^e for every bf16 x in the block
+        bs.mode = 1;
+        return bs;
+    }
+    if (!(amax > 0.0f)) {
+        bs.s = 1.0f;
+        bs.r = 1.0f;
+        bs.mode = 1;
+        return bs;
+    }
+    bs.s = __fdiv_rn(amax, 448.0f);
+    bs.r = __frcp_rn(bs.s);
+    // The two-step correction needs every remainder x - s*q to be exact; that
+    // holds for s >= 2^-90 (see quotient_rn).  Smaller scales (amax below
+    // about 2^-81) take the IEEE division.
+    bs.mode = (__float_as_uint(bs.s) >= (uint32_t)(127 - 90) << 23) ? 0 : 2;
+    return bs;
+}
+
+// RN_fp32(x / s).
+//
+// mode 0 uses a hoisted correctly rounded reciprocal r = RN(1/s) and two
+// residual corrections (Markstein's theorem, as stated in Muller et al.,
+// "Handbook of Floating-Point Arithmetic", division via FMA):
+//   q0 = RN(x r)                   -- within 1.5 ulp of x/s
+//   q1 = RN(q0 + RN(x - s q0) r)   -- faithful (within 1 ulp)
+//   q2 = RN(q1 + (x - s q1) r)     -- x - s q1 is exact for a faithful q1,
+//                                     and the theorem gives q2 = RN(x/s)
+// valid while no remainder underflows: |x/s| >= 2^-11 matters for the E4M3
+// code and s >= 2^-90 keeps x - s q a multiple of 2^-149; quotients below
+// 2^-11 round to a signed zero code either way.
+__device__ __forceinline__ float quotient_rn(float x, const BlockScale &bs) {
+    if (bs.mode == 1) return x * bs.r;
+    if (bs.mode == 2) return __fdiv_rn(x, bs.s);
+    float q = x * bs.r;
+    float rem = fmaf(-bs.s, q, x);
+    q = fmaf(rem, bs.r, q);
+    rem = fmaf(-bs.s, q, x);
+    return fmaf(rem, bs.r, q);
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating to
+// +-448); `lo` goes to bits 0..7, `hi` to bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes).
+__device__ __forceinline__ uint2 quant8(const uint4 &v, const BlockScale &bs) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p[i] = e4m3x2(quotient_rn(bf16lo_to_f32(w[i]), bs), quotient_rn(bf16hi_to_f32(w[i]), bs));
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+__device__ __forceinline__ uint32_t absmax8(uint32_t acc, const uint4 &v) {
+    acc = absmax_bf16x2(acc, v.x);
+    acc = absmax_bf16x2(acc, v.y);
+    acc = absmax_bf16x2(acc, v.z);
+    return absmax_bf16x2(acc, v.w);
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,346 @@
+// Block-scaled FP8 GEMM for decode-sized M (1..256 tokens).
+//
+// Same operation as the large-M kernel (FP8 linear layer with 1x128 / 128x128
+// block scales; page "NVIDIA NeMo RL достигает ускорения на 48% благодаря
+// сквозному обучению с точностью FP8", greentreeone.com, §Технический
+// прорыв), shaped for generation, where the step is bound by streaming the
+// weights (upppp.jp NeMo RL FP8 article, §NeMo RLとは: the generation phase
+// is the latency-critical one).
+//
+// The operands are swapped: 128 weight rows fill the MMA's M side and the
+// tokens, padded to NT in {16, 32, 64, 128, 256}, are its N side, so
+// D[n, m] = sum_k qb[n, k] qa[m, k] lands in TMEM with lane = weight row and
+// column = token.  The K-blocks are split over `splits` CTAs per 128-row
+// weight tile so that the weight stream is spread over every SM; the last
+// CTA of a tile to finish (an atomic ticket in the workspace) adds the fp32
+// partials of all splits in split order and writes bf16, so the result does
+// not depend on which CTA finishes last.
+//
+// Per K-block the promotion multiplies column m by sA[kb, m] * sB[nb, kb]:
+// sB is one value per CTA and K-block, the NT values of sA travel with the
+// operands through the TMA ring (a 2-D fp32 tile, zero-filled past M).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace skinny {
+
+constexpr int BMW = 128;     // weight rows per CTA (MMA M)
+constexpr int BK = 128;
+
+template <int NT>
+struct Cfg {
+    static constexpr int W_BYTES = BMW * BK;
+    static constexpr int A_BYTES = NT * BK;
+    static constexpr int S_BYTES = 1024;                       // NT fp32 scales, padded for alignment
+    static constexpr int STAGE_BYTES = W_BYTES + A_BYTES + S_BYTES;
+    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int NBUF = NT >= 256 ? 2 : (NT >= 128 ? 4 : 4);
+    static constexpr int TMEM_USED = NBUF * NT;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : (TMEM_USED <= 64 ? 64 : (TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512)));
+    static constexpr int EPI_WARPS = NT >= 128 ? 8 : 4;
+    static constexpr int CPW = NT / (EPI_WARPS / 4);           // token columns per epilogue warp
+    static constexpr int CHUNK = CPW >= 128 ? 16 : (CPW < 32 ? CPW : 32);
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(BMW, NT);
+};
+
+struct __align__(8) Ctrl {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[4];
+    uint64_t tempty[4];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+    int32_t last;
+};
+
+template <int NT>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)Cfg<NT>::STAGES * Cfg<NT>::STAGE_BYTES + sizeof(Ctrl);
+}
+
+__device__ __forceinline__ void record_timeout(int* status) {
+    if (status) atomicCAS(status, 0, kStatusTimeout);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+    return r;
+}
+
+template <int CHUNK>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[CHUNK]);
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_x32(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_x16(taddr, r); }
+
+template <int NT>
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
+    k_gemm_skinny(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+                  const __grid_constant__ CUtensorMap tm_sa, const float* __restrict__ sb,
+                  uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K, int splits,
+                  uint8_t* __restrict__ ws, int* status) {
+    using C = Cfg<NT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)C::STAGES * C::STAGE_BYTES);
+
+    const int warp = (int)warp_id(), lane = (int)lane_id();
+    const int KB = K / BK, NB = N / BMW;
+    const int tile = blockIdx.x, split = blockIdx.y;
+    const int kb_begin = (int)((int64_t)split * KB / splits);
+    const int kb_end = (int)((int64_t)(split + 1) * KB / splits);
+    const int nkb = kb_end - kb_begin;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1 + C::EPI_WARPS);
+        }
+        for (int b = 0; b < C::NBUF; ++b) {
+            mbar_init(&ctl->tfull[b], 1);
+            mbar_init(&ctl->tempty[b], C::EPI_WARPS);
+        }
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort_flag = 0;
+        mbar_init_fence();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_sa);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile int32_t* abort_flag = &ctl->abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t evict_first = l2_policy_evict_first();
+            uint32_t it = 0;
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i, ++it) {
+                const int kb = kb_begin + i;
+                const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
+                if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + (size_t)s * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&ctl->full[s], C::W_BYTES + C::A_BYTES + NT * 4);
+                tma_load_2d_hint(st, &tm_w, &ctl->full[s], kb * BK, tile * BMW, evict_first);
+                tma_load_2d(st + C::W_BYTES, &tm_a, &ctl->full[s], kb * BK, 0);
+                tma_load_2d(st + C::W_BYTES + C::A_BYTES, &tm_sa, &ctl->full[s], 0, kb);
+            }
+            if (!ok) {
+                record_timeout(status);
+                *abort_flag = 1;
+                const uint32_t n = it < (uint32_t)C::STAGES ? it : (uint32_t)C::STAGES;
+                for (uint32_t j = it - n; j < it; ++j)
+                    mbar_wait(&ctl->full[j % C::STAGES], (j / C::STAGES) & 1, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1;
+                const uint32_t b = i % C::NBUF, tph = (i / C::NBUF) & 1;
+                if (!mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs) ||
+                    !mbar_wait(&ctl->full[s], ph, kWaitLimitNs) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sw = smem_u32(smem + (size_t)s * C::STAGE_BYTES);
+                const uint64_t adesc = sdesc_kmajor_sw128(sw);
+                const uint64_t bdesc = sdesc_kmajor_sw128(sw + C::W_BYTES);
+                const uint32_t d = tmem_base + b * NT;
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k)
+                    umma_f8f6f4(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC, k > 0 ? 1u : 0u);
+                umma_commit(&ctl->empty[s]);
+                umma_commit(&ctl->tfull[b]);
+            }
+            if (!ok) {
+                record_timeout(status);
+                *abort_flag = 1;
+            }
+            umma_commit(&ctl->mma_done);
+            mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const int cw = ew >> 2;                 // which CPW-wide column slice
+        const int col0 = cw * C::CPW;
+        const int row = q * 32 + lane;          // weight row within the tile
+        const int n = tile * BMW + row;
+        float acc[C::CPW];
+#pragma unroll
+        for (int j = 0; j < C::CPW; ++j) acc[j] = 0.0f;
+        const float* sbp = sb + (size_t)tile * KB;
+        float sw_next = nkb > 0 ? __ldg(sbp + kb_begin) : 0.0f;
+        bool ok = true;
+        for (int i = 0; i < nkb; ++i) {
+            const float swv = sw_next;
+            if (i + 1 < nkb) sw_next = __ldg(sbp + kb_begin + i + 1);
+            const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1;
+            const uint32_t b = i % C::NBUF, tph = (i / C::NBUF) & 1;
+            bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs) && mbar_wait(&ctl->full[s], ph, kWaitLimitNs) &&
+                       !*abort_flag;
+            got = __all_sync(0xFFFFFFFFu, got);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const float* s_sa = reinterpret_cast<const float*>(smem + (size_t)s * C::STAGE_BYTES + C::W_BYTES + C::A_BYTES);
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * NT + col0;
+#pragma unroll
+            for (int cc = 0; cc < C::CPW / C::CHUNK; ++cc) {
+                uint32_t v[C::CHUNK];
+                tmem_ld_chunk<C::CHUNK>(taddr + cc * C::CHUNK, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < C::CHUNK; ++j) {
+                    const float sc = s_sa[col0 + cc * C::CHUNK + j] * swv;
+                    acc[cc * C::CHUNK + j] = fmaf(__uint_as_float(v[j]), sc, acc[cc * C::CHUNK + j]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ctl->tempty[b]);
+                mbar_arrive(&ctl->empty[s]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) {
+                record_timeout(status);
+                *abort_flag = 1;
+            }
+        } else if (splits == 1) {
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < C::CPW; ++j) {
+                    const int m = col0 + j;
+                    if (m < M) c[(size_t)m * ldc + n] = f32_to_bf16_rn(acc[j]);
+                }
+            }
+        } else {
+            // Partials: ws layout [tickets: NB int32, padded to 256 B]
+            //                     [splits][NB][NT][128] fp32 (row fastest, coalesced).
+            int32_t* tickets = reinterpret_cast<int32_t*>(ws);
+            float* part = reinterpret_cast<float*>(ws + (((size_t)NB * 4 + 255) & ~size_t(255)));
+            float* mine = part + (((size_t)split * NB + tile) * NT) * BMW;
+#pragma unroll
+            for (int j = 0; j < C::CPW; ++j) mine[(size_t)(col0 + j) * BMW + row] = acc[j];
+            __threadfence();
+            named_bar_sync(1, 32 * C::EPI_WARPS);
+            if (ew == 0 && lane == 0) {
+                const int prev = atomicAdd(&tickets[tile], 1);
+                ctl->last = (prev == splits - 1);
+            }
+            named_bar_sync(1, 32 * C::EPI_WARPS);
+            if (ctl->last) {
+                __threadfence();
+                if (n < N) {
+#pragma unroll 4
+                    for (int j = 0; j < C::CPW; ++j) {
+                        const int m = col0 + j;
+                        if (m >= M) break;
+                        float sum = 0.0f;
+                        for (int sp = 0; sp < splits; ++sp)
+                            sum += __ldcg(part + (((size_t)sp * NB + tile) * NT + m) * BMW + row);
+                        c[(size_t)m * ldc + n] = f32_to_bf16_rn(sum);
+                    }
+                }
+                if (ew == 0 && lane == 0) tickets[tile] = 0;   // leave the ticket zero for the next call
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int NT>
+cudaError_t launch_nt(const GemmArgs& a, cudaStream_t st) {
+    using C = Cfg<NT>;
+    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done_mask & (1 << (dev & 31)))) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_skinny<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem_bytes<NT>());
+        if (e != cudaSuccess) return e;
+        attr_done_mask |= 1 << (dev & 31);
+    }
+    dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits);
+    k_gemm_skinny<NT><<<grid, C::THREADS, smem_bytes<NT>(), st>>>(
+        *a.tm_b, *a.tm_a, *a.tm_sa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
+        a.splits, static_cast<uint8_t*>(a.workspace), a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace skinny
+
+int skinny_tile_n(int64_t M) {
+    if (M <= 16) return 16;
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
+    if (M <= 128) return 128;
+    if (M <= 256) return 256;
+    return 0;
+}
+
+int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count) {
+    (void)M;
+    const int64_t tiles = N / 128, KB = K / 128;
+    int64_t s = sm_count / (tiles > 0 ? tiles : 1);
+    if (s > KB / 2) s = KB / 2;     // at least two K-blocks per split
+    if (s > 32) s = 32;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+size_t skinny_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
+    (void)K;
+    const int nt = skinny_tile_n(M);
+    if (nt == 0 || splits <= 1) return 0;
+    const int64_t NB = N / 128;
+    return (((size_t)NB * 4 + 255) & ~size_t(255)) + (size_t)splits * NB * nt * 128 * sizeof(float);
+}
+
+cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
+    if (a.M == 0) return cudaSuccess;
+    switch (skinny_tile_n(a.M)) {
+        case 16: return skinny::launch_nt<16>(a, st);
+        case 32: return skinny::launch_nt<32>(a, st);
+        case 64: return skinny::launch_nt<64>(a, st);
+        case 128: return skinny::launch_nt<128>(a, st);
+        case 256: return skinny::launch_nt<256>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fp8bs

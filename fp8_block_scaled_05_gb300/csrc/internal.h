@@ -1,0 +1,61 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+// Upper bound on any single wait inside a kernel before it records a timeout
+// and returns (nanoseconds of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Codes written to the per-device status word (same values as fp8_status).
+constexpr int kStatusTimeout = 8;
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int* status = nullptr;          // device address of the status word
+};
+
+// ------------------------------------------------------------- quantisers
+cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                   float* s, int64_t lds, bool pow2, cudaStream_t st);
+cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                        int64_t ldq, float* s, bool pow2, cudaStream_t st);
+
+// ------------------------------------------------------------- GEMMs
+struct GemmArgs {
+    const CUtensorMap* tm_a;        // qa [rows, K] uint8, box {128, 128}, 128B swizzle
+    const CUtensorMap* tm_b;        // qb [rows, K] uint8, box {128, BN}, 128B swizzle
+    const CUtensorMap* tm_sa;       // sa [KB, ldsa] fp32 (skinny / MX paths only)
+    const float* sa;
+    int64_t ldsa;
+    const float* sb;
+    void* c;
+    int64_t ldc;
+    int64_t M, N, K;
+    const int32_t* offsets;         // grouped: [G+1] on device; nullptr for dense
+    int32_t G;
+    void* workspace;
+    size_t ws_bytes;
+    int32_t splits;
+    int* status;
+    int sm_count;
+};
+
+// Dense / grouped kernel with per-K-block fp32 promotion (tcgen05, TMEM).
+constexpr int kPromoteBN = 256;
+cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st);
+
+// Skinny (decode) kernel: weights on the MMA's M side, tokens on N, split-K.
+int skinny_tile_n(int64_t M);                         // padded token count, 0 if M > 256
+int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count);
+size_t skinny_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
+cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
+
+}  // namespace fp8bs

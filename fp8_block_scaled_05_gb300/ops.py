@@ -1,0 +1,258 @@
+"""ctypes binding of libfp8bs.so (include/fp8bs.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library.  Functions named like the C entry points take torch
+CUDA tensors (PyTorch supplies device memory and streams) and raise
+``FP8Error`` on any non-OK status.  ``quant_act``, ``quant_weight``, ``gemm``,
+``grouped_gemm`` and ``linear`` are conveniences that allocate their outputs
+with torch and then make the same calls.
+
+There is no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+FP8_OK = 0
+STATUS_NAMES = {
+    0: "FP8_OK", 1: "FP8_ERR_NULL", 2: "FP8_ERR_SHAPE", 3: "FP8_ERR_ALIGN", 4: "FP8_ERR_SCALE_MODE",
+    5: "FP8_ERR_WORKSPACE", 6: "FP8_ERR_ARCH", 7: "FP8_ERR_CUDA", 8: "FP8_ERR_TIMEOUT",
+    9: "FP8_ERR_NOT_IMPLEMENTED",
+}
+FP8_SCALE_FP32_AMAX = 0
+FP8_SCALE_POW2 = 1
+FP8_GEMM_SCALES_POW2 = 0x1
+FP8_GEMM_PATH_AUTO = 0x00
+FP8_GEMM_PATH_PROMOTE = 0x10
+FP8_GEMM_PATH_MX = 0x20
+FP8_GEMM_PATH_SKINNY = 0x30
+PATHS = {"auto": FP8_GEMM_PATH_AUTO, "promote": FP8_GEMM_PATH_PROMOTE, "mx": FP8_GEMM_PATH_MX,
+         "skinny": FP8_GEMM_PATH_SKINNY}
+
+# Every function the header declares, with its ctypes signature.
+_i64, _u32, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+SIGNATURES = {
+    "fp8_quant_act_1x128": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, ctypes.c_int, _vp]),
+    "fp8_quant_weight_128x128": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, ctypes.c_int, _vp]),
+    "fp8_blockscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64,
+                                            _u32, _vp, _sz, _vp]),
+    "fp8_blockscaled_grouped_gemm": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64,
+                                                    _i64, _i64, _u32, _vp, _sz, _vp]),
+    "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
+    "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fp8_last_device_status": (ctypes.c_int, [_vp]),
+    "fp8_gemm_plan": (_u32, [_i64, _i64, _i64, _u32, ctypes.POINTER(_i32)]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FP8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once; raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is not built: run `python -m fp8_block_scaled_05_gb300.build` "
+                        "(there is no CPU fallback)")
+                L = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    f = getattr(L, name)
+                    f.restype = res
+                    f.argtypes = args
+                _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().fp8_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - only used for messages
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def _check(status: int, where: str):
+    if status != FP8_OK:
+        raise FP8Error(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name: str, rows_major: bool = True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if rows_major and t.dim() >= 1 and t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride in its last dimension")
+
+
+# ----------------------------------------------------------- C entry points
+def fp8_quant_act_1x128(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, mode: int = FP8_SCALE_FP32_AMAX,
+                        stream=None) -> None:
+    """x bf16 [M, K]; q uint8 [M, K]; s fp32 [K/128, lds] with lds >= M."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    _need(s, torch.float32, "s")
+    M, K = x.shape
+    _check(lib().fp8_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), s.stride(0),
+                                     int(mode), _stream(stream)), "fp8_quant_act_1x128")
+
+
+def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor,
+                             mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
+    """w bf16 [N, K]; q uint8 [N, K]; s fp32 [N/128, K/128] contiguous."""
+    _need(w, torch.bfloat16, "w")
+    _need(q, torch.uint8, "q")
+    _need(s, torch.float32, "s")
+    if not s.is_contiguous():
+        raise ValueError("s must be contiguous")
+    N, K = w.shape
+    _check(lib().fp8_quant_weight_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(s), int(mode),
+                                          _stream(stream)), "fp8_quant_weight_128x128")
+
+
+def fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
+                         stream=None) -> None:
+    """C[M, N] (bf16) = block-scaled qa[M, K] * qb[N, K]^T."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(c, torch.bfloat16, "c")
+    M, K = qa.shape
+    N = qb.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_blockscaled_gemm(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0),
+                                      _ptr(sb), _ptr(c), c.stride(0), M, N, K, int(flags), _ptr(workspace),
+                                      ws_bytes, _stream(stream)), "fp8_blockscaled_gemm")
+
+
+def fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags: int = 0,
+                                 workspace: torch.Tensor | None = None, stream=None) -> None:
+    """Per-expert GEMM; offsets int32 [G+1] on the device; qb uint8 [G, N, K]."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(c, torch.bfloat16, "c")
+    _need(offsets, torch.int32, "offsets")
+    if not (qb.is_contiguous() and sb.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("qb, sb and offsets must be contiguous")
+    M, K = qa.shape
+    G, N = qb.shape[0], qb.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_blockscaled_grouped_gemm(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(offsets), G,
+                                              M, _ptr(qb), _ptr(sb), _ptr(c), c.stride(0), N, K, int(flags),
+                                              _ptr(workspace), ws_bytes, _stream(stream)),
+           "fp8_blockscaled_grouped_gemm")
+
+
+def fp8_gemm_workspace_size(M: int, N: int, K: int, G: int = 1) -> int:
+    return int(lib().fp8_gemm_workspace_size(M, N, K, G))
+
+
+def fp8_gemm_plan(M: int, N: int, K: int, flags: int = 0):
+    sp = ctypes.c_int32(0)
+    path = lib().fp8_gemm_plan(M, N, K, flags, ctypes.byref(sp))
+    return int(path), int(sp.value)
+
+
+def fp8_last_device_status(stream=None) -> int:
+    return int(lib().fp8_last_device_status(_stream(stream)))
+
+
+# ----------------------------------------------------------- conveniences
+def round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+def quant_act(x: torch.Tensor, pow2: bool = False, stream=None):
+    """Returns (q uint8 [M, K], s fp32 [K/128, round_up(M, 4)])."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, max(round_up(M, 4), 4)), dtype=torch.float32, device=x.device)
+    fp8_quant_act_1x128(x, q, s, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return q, s
+
+
+def quant_weight(w: torch.Tensor, pow2: bool = False, stream=None):
+    """Returns (q uint8 [N, K], s fp32 [N/128, K/128])."""
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8_quant_weight_128x128(w, q, s, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return q, s
+
+
+_ws: dict[int, torch.Tensor] = {}
+
+
+def workspace_for(M: int, N: int, K: int, G: int, device) -> torch.Tensor | None:
+    """A zero-initialised workspace of at least the needed size, kept per device."""
+    need = fp8_gemm_workspace_size(M, N, K, G)
+    if need == 0:
+        return None
+    dev = torch.device(device).index or 0
+    ws = _ws.get(dev)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(round_up(need, 1 << 20), dtype=torch.uint8, device=device)
+        _ws[dev] = ws
+    return ws
+
+
+def gemm(qa, sa, qb, sb, pow2: bool = False, path: str = "auto", out: torch.Tensor | None = None, stream=None):
+    """C = block-scaled GEMM of quantised operands; allocates C (bf16 [M, N])
+    and, for the split-K path, a zero-filled workspace kept per device."""
+    M, K = qa.shape
+    N = qb.shape[0]
+    c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    flags = PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0)
+    # For M <= 256 the automatic plan is the split-K one, so the size query
+    # also covers an explicitly requested skinny path.
+    ws = workspace_for(M, N, K, 1, qa.device) if path in ("auto", "skinny") else None
+    fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags, ws, stream)
+    return c
+
+
+def grouped_gemm(qa, sa, offsets, qb, sb, pow2: bool = False, out=None, stream=None):
+    M, K = qa.shape
+    N = qb.shape[1]
+    c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    flags = FP8_GEMM_SCALES_POW2 if pow2 else 0
+    fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags, None, stream)
+    return c
+
+
+def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):
+    """bf16 y = FP8 linear layer: quantise x (1x128) and w (128x128), then the
+    block-scaled GEMM.  Returns (y, (qa, sa), (qw, sw))."""
+    qa, sa = quant_act(x, pow2, stream)
+    qw, sw = quant_weight(w, pow2, stream)
+    return gemm(qa, sa, qw, sw, pow2, stream=stream), (qa, sa), (qw, sw)

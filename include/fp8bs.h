@@ -1,0 +1,196 @@
+/*
+ * fp8bs.h -- C ABI of the GB300 (sm_103a) block-scaled FP8 linear layer.
+ *
+ * The operation (page "NVIDIA NeMo RL достигает ускорения на 48% благодаря
+ * сквозному обучению с точностью FP8", greentreeone.com, §Технический
+ * прорыв): linear layers compute on FP8 E4M3 codes, with activations
+ * quantised in 1x128 blocks and weights in 128x128 blocks, each block
+ * carrying its own scale; attention, normalisation and non-linearities stay
+ * bf16 and are not part of this library.  The scale is recomputed from the
+ * block's current amax on every call because the policy's weights change
+ * after each optimizer step (upppp.jp NeMo RL FP8 article,
+ * §KVキャッシュとAttentionにも拡張).  A power-of-two scale option exists
+ * (upppp.jp article, §設定方法).  Accumulation is kept in higher precision
+ * than the FP8 operands (ai.warp-studio.com end-to-end FP8 RL article,
+ * §FP8強化学習における精度と安定性の確保).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" must be device (or managed) memory of the
+ *    current CUDA device; the caller owns every buffer, the library never
+ *    frees or keeps them.  Sizes and leading dimensions are in ELEMENTS.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  A returned FP8_OK means "validated and
+ *    enqueued", not "finished".
+ *  - Arguments are validated on the host before anything touches the GPU:
+ *    a call that returns an error has enqueued nothing.
+ *  - Kernels never trap.  Every wait inside a kernel has a time limit; a
+ *    wait that runs out records FP8_ERR_TIMEOUT in a per-device status word
+ *    (read it with fp8_last_device_status) and the kernel returns.
+ *  - Non-finite inputs (NaN, Inf) are outside the contract: the calls run,
+ *    the codes they produce are unspecified.
+ *  - E4M3 is the OCP OFP8 "fn" variant: bias 7, no infinities, NaN = S.1111.111,
+ *    largest finite magnitude 448.  Conversion rounds to nearest, ties to
+ *    even, and saturates to +-448.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8BS_API __attribute__((visibility("default")))
+#else
+#define FP8BS_API
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *fp8_stream_t;
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_NULL = 1,            /* a required pointer is NULL */
+    FP8_ERR_SHAPE = 2,           /* sizes out of range, or a leading dimension too small */
+    FP8_ERR_ALIGN = 3,           /* a pointer or a row pitch breaks the 16-byte rule */
+    FP8_ERR_SCALE_MODE = 4,      /* unknown scale mode or flag bits */
+    FP8_ERR_WORKSPACE = 5,       /* workspace missing or smaller than fp8_gemm_workspace_size() */
+    FP8_ERR_ARCH = 6,            /* no CUDA device, or the current device is not sm_103 */
+    FP8_ERR_CUDA = 7,            /* a CUDA runtime/driver call failed (launch, descriptor) */
+    FP8_ERR_TIMEOUT = 8,         /* a kernel wait ran out of time (device status word only) */
+    FP8_ERR_NOT_IMPLEMENTED = 9  /* the requested path is not built */
+} fp8_status;
+
+typedef enum {
+    /* s = RN_fp32(amax / 448); an all-zero block gets s = 1. */
+    FP8_SCALE_FP32_AMAX = 0,
+    /* s = 2^e, e = ceil(log2(amax / 448)) clamped to [-127, 127]; an
+     * all-zero block gets s = 1.  The cast is then an exact multiply. */
+    FP8_SCALE_POW2 = 1
+} fp8_scale_mode;
+
+/* GEMM flags. */
+#define FP8_GEMM_SCALES_POW2   0x1u  /* caller promises every sA, sB is an exact power of two
+                                        in [2^-127, 2^127] (as FP8_SCALE_POW2 produces); lets the
+                                        hardware block-scaled (UE8M0) path run */
+#define FP8_GEMM_PATH_MASK     0xF0u /* kernel selection; 0 = automatic */
+#define FP8_GEMM_PATH_AUTO     0x00u
+#define FP8_GEMM_PATH_PROMOTE  0x10u /* large-M kernel, fp32 scale promotion per K-block */
+#define FP8_GEMM_PATH_MX       0x20u /* large-M kernel, hardware UE8M0 block scaling (needs SCALES_POW2) */
+#define FP8_GEMM_PATH_SKINNY   0x30u /* M <= 256: weights as the MMA's M side, split-K */
+
+/*
+ * 1x128 activation quantisation.
+ *
+ *   for every row m < M and K-block kb < K/128:
+ *     amax      = max_{k in kb} |x[m, k]|
+ *     s[kb, m]  = scale(amax)           (see fp8_scale_mode)
+ *     q[m, k]   = e4m3( RN_fp32(x[m, k] / s[kb, m]) )
+ *
+ * x   device, bf16 [M, K] row-major, row pitch ldx (>= K, ldx % 8 == 0, x 16-byte aligned)
+ * q   device, uint8 E4M3 codes [M, K] row-major, row pitch ldq (>= K, ldq % 16 == 0, 16-byte aligned)
+ * s   device, fp32 [K/128][lds]: the scale of row m, K-block kb is s[kb * lds + m]
+ *     (K-block-major so that a GEMM reads the scales of consecutive rows
+ *     contiguously); lds >= M, lds % 4 == 0, 16-byte aligned.
+ * M >= 0 (M == 0 is a no-op), K > 0 and K % 128 == 0, M * K < 2^40.
+ */
+FP8BS_API fp8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                               fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
+ * 128x128 weight quantisation (run after every optimizer step).
+ *
+ *   for every tile (nb, kb), nb < N/128, kb < K/128:
+ *     amax        = max over the 128x128 tile of |w|
+ *     s[nb, kb]   = scale(amax)
+ *     q[n, k]     = e4m3( RN_fp32(w[n, k] / s[n/128, k/128]) )
+ *
+ * w   device, bf16 [N, K] row-major, row pitch ldw (>= K, ldw % 8 == 0, 16-byte aligned)
+ * q   device, uint8 [N, K] row-major, row pitch ldq (>= K, ldq % 16 == 0, 16-byte aligned)
+ * s   device, fp32 [N/128][K/128] row-major, contiguous, 16-byte aligned
+ * N, K > 0, both multiples of 128.
+ */
+FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                    uint8_t *q, int64_t ldq, float *s,
+                                    fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM, C = A * B^T ("TN": both operands K-major):
+ *
+ *   C[m, n] = bf16_RN( sum_kb  sA[kb, m] * sB[n/128, kb] * P[m, n, kb] ),
+ *   P[m, n, kb] = sum_{k in kb} dec(qa[m, k]) * dec(qb[n, k])
+ *
+ * Each K-block's partial P is accumulated in fp32 by the tensor cores and
+ * promoted into an fp32 running sum with the scale product (or, with
+ * FP8_GEMM_SCALES_POW2 and the MX path, scaled by the hardware).  The order
+ * of the fp32 additions is not specified; results agree with an exact
+ * evaluation to fp32 accumulation error plus bf16 output rounding.
+ *
+ * qa  device, uint8 [M, K], row pitch lda (>= K, % 16 == 0)
+ * sa  device, fp32 [K/128][ldsa] as written by fp8_quant_act_1x128 (ldsa >= M, % 4 == 0)
+ * qb  device, uint8 [N, K], row pitch ldb (>= K, % 16 == 0)
+ * sb  device, fp32 [N/128][K/128] contiguous, as written by fp8_quant_weight_128x128
+ * c   device, bf16 [M, N], row pitch ldc (>= N, % 8 == 0)
+ * M >= 0 (0 is a no-op), N, K > 0 and multiples of 128.  All pointers 16-byte aligned.
+ * flags: FP8_GEMM_SCALES_POW2 | one FP8_GEMM_PATH_* value.
+ * workspace: device scratch of at least fp8_gemm_workspace_size(M, N, K, 1) bytes
+ *     (may be NULL when that size is 0).  Its first bytes hold split-K
+ *     semaphores that must be zero before the first use; every completed
+ *     call leaves them zero again (allocate it zero-filled once and reuse it).
+ *     Calls that share a workspace must not run concurrently.
+ */
+FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                const uint8_t *qb, int64_t ldb, const float *sb,
+                                void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                uint32_t flags, void *workspace, size_t ws_bytes,
+                                fp8_stream_t stream);
+
+/*
+ * Grouped (mixture-of-experts) block-scaled GEMM: for each expert g < G,
+ * rows offsets[g] .. offsets[g+1]-1 of A (tokens sorted by expert) times
+ * expert g's weights:
+ *
+ *   C[m, n] = bf16( sum_kb sA[kb, m] * sB[g][n/128, kb] * P_g[m, n, kb] )
+ *
+ * qa       device, uint8 [M_total, K], row pitch lda;  sa device fp32 [K/128][ldsa]
+ * offsets  device, int32 [G+1], non-decreasing, offsets[0] == 0,
+ *          offsets[G] == M_total.  Read on the device, so no host sync is
+ *          needed; values that break these rules are outside the contract
+ *          (the kernel clamps them to [0, M_total] and never reads or
+ *          writes out of bounds).
+ * qb       device, uint8 [G][N][K] contiguous;  sb device fp32 [G][N/128][K/128] contiguous
+ * c        device, bf16 [M_total, N], row pitch ldc
+ * Empty experts are allowed.  G >= 1, N and K multiples of 128.
+ */
+FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                        const int32_t *offsets, int32_t G, int64_t M_total,
+                                        const uint8_t *qb, const float *sb,
+                                        void *c, int64_t ldc, int64_t N, int64_t K,
+                                        uint32_t flags, void *workspace, size_t ws_bytes,
+                                        fp8_stream_t stream);
+
+/* Bytes of workspace fp8_blockscaled_gemm (G == 1) or
+ * fp8_blockscaled_grouped_gemm (G > 1) needs for these sizes; 0 when none. */
+FP8BS_API size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t G);
+
+/* Static, human-readable name of a status code. */
+FP8BS_API const char *fp8_status_string(fp8_status status);
+
+/* Synchronises `stream`, returns the current device's status word (FP8_OK
+ * or the first error a kernel recorded, e.g. FP8_ERR_TIMEOUT) and clears it. */
+FP8BS_API fp8_status fp8_last_device_status(fp8_stream_t stream);
+
+/* Which kernel fp8_blockscaled_gemm would run for these arguments
+ * (one of the FP8_GEMM_PATH_* values, never AUTO), and, through
+ * `splits` (may be NULL), how many K-splits it would use. */
+FP8BS_API uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t *splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,196 @@
+"""GPU parity of the block-scaled GEMMs (large-M promote kernel, skinny
+split-K kernel, grouped MoE kernel) with the oracle's fp64
+dequantise-then-multiply reference; operands come from the oracle's own
+quantisers on the same seeded inputs, so the GEMM is checked on its own."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8_oracle as O
+from fp8_block_scaled_05_gb300 import inputs as I
+from tests.helpers import assert_gemm_close, bf16_to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from fp8_block_scaled_05_gb300 import build, ops as _ops
+    build.build()
+    return _ops
+
+
+def _to_dev(qa, sa_mk, qw, sw):
+    """Oracle operands -> device tensors in the library's layouts."""
+    M = qa.shape[0]
+    lds = max(4, (M + 3) // 4 * 4)
+    sa_dev = torch.zeros((sa_mk.shape[1], lds), dtype=torch.float32)
+    sa_dev[:, :M] = torch.from_numpy(np.ascontiguousarray(sa_mk.T))
+    return (torch.from_numpy(qa).cuda(), sa_dev.cuda(), torch.from_numpy(qw).cuda(),
+            torch.from_numpy(np.ascontiguousarray(sw)).cuda())
+
+
+def _case(M, N, K, seed, pow2=False, outliers=True):
+    a = I.normal_bf16(I.stream(seed, 1), (M, K))
+    if outliers and K >= 256:
+        a, _ = I.with_outlier_columns(a, I.stream(seed, 2), max(1, K // 100), 30.0)
+    w = I.normal_bf16(I.stream(seed, 3), (N, K), std=0.02)
+    qa, sa = O.quant_act_1x128(bf16_to_np(a), pow2)
+    qw, sw = O.quant_weight_128x128(bf16_to_np(w), pow2)
+    return qa, sa, qw, sw
+
+
+def _run(ops, qa, sa, qw, sw, path, pow2=False):
+    dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
+    c = ops.gemm(dqa, dsa, dqw, dsw, pow2=pow2, path=path)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    return bf16_to_np(c)
+
+
+@pytest.mark.parametrize("path", ["promote", "skinny"])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_tiny(ops, path, pow2):
+    case = I.tiny()
+    qa, sa = O.quant_act_1x128(bf16_to_np(case.a), pow2)
+    qw, sw = O.quant_weight_128x128(bf16_to_np(case.w), pow2)
+    c = _run(ops, qa, sa, qw, sw, path, pow2)
+    assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"tiny/{path}/{pow2}")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 640, 1152), (128, 256, 128), (129, 128, 256), (513, 384, 512),
+                                   (1000, 1280, 384)])
+def test_promote_ragged(ops, M, N, K):
+    qa, sa, qw, sw = _case(M, N, K, seed=M + N)
+    c = _run(ops, qa, sa, qw, sw, "promote")
+    assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"promote {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 8, 16, 17, 33, 64, 100, 128, 200, 256])
+def test_skinny_ragged(ops, M):
+    N, K = 640, 2048
+    qa, sa, qw, sw = _case(M, N, K, seed=M)
+    c = _run(ops, qa, sa, qw, sw, "skinny")
+    assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"skinny M={M}")
+
+
+@pytest.mark.parametrize("path", ["promote", "skinny"])
+def test_exact_integer_gemm(ops, path):
+    """Codes decoding to {-1, 0, 1}, power-of-two scales: every output is an
+    integer times a power of two with |C| <= 256, exact in bf16; the GPU must
+    reproduce it exactly."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    M, N, K = 200, 384, 256
+    lut = np.array([0x00, 0x38, 0xB8], np.uint8)
+    qa = lut[rng.integers(0, 3, (M, K))]
+    qw = lut[rng.integers(0, 3, (N, K))]
+    sa = (2.0 ** rng.integers(-3, 3, (M, K // 128))).astype(np.float32)
+    sw = (2.0 ** rng.integers(-2, 2, (N // 128, K // 128))).astype(np.float32)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    assert np.all(np.abs(ref) <= 256 * 2 ** 5)
+    c = _run(ops, qa, sa, qw, sw, path)
+    assert np.array_equal(c, ref)
+
+
+def test_rejects_bad_arguments(ops):
+    qa = torch.zeros((4, 2048), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((16, 4), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((128, 2048), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((1, 16), dtype=torch.float32, device="cuda")
+    c = torch.empty((4, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ops.FP8Error) as e:
+        ops.fp8_blockscaled_gemm(qa[:, :200], sa, qw[:, :200], sw, c)
+    assert e.value.status == 2
+    with pytest.raises(ops.FP8Error) as e:
+        ops.fp8_blockscaled_gemm(qa, sa, qw, sw, c, flags=ops.FP8_GEMM_PATH_SKINNY, workspace=None)
+    assert e.value.status == 5
+
+
+# ------------------------------------------------------------ full sizes
+@pytest.mark.parametrize("layer", ["qkv", "down"])
+def test_llama_full_size_sampled_rows(ops, layer):
+    """Llama-3.1-8B layer shapes, whole path on the GPU (quantisers + GEMM),
+    checked on sampled output rows against the oracle."""
+    case = I.llama8b_layers(layers=[layer])[0]
+    y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda())
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.Generator(np.random.PCG64(8)).choice(case.a.shape[0], 24, replace=False))
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]))
+    assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
+    qw_o, sw_o = qw.cpu().numpy(), sw.cpu().numpy()
+    ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
+    assert_gemm_close(bf16_to_np(y[rows]), ref, f"llama {layer}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 64, 256])
+def test_decode_full_size(ops, M):
+    K, N = 14336, 4096
+    case = I.decode_case(M, K, N)
+    y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda())
+    torch.cuda.synchronize()
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a))
+    assert np.array_equal(qa.cpu().numpy(), qa_o)
+    ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
+    assert_gemm_close(bf16_to_np(y), ref, f"decode M={M}")
+
+
+# ------------------------------------------------------------ grouped
+def _grouped_inputs(offsets, N, K, seed):
+    G = len(offsets) - 1
+    M = int(offsets[-1])
+    a = I.normal_bf16(I.stream(seed, 1), (M, K))
+    w = I.normal_bf16(I.stream(seed, 2), (G, N, K), std=0.02)
+    qa, sa = O.quant_act_1x128(bf16_to_np(a))
+    qs = [O.quant_weight_128x128(bf16_to_np(w[g])) for g in range(G)]
+    qw = np.stack([q for q, _ in qs])
+    sw = np.stack([s for _, s in qs])
+    return qa, sa, qw, sw
+
+
+def _run_grouped(ops, qa, sa, offsets, qw, sw):
+    dqa, dsa, _, _ = _to_dev(qa, sa, qw[0], sw[0])
+    c = ops.grouped_gemm(dqa, dsa, torch.tensor(offsets, dtype=torch.int32, device="cuda"),
+                         torch.from_numpy(qw).cuda(), torch.from_numpy(sw).cuda())
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    return bf16_to_np(c)
+
+
+@pytest.mark.parametrize("offsets", [[0, 5, 5, 140, 140, 300, 301], [0, 0, 0, 128], [0, 1000],
+                                     [0, 129, 258, 387, 516]])
+def test_grouped_ragged_with_empty_experts(ops, offsets):
+    N, K = 384, 512
+    qa, sa, qw, sw = _grouped_inputs(offsets, N, K, seed=len(offsets))
+    c = _run_grouped(ops, qa, sa, offsets, qw, sw)
+    assert_gemm_close(c, O.grouped_gemm_ref(qa, sa, offsets, qw, sw), f"grouped {offsets}")
+
+
+def test_grouped_moe_full_size_sampled_rows(ops):
+    """Qwen3-30B-A3B-shaped experts (gate+up: K 2048, N 1536), Zipf routing."""
+    m = I.moe_case(with_weights=False)
+    G, N, K = 128, 1536, 2048
+    w = I.normal_bf16(I.stream(0, 82), (G, N, K), std=0.02)
+    x = m.a_gate_up.cuda()
+    qa, sa = ops.quant_act(x)
+    qw = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    wd = w.cuda()
+    for g in range(G):
+        ops.fp8_quant_weight_128x128(wd[g], qw[g], sw[g])
+    offs = torch.from_numpy(m.offsets).cuda()
+    c = ops.grouped_gemm(qa, sa, offs, qw, sw)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    rng = np.random.Generator(np.random.PCG64(9))
+    rows = np.sort(rng.choice(x.shape[0], 32, replace=False))
+    # include the first and last row of a few experts (tile edges)
+    rows = np.unique(np.concatenate([rows, m.offsets[1:6] - 1, m.offsets[:5]]))
+    rows = rows[rows < x.shape[0]]
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_gate_up[rows]))
+    assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
+    grp = np.searchsorted(m.offsets, rows, side="right") - 1
+    qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
+    ref = np.stack([O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], qw_n[g], sw_n[g])[0] for i, g in enumerate(grp)])
+    assert_gemm_close(bf16_to_np(c[rows]), ref, "moe gate_up")
