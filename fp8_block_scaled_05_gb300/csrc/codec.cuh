@@ -90,6 +90,23 @@ __device__ __forceinline__ BlockScale make_scale(float amax, bool pow2) {
     return bs;
 }
 
+// The per-block constants from a stored scale s and its reciprocal factor r
+// (as make_scale produced them); lets one lane compute a block's scale and
+// others rebuild it from two shuffled values.
+__device__ __forceinline__ BlockScale scale_from_sr(float s, float r, bool pow2) {
+    BlockScale bs;
+    bs.s = s;
+    bs.r = r;
+    bs.mode = pow2 ? 1 : ((__float_as_uint(s) >= (uint32_t)(127 - 90) << 23) ? 0 : 2);
+    return bs;
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // RN_fp32(x / s).
 //
 // mode 0 uses a hoisted correctly rounded reciprocal r = RN(1/s) and two
@@ -101,7 +118,9 @@ __device__ __forceinline__ BlockScale make_scale(float amax, bool pow2) {
 //                                     and the theorem gives q2 = RN(x/s)
 // valid while no remainder underflows: |x/s| >= 2^-11 matters for the E4M3
 // code and s >= 2^-90 keeps x - s q a multiple of 2^-149; quotients below
-// 2^-11 round to a signed zero code either way.
+// 2^-11 round to a signed zero code either way.  The corrections can turn a
+// zero quotient's sign positive ((+0) + (-0) = +0 under round-to-nearest), so
+// the sign of x is put back: RN(x/s) always carries the sign of x.
 __device__ __forceinline__ float quotient_rn(float x, const BlockScale &bs) {
     if (bs.mode == 1) return x * bs.r;
     if (bs.mode == 2) return __fdiv_rn(x, bs.s);
@@ -109,7 +128,7 @@ __device__ __forceinline__ float quotient_rn(float x, const BlockScale &bs) {
     float rem = fmaf(-bs.s, q, x);
     q = fmaf(rem, bs.r, q);
     rem = fmaf(-bs.s, q, x);
-    return fmaf(rem, bs.r, q);
+    return copysignf(fmaf(rem, bs.r, q), x);
 }
 
 // Two fp32 values to two E4M3 codes (round to nearest even, saturating to

@@ -22,13 +22,19 @@ namespace fp8bs {
 // ---------------------------------------------------------------------------
 // 1x128 activations.  CTA tile: 32 rows x 8 K-blocks.  Warp w owns rows
 // 4w..4w+3; a warp-wide 512-byte load covers two adjacent K-blocks of one
-// row, half-warp h handling K-block 2p+h.  Scales are gathered in shared
-// memory and written K-block-major (32 consecutive rows per 128-byte store).
+// row, half-warp h handling K-block 2p+h.  A warp therefore holds 32 blocks
+// (16 "items" i = 4r+p per half).  Their amax values are reduced with a
+// butterfly reduce-scatter over each half (15 shuffles instead of 64), after
+// which lane 16h+i holds the amax of item i of half h and computes that one
+// block's scale; the other lanes fetch (s, 1/s) with two shuffles per item.
+// Scales are gathered in shared memory and written K-block-major (32
+// consecutive rows per 128-byte store).
 // ---------------------------------------------------------------------------
 constexpr int kActRows = 32;
 constexpr int kActKB = 8;
 constexpr int kActRowsPerWarp = 4;
 constexpr int kActPairs = kActKB / 2;
+constexpr int kActItems = kActRowsPerWarp * kActPairs;   // 16 blocks per half-warp
 
 __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
                                                          int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
@@ -38,37 +44,51 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
     const int64_t m0 = (int64_t)blockIdx.y * kActRows;
     const int64_t kb0 = (int64_t)blockIdx.x * kActKB;
 
-    uint4 v[kActRowsPerWarp][kActPairs];
+    uint4 v[kActItems];
 #pragma unroll
-    for (int r = 0; r < kActRowsPerWarp; ++r) {
+    for (int i = 0; i < kActItems; ++i) {
+        const int r = i / kActPairs, p = i % kActPairs;
         const int64_t m = m0 + warp * kActRowsPerWarp + r;
+        const int64_t kb = kb0 + 2 * p + half;
+        if (m < M && kb < KB)
+            v[i] = __ldcs(reinterpret_cast<const uint4*>(x + m * ldx + kb * 128 + l16 * 8));
+        else
+            v[i] = make_uint4(0, 0, 0, 0);
+    }
+
+    // Butterfly reduce-scatter: after the step with offset o, a lane keeps the
+    // items whose index bit o matches its own lane bit o.
+    uint32_t a[kActItems];
 #pragma unroll
-        for (int p = 0; p < kActPairs; ++p) {
-            const int64_t kb = kb0 + 2 * p + half;
-            if (m < M && kb < KB) {
-                const uint16_t* src = x + m * ldx + kb * 128 + l16 * 8;
-                v[r][p] = __ldcs(reinterpret_cast<const uint4*>(src));
-            } else {
-                v[r][p] = make_uint4(0, 0, 0, 0);
-            }
+    for (int i = 0; i < kActItems; ++i) a[i] = absmax8(0u, v[i]);
+#pragma unroll
+    for (int o = kActItems / 2; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const uint32_t send = upper ? a[j] : a[j + o];
+            const uint32_t keep = upper ? a[j + o] : a[j];
+            a[j] = max_u16x2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
         }
     }
-#pragma unroll
-    for (int r = 0; r < kActRowsPerWarp; ++r) {
+    // this lane's block: item l16 of half `half`
+    const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), pow2 != 0);
+    {
+        const int r = l16 / kActPairs, p = l16 % kActPairs;
         const int rl = warp * kActRowsPerWarp + r;
-        const int64_t m = m0 + rl;
+        if (m0 + rl < M && kb0 + 2 * p + half < KB) s_tile[2 * p + half][rl] = own.s;
+    }
 #pragma unroll
-        for (int p = 0; p < kActPairs; ++p) {
-            const int64_t kb = kb0 + 2 * p + half;
-            float amax = absmax_pair_to_f32(absmax8(0u, v[r][p]));
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            const BlockScale bs = make_scale(amax, pow2 != 0);
-            if (m < M && kb < KB) {
-                const uint2 c = quant8(v[r][p], bs);
-                __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8), c);
-                if (l16 == 0) s_tile[2 * p + half][rl] = bs.s;
-            }
+    for (int i = 0; i < kActItems; ++i) {
+        const int r = i / kActPairs, p = i % kActPairs;
+        const int src = (lane & 16) | i;
+        const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
+        const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
+        const int64_t m = m0 + warp * kActRowsPerWarp + r;
+        const int64_t kb = kb0 + 2 * p + half;
+        if (m < M && kb < KB) {
+            const uint2 c = quant8(v[i], scale_from_sr(si, ri, pow2 != 0));
+            __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8), c);
         }
     }
     __syncthreads();

@@ -1,0 +1,100 @@
+"""Per-kernel micro-benchmark of the library.
+
+Runs one entry point on one shape, `--warmup` times untimed and `--iters`
+times timed with CUDA events on the launching stream (L2 flushed before each
+timed launch unless --no-flush), and prints one JSON line with the mean time
+and the achieved rate (algorithmic bytes or FLOPs).  Also the command used for
+ncu captures of a single kernel.
+
+  python -m fp8_block_scaled_05_gb300.kbench --kernel gemm --M 4096 --N 28672 --K 4096
+  python -m fp8_block_scaled_05_gb300.kbench --kernel quant_act --M 4096 --K 14336
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import build as _build
+from . import ops
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--kernel", required=True, choices=["quant_act", "quant_weight", "gemm", "grouped"])
+    p.add_argument("--M", type=int, default=4096)
+    p.add_argument("--N", type=int, default=4096)
+    p.add_argument("--K", type=int, default=4096)
+    p.add_argument("--G", type=int, default=128, help="experts (grouped)")
+    p.add_argument("--pow2", action="store_true")
+    p.add_argument("--path", default="auto", choices=list(ops.PATHS))
+    p.add_argument("--iters", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--no-flush", action="store_true")
+    a = p.parse_args(argv)
+
+    _build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    M, N, K = a.M, a.N, a.K
+    mode = ops.FP8_SCALE_POW2 if a.pow2 else ops.FP8_SCALE_FP32_AMAX
+    flush = None if a.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    if a.kernel == "quant_act":
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev)
+        run = lambda: ops.fp8_quant_act_1x128(x, q, s, mode)  # noqa: E731
+        work, unit = 3.0 * M * K + 4.0 * M * (K // 128), "GB/s"
+    elif a.kernel == "quant_weight":
+        w = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+        run = lambda: ops.fp8_quant_weight_128x128(w, q, s, mode)  # noqa: E731
+        work, unit = 3.0 * N * K + 4.0 * (N // 128) * (K // 128), "GB/s"
+    elif a.kernel == "gemm":
+        qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
+        qw, sw = ops.quant_weight((torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16), a.pow2)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda: ops.gemm(qa, sa, qw, sw, a.pow2, a.path, out=c)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    else:
+        G = a.G
+        sizes = torch.full((G,), M // G, dtype=torch.int64)
+        sizes[: M - int(sizes.sum())] += 1
+        offs = torch.zeros(G + 1, dtype=torch.int32)
+        offs[1:] = torch.cumsum(sizes, 0)
+        offs = offs.to(dev)
+        qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
+        qw = torch.randint(0, 0x7E, (G, N, K), dtype=torch.uint8, device=dev, generator=g)
+        sw = torch.rand((G, N // 128, K // 128), generator=g, device=dev) * 1e-3
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda: ops.grouped_gemm(qa, sa, offs, qw, sw, a.pow2, out=c)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+
+    for _ in range(a.warmup):
+        run()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(a.iters):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    st = ops.fp8_last_device_status()
+    ms = sum(times) / len(times)
+    rate = work / (ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
+    plan = ops.fp8_gemm_plan(M, N, K, ops.PATHS[a.path]) if a.kernel == "gemm" else None
+    print(json.dumps({"kernel": a.kernel, "M": M, "N": N, "K": K, "pow2": a.pow2, "path": a.path, "plan": plan,
+                      "ms": ms, "min_ms": min(times), unit: rate, "status": st}))
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

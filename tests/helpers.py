@@ -80,16 +80,15 @@ def planted_rows(amaxes: np.ndarray, block: int, per_row_blocks: int, seed: int 
         vals = f[np.abs(f) <= a]
         vals = vals[rng.permutation(vals.size)]
         n = block - 1
-        pad = (-vals.size) % n
-        if pad:
-            vals = np.concatenate([vals, vals[:pad]])
+        # repeat cyclically up to a whole number of blocks (small amax values
+        # have fewer candidates than one block holds)
+        vals = np.resize(vals, ((vals.size + n - 1) // n) * n)
         chunks = vals.reshape(-1, n)
         amax_col = np.where(rng.integers(0, 2, (chunks.shape[0], 1)) == 1, a, -a).astype(np.float32)
         blk = np.concatenate([amax_col, chunks], axis=1)
         idx = np.argsort(rng.random(blk.shape), axis=1)
         blocks.append(np.take_along_axis(blk, idx, axis=1))
     allb = np.concatenate(blocks, axis=0)
-    pad = (-allb.shape[0]) % per_row_blocks
-    if pad:
-        allb = np.concatenate([allb, allb[:pad]], axis=0)
+    allb = np.resize(allb, (((allb.shape[0] + per_row_blocks - 1) // per_row_blocks) * per_row_blocks,
+                            allb.shape[1]))
     return allb.reshape(-1, per_row_blocks * block).astype(np.float32)

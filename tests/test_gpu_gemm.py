@@ -78,18 +78,20 @@ def test_skinny_ragged(ops, M):
 
 @pytest.mark.parametrize("path", ["promote", "skinny"])
 def test_exact_integer_gemm(ops, path):
-    """Codes decoding to {-1, 0, 1}, power-of-two scales: every output is an
-    integer times a power of two with |C| <= 256, exact in bf16; the GPU must
-    reproduce it exactly."""
+    """Codes decoding to {-1, 0, 1}, K = 256, and a power-of-two scale that is
+    the same for both K-blocks of a row (and of a weight tile row): every
+    output is an integer in [-256, 256] (at most 8 significant bits) times a
+    power of two, exact in bf16; the GPU must reproduce it exactly."""
     rng = np.random.Generator(np.random.PCG64(31))
     M, N, K = 200, 384, 256
     lut = np.array([0x00, 0x38, 0xB8], np.uint8)
     qa = lut[rng.integers(0, 3, (M, K))]
     qw = lut[rng.integers(0, 3, (N, K))]
-    sa = (2.0 ** rng.integers(-3, 3, (M, K // 128))).astype(np.float32)
-    sw = (2.0 ** rng.integers(-2, 2, (N // 128, K // 128))).astype(np.float32)
+    sa = np.repeat(2.0 ** rng.integers(-3, 3, (M, 1)), K // 128, axis=1).astype(np.float32)
+    sw = np.repeat(2.0 ** rng.integers(-2, 2, (N // 128, 1)), K // 128, axis=1).astype(np.float32)
     ref = O.gemm_ref(qa, sa, qw, sw)
-    assert np.all(np.abs(ref) <= 256 * 2 ** 5)
+    ints = ref / (sa[:, :1].astype(np.float64) * np.repeat(sw[:, 0], 128)[None, :])
+    assert np.array_equal(ints, np.round(ints)) and np.all(np.abs(ints) <= 256)
     c = _run(ops, qa, sa, qw, sw, path)
     assert np.array_equal(c, ref)
 
