@@ -12,18 +12,25 @@
 // FP8 article, §まとめ; greentreeone.com page, §Реальные прирост
 // производительности, Qwen3-30B).
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x 256):
+// Design (one CTA per SM, persistent over output tiles of 128 x 256; three
+// warpgroups):
 //   warp 0      TMA producer: qa tile 128x128 and qb tile 256x128 per K-block
 //               into a 4-stage shared-memory ring (128-byte swizzle).
 //   warp 1      TMEM owner and MMA issuer: for every K-block, four
 //               tcgen05.mma (M=128, N=256, K=32) into one of two 256-column
 //               TMEM buffers, the first with accumulate = 0.
-//   warps 2..9  promotion: each K-block's fp32 partial is read from TMEM
+//   warps 4..11 promotion: each K-block's fp32 partial is read from TMEM
 //               (tcgen05.ld) and added into registers with the scale product
-//               sA*sB; the buffer is handed back right after the read, so the
-//               tensor core works on K-block kb+1 while kb is being promoted.
-//               Warp w owns TMEM lanes 32*(w%4).. and one 128-column half,
-//               i.e. one nb block with a single sB per K-block.
+//               sA*sB; the buffer is handed back right after the last read,
+//               so the tensor core works on K-block kb+1 while kb is being
+//               promoted.  Warp w owns TMEM lanes 32*(w%4).. and one
+//               128-column half, i.e. one nb block with a single sB per
+//               K-block.  The four 32-column reads of a K-block are pipelined
+//               with the FMAs of the previous chunk.
+//   Registers: the first warpgroup (producer, MMA, two idle warps) gives its
+//   registers to the two promotion warpgroups (setmaxnreg 40 / 232, summing
+//   to the 168 per thread the CTA is launched with), which hold 128 fp32
+//   accumulators plus two 32-column staging chunks per thread.
 // Every wait is bounded; a wait that runs out records a timeout in the status
 // word and the kernel unwinds (waiting, bounded, for its own copies and MMAs).
 #include <cstdint>
@@ -41,8 +48,13 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;
 constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARP0 = 4;                 // first promotion warp (warpgroups 1 and 2)
+constexpr int LAUNCH_REGS = 168;             // per thread at launch: 65536 / 384, rounded to 8
+constexpr int REGS_CTRL = 40;                // warpgroup 0 after setmaxnreg.dec
+constexpr int REGS_EPI = 232;                // warpgroups 1, 2 after setmaxnreg.inc
+static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * LAUNCH_REGS, "register split exceeds the launch");
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
@@ -176,6 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_tiles = ctl->n_tiles;
     volatile int32_t* abort_flag = &ctl->abort_flag;
 
+    if (warp < EPI_WARP0) regs_dealloc<REGS_CTRL>();
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -240,10 +253,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------ promotion epilogue
+        regs_alloc<REGS_EPI>();
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;          // 128-column half of the 256-wide tile
+        const int h = (warp - EPI_WARP0) >> 2;  // 128-column half of the 256-wide tile
         const int row_in_tile = q * 32 + lane;
         const int NB = N / 128;
         uint32_t kbg = 0;
@@ -255,16 +269,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nb = tl.n0 / 128 + h;
             const bool vcol = nb < NB;
             const float* sbp = sb + ((size_t)tl.g * NB + (vcol ? nb : 0)) * KB;
-            float acc[128];
+            const float* sap = sa + m;
+            float acc[4][32];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-            float sa_n = vrow ? __ldg(sa + m) : 0.0f;
-            float sb_n = vcol ? __ldg(sbp) : 0.0f;
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[cc][j] = 0.0f;
+            // scales prefetched two K-blocks ahead
+            float sa0 = vrow ? __ldg(sap) : 0.0f, sb0 = vcol ? __ldg(sbp) : 0.0f;
+            float sa1 = (vrow && KB > 1) ? __ldg(sap + ldsa) : 0.0f, sb1 = (vcol && KB > 1) ? __ldg(sbp + 1) : 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++kbg) {
-                const float sc = sa_n * sb_n;
-                if (kb + 1 < KB) {
-                    sa_n = vrow ? __ldg(sa + (size_t)(kb + 1) * ldsa + m) : 0.0f;
-                    sb_n = vcol ? __ldg(sbp + kb + 1) : 0.0f;
+                const float sc = sa0 * sb0;
+                sa0 = sa1;
+                sb0 = sb1;
+                if (kb + 2 < KB) {
+                    sa1 = vrow ? __ldg(sap + (size_t)(kb + 2) * ldsa) : 0.0f;
+                    sb1 = vcol ? __ldg(sbp + kb + 2) : 0.0f;
                 }
                 const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
                 bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs) && !*abort_flag;
@@ -275,19 +295,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
+                uint32_t v0[32], v1[32];
+                tmem_ld_x32(taddr, v0);
+                tmem_ld_wait();
+                tmem_ld_x32(taddr + 32, v1);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t v[16];
-                    tmem_ld_x16(taddr + cc * 16, v);
-                    tmem_ld_wait();
-                    if (cc == 7) {
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->tempty[b]);
-                    }
+                for (int j = 0; j < 32; ++j) acc[0][j] = fmaf(__uint_as_float(v0[j]), sc, acc[0][j]);
+                tmem_ld_wait_after(acc[0]);
+                tmem_ld_x32(taddr + 64, v0);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[cc * 16 + j] = fmaf(__uint_as_float(v[j]), sc, acc[cc * 16 + j]);
-                }
+                for (int j = 0; j < 32; ++j) acc[1][j] = fmaf(__uint_as_float(v1[j]), sc, acc[1][j]);
+                tmem_ld_wait_after(acc[1]);
+                tmem_ld_x32(taddr + 96, v1);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[2][j] = fmaf(__uint_as_float(v0[j]), sc, acc[2][j]);
+                tmem_ld_wait_after(acc[2]);
+                // all four chunks are in registers: hand the buffer back
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[3][j] = fmaf(__uint_as_float(v1[j]), sc, acc[3][j]);
             }
             if (!ok) break;
             if (vrow && vcol) {
@@ -297,7 +325,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t p[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float lo = acc[j * 8 + 2 * e], hi = acc[j * 8 + 2 * e + 1];
+                        const int col = j * 8 + 2 * e;
+                        const float lo = acc[col >> 5][col & 31], hi = acc[(col + 1) >> 5][(col + 1) & 31];
                         uint32_t r;
                         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
                         p[e] = r;
@@ -333,7 +362,13 @@ cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done_mask[grouped] & (1 << (dev & 31)))) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        // The setmaxnreg split is only safe if the CTA really starts with
+        // LAUNCH_REGS registers per thread; refuse to launch otherwise.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done_mask[grouped] |= 1 << (dev & 31);
     }

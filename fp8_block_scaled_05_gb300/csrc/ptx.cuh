@@ -230,6 +230,33 @@ __host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, uint32_t sfa_
            | (sfa_id << 29);                  // [29,31) A scale-factor byte id
 }
 
+// Waits for this thread's outstanding tcgen05.ld and, through the "+f"
+// operands, makes the 32 given accumulators inputs of the wait: the compiler
+// must finish the arithmetic that produces them before it, so that work
+// overlaps the load in flight instead of queueing behind its completion.
+__device__ __forceinline__ void tmem_ld_wait_after(float (&a)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]), "+f"(a[7]),
+                   "+f"(a[8]), "+f"(a[9]), "+f"(a[10]), "+f"(a[11]), "+f"(a[12]), "+f"(a[13]), "+f"(a[14]),
+                   "+f"(a[15]), "+f"(a[16]), "+f"(a[17]), "+f"(a[18]), "+f"(a[19]), "+f"(a[20]), "+f"(a[21]),
+                   "+f"(a[22]), "+f"(a[23]), "+f"(a[24]), "+f"(a[25]), "+f"(a[26]), "+f"(a[27]), "+f"(a[28]),
+                   "+f"(a[29]), "+f"(a[30]), "+f"(a[31])
+                 :
+                 : "memory");
+}
+
+// Per-warpgroup register reallocation (all four warps of the warpgroup
+// execute it).  The sum over warpgroups must stay within the registers the
+// CTA was launched with.
+template <int N>
+__device__ __forceinline__ void regs_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ----------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }

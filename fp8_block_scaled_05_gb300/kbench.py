@@ -2,8 +2,10 @@
 
 Runs one entry point on one shape, `--warmup` times untimed and `--iters`
 times timed with CUDA events on the launching stream (L2 flushed before each
-timed launch unless --no-flush), and prints one JSON line with the mean time
-and the achieved rate (algorithmic bytes or FLOPs).  Also the command used for
+timed launch unless --no-flush; all iterations are enqueued before one
+synchronize so host launch overhead does not land inside the event pairs),
+and prints one JSON line with the mean time and the achieved rate
+(algorithmic bytes or FLOPs).  Also the command used for
 ncu captures of a single kernel.
 
   python -m fp8_block_scaled_05_gb300.kbench --kernel gemm --M 4096 --N 28672 --K 4096
@@ -77,16 +79,18 @@ def main(argv=None):
     for _ in range(a.warmup):
         run()
     torch.cuda.synchronize()
-    times = []
-    for _ in range(a.iters):
+    # Enqueue every iteration before waiting once, so that the host's launch
+    # overhead overlaps the GPU work (the flush takes longer than one launch)
+    # and each event pair brackets only the kernel.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.iters)]
+    for e0, e1 in evs:
         if flush is not None:
             flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         run()
         e1.record()
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    times = [e0.elapsed_time(e1) for e0, e1 in evs]
     st = ops.fp8_last_device_status()
     ms = sum(times) / len(times)
     rate = work / (ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
