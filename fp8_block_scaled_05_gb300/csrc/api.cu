@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -130,10 +131,10 @@ fp8_status check_mode(int mode) { return (mode == FP8_SCALE_FP32_AMAX || mode ==
 
 constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_MASK;
 
-uint32_t plan_path(int64_t M, uint32_t flags) {
+uint32_t plan_path(int64_t M, int64_t K, uint32_t flags) {
     const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
     if (forced != FP8_GEMM_PATH_AUTO) return forced;
-    if (M <= 256) return FP8_GEMM_PATH_SKINNY;
+    if (M <= 256 && K <= 128 * 1024) return FP8_GEMM_PATH_SKINNY;
     return FP8_GEMM_PATH_PROMOTE;
 }
 
@@ -156,6 +157,25 @@ fp8_status check_gemm_common(const void* qa, int64_t lda, const float* sa, int64
 }
 
 }  // namespace
+
+// Tile width of the promote kernel.  128 gives four TMEM accumulator buffers
+// (more slack between the tensor core and the promotion warps), 256 halves
+// the operand traffic per FLOP.  FP8BS_PROMOTE_BN=128|256 overrides the
+// choice (for tuning).
+int promote_tile_n(int64_t M, int64_t N, int64_t K, int32_t G) {
+    (void)M;
+    (void)K;
+    (void)G;
+    static int forced = [] {
+        const char* e = std::getenv("FP8BS_PROMOTE_BN");
+        if (!e) return 0;
+        const int v = std::atoi(e);
+        return (v == 128 || v == 256) ? v : 0;
+    }();
+    if (forced) return forced;
+    return (N % 256 == 0) ? 256 : 128;
+}
+
 }  // namespace fp8bs
 
 using namespace fp8bs;
@@ -206,7 +226,7 @@ fp8_status fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t
 }
 
 uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t* splits) {
-    const uint32_t path = plan_path(M, flags);
+    const uint32_t path = plan_path(M, K, flags);
     int32_t sp = 1;
     if (path == FP8_GEMM_PATH_SKINNY) {
         int sms = 152;
@@ -233,9 +253,9 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     if (M == 0) return FP8_OK;
     if (ldb < K) return FP8_ERR_SHAPE;
     if (ldb % 16) return FP8_ERR_ALIGN;
-    const uint32_t path = plan_path(M, flags);
+    const uint32_t path = plan_path(M, K, flags);
     if (path == FP8_GEMM_PATH_MX) return FP8_ERR_NOT_IMPLEMENTED;
-    if (path == FP8_GEMM_PATH_SKINNY && M > 256) return FP8_ERR_SHAPE;
+    if (path == FP8_GEMM_PATH_SKINNY && (M > 256 || K / 128 > 1024)) return FP8_ERR_SHAPE;
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
 
@@ -273,10 +293,11 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
             return e;
         return cuda_status(launch_gemm_skinny(a, st));
     }
+    a.bn = promote_tile_n(M, N, K, 1);
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, kPromoteBN,
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
     return cuda_status(launch_gemm_promote(a, st));
@@ -311,10 +332,11 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.status = d->status;
     a.sm_count = d->sm_count;
     a.splits = 1;
+    a.bn = promote_tile_n(M_total, N, K, G);
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M_total, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, (uint64_t)G * N, K, 128, kPromoteBN,
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, (uint64_t)G * N, K, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
     return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -12,25 +12,30 @@
 // FP8 article, §まとめ; greentreeone.com page, §Реальные прирост
 // производительности, Qwen3-30B).
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x 256; three
-// warpgroups):
-//   warp 0      TMA producer: qa tile 128x128 and qb tile 256x128 per K-block
-//               into a 4-stage shared-memory ring (128-byte swizzle).
-//   warp 1      TMEM owner and MMA issuer: for every K-block, four
-//               tcgen05.mma (M=128, N=256, K=32) into one of two 256-column
-//               TMEM buffers, the first with accumulate = 0.
-//   warps 4..11 promotion: each K-block's fp32 partial is read from TMEM
+// Design (one CTA per SM, persistent over output tiles of 128 x BN, BN = 128
+// or 256):
+//   warp 0      TMA producer: qa tile 128x128 and qb tile BNx128 per K-block
+//               into a 192 KB shared-memory ring (128-byte swizzle).
+//   warps 1, 3  MMA issuers, one thread each, taking alternate K-blocks: four
+//               tcgen05.mma (M=128, N=BN, K=32) per K-block into one of
+//               512/BN BN-column TMEM buffers, the first with accumulate = 0.
+//               Two issuers keep the tensor core fed while either waits on a
+//               barrier (one thread waiting per K-block leaves the MMA queue
+//               empty for the length of the wait).  Warp 1 owns TMEM.
+//   warp 2      scale producer: cp.async copies of the 128 activation scales
+//               and the weight scale(s) of each K-block into an 8-slot
+//               shared-memory ring, so the promotion never waits on a global
+//               load.
+//   warps 4..   promotion: each K-block's fp32 partial is read from TMEM
 //               (tcgen05.ld) and added into registers with the scale product
-//               sA*sB; the buffer is handed back right after the last read,
-//               so the tensor core works on K-block kb+1 while kb is being
-//               promoted.  Warp w owns TMEM lanes 32*(w%4).. and one
-//               128-column half, i.e. one nb block with a single sB per
-//               K-block.  The four 32-column reads of a K-block are pipelined
-//               with the FMAs of the previous chunk.
-//   Registers: the first warpgroup (producer, MMA, two idle warps) gives its
-//   registers to the two promotion warpgroups (setmaxnreg 40 / 232, summing
-//   to the 168 per thread the CTA is launched with), which hold 128 fp32
-//   accumulators plus two 32-column staging chunks per thread.
+//               sA*sB; the buffer is handed back right after the read, so the
+//               tensor core works on the next K-blocks meanwhile.  Warp w owns
+//               TMEM lanes 32*(w%4).. and a column slice of the tile that lies
+//               inside one 128-column weight block (one sB per K-block).
+//               BN = 128: 16 warps x 32 columns (4 TMEM buffers, 96 registers
+//               per thread).  BN = 256: 8 warps x 128 columns (2 buffers); the
+//               first warpgroup hands registers to the promotion warpgroups
+//               (setmaxnreg 40 / 232 within the 168 per thread of the launch).
 // Every wait is bounded; a wait that runs out records a timeout in the status
 // word and the kernel unwinds (waiting, bounded, for its own copies and MMAs).
 #include <cstdint>
@@ -43,35 +48,60 @@
 namespace fp8bs {
 namespace promote {
 
-constexpr int BM = 128, BN = kPromoteBN, BK = 128;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 384;
-constexpr int EPI_WARPS = 8;
-constexpr int EPI_WARP0 = 4;                 // first promotion warp (warpgroups 1 and 2)
-constexpr int LAUNCH_REGS = 168;             // per thread at launch: 65536 / 384, rounded to 8
-constexpr int REGS_CTRL = 40;                // warpgroup 0 after setmaxnreg.dec
-constexpr int REGS_EPI = 232;                // warpgroups 1, 2 after setmaxnreg.inc
-static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * LAUNCH_REGS, "register split exceeds the launch");
-constexpr int TMEM_COLS = 512;
+constexpr int BM = 128, BK = 128;
+constexpr int EPI_WARP0 = 4;                 // first promotion warp
+constexpr int SCALE_WARP = 2;
 constexpr int MAX_GROUPS = 1024;
-constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+constexpr int SRING = 8;                     // scale ring slots
+constexpr int RING_BYTES = 192 * 1024;       // operand ring
 
-struct __align__(8) Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t mma_done;
+template <int BN_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;   // 4 (BN 256) or 6 (BN 128)
+    static constexpr int NBUF = 512 / BN;                     // TMEM accumulator buffers
+    static constexpr int EPI_WARPS = BN == 128 ? 16 : 8;
+    static constexpr int SLICES = EPI_WARPS / 4;              // column slices per TMEM lane quarter
+    static constexpr int EPI_COLS = BN / SLICES;              // columns per promotion warp
+    static constexpr int CHUNKS = EPI_COLS / 32;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    static constexpr bool SPLIT_REGS = BN == 256;
+    static constexpr int LAUNCH_REGS = 168;                   // 65536 / 384, rounded to 8 (BN 256)
+    static constexpr int REGS_CTRL = 40;                      // warpgroup 0 after setmaxnreg.dec
+    static constexpr int REGS_EPI = 232;                      // promotion warpgroups after .inc
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+    static_assert(STAGES % 2 == 0 && NBUF % 2 == 0, "each stage / buffer belongs to one MMA issuer");
+    static_assert(STAGES <= 8 && NBUF <= 4, "barrier arrays");
+    static_assert(!SPLIT_REGS || (128 * REGS_CTRL + (THREADS - 128) * REGS_EPI <= THREADS * LAUNCH_REGS),
+                  "register split exceeds the launch");
+};
+
+struct ScaleSlot {
+    float sa[BM];
+    float sb[2];
+    float pad[2];
+};
+
+struct __align__(16) Ctrl {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[4];
+    uint64_t tempty[4];
+    uint64_t sfull[SRING];
+    uint64_t sempty[SRING];
+    uint64_t mma_done[2];
     uint32_t tmem_base;
     int32_t n_tiles;
     int32_t abort_flag;
+    int32_t pad_;
+    ScaleSlot ring[SRING];
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl) +
-                              (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+constexpr size_t SMEM_BYTES =
+    1024 /*align slack*/ + (size_t)RING_BYTES + sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
 
 struct Tile {
     int32_t m0, row_end, brow, n0, g;
@@ -80,7 +110,7 @@ struct Tile {
 // Tile t -> coordinates.  Dense: m-tiles vary fastest so that CTAs running at
 // the same time share the weight tile.  Grouped: tiles of expert g follow
 // those of expert g-1; inside an expert, m-tiles vary fastest.
-template <bool GROUPED>
+template <int BN, bool GROUPED>
 __device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* cum, const int32_t* glo,
                                             const int32_t* ghi, int G) {
     Tile r;
@@ -102,7 +132,6 @@ __device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* 
         const int local = t - cum[g];
         const int MTg = (ghi[g] - glo[g] + BM - 1) / BM;
         const int mt = local % MTg, nt = local / MTg;
-        (void)N;
         r.m0 = glo[g] + mt * BM;
         r.row_end = ghi[g];
         r.brow = g * N + nt * BN;
@@ -116,15 +145,21 @@ __device__ __forceinline__ void record_timeout(int* status) {
     if (status) atomicCAS(status, 0, kStatusTimeout);
 }
 
-template <bool GROUPED>
-__global__ void __launch_bounds__(THREADS, 1)
+__device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[32], float sc) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v[j]), sc, acc[j]);
+}
+
+template <int BN, bool GROUPED>
+__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status) {
+    using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)STAGES * STAGE_BYTES);
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)RING_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
     int32_t* glo = cum + (MAX_GROUPS + 1);
     int32_t* ghi = glo + (MAX_GROUPS + 1);
@@ -132,27 +167,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK;
     const int NT = (N + BN - 1) / BN;
+    const int NB = N / 128;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::NBUF; ++b) {
             mbar_init(&ctl->tfull[b], 1);
-            mbar_init(&ctl->tempty[b], EPI_WARPS);
+            mbar_init(&ctl->tempty[b], C::EPI_WARPS);
         }
-        mbar_init(&ctl->mma_done, 1);
+        for (int s = 0; s < SRING; ++s) {
+            mbar_init(&ctl->sfull[s], 32);        // one cp.async arrival per lane of the scale warp
+            mbar_init(&ctl->sempty[s], C::EPI_WARPS);
+        }
+        mbar_init(&ctl->mma_done[0], 1);
+        mbar_init(&ctl->mma_done[1], 1);
         ctl->abort_flag = 0;
         mbar_init_fence();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+        tmem_alloc(&ctl->tmem_base, 512);
         tmem_relinquish();
     }
-    if (warp == 2) {
+    if (warp == 3) {
         if (GROUPED) {
             // Per-expert row ranges (clamped to [0, M]) and the running tile count.
             int carry = 0;
@@ -188,58 +229,70 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_tiles = ctl->n_tiles;
     volatile int32_t* abort_flag = &ctl->abort_flag;
 
-    if (warp < EPI_WARP0) regs_dealloc<REGS_CTRL>();
+    if constexpr (C::SPLIT_REGS) {
+        if (warp < EPI_WARP0) regs_dealloc<C::REGS_CTRL>();
+    }
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<GROUPED>(t, M, N, cum, glo, ghi, G);
+                const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs) || *abort_flag) {
+                    const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sA = smem + (size_t)s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);
+                    uint8_t* sA = smem + (size_t)s * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&ctl->full[s], C::STAGE_BYTES);
                     tma_load_2d(sA, &tm_a, &ctl->full[s], kb * BK, tl.m0);
-                    tma_load_2d(sA + A_BYTES, &tm_b, &ctl->full[s], kb * BK, tl.brow);
+                    tma_load_2d(sA + C::A_BYTES, &tm_b, &ctl->full[s], kb * BK, tl.brow);
                 }
             }
             if (!ok) {
                 record_timeout(status);
                 *abort_flag = 1;
                 // Let the copies already issued land before the CTA can exit.
-                const uint32_t n = it < STAGES ? it : STAGES;
+                const uint32_t n = it < (uint32_t)C::STAGES ? it : (uint32_t)C::STAGES;
                 for (uint32_t j = it - n; j < it; ++j)
-                    mbar_wait(&ctl->full[j % STAGES], (j / STAGES) & 1, kWaitLimitNs);
+                    mbar_wait(&ctl->full[j % C::STAGES], (j / C::STAGES) & 1, kWaitLimitNs);
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------ MMA issuers
         if (lane == 0) {
-            uint32_t it = 0, kbg = 0;
+            const uint32_t me = warp == 1 ? 0u : 1u;   // takes K-blocks it with it % 2 == me
+            uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++it, ++kbg) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
-                    const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
-                    if (!mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs) ||
-                        !mbar_wait(&ctl->full[s], ph, kWaitLimitNs) || *abort_flag) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    if ((it & 1) != me) continue;
+                    const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
+                    const uint32_t b = it % C::NBUF, tph = (it / C::NBUF) & 1;
+                    // Operands and scales first (usually ready early), then the TMEM
+                    // buffer, so the MMAs go out as soon as the promotion warps release
+                    // it.  Waiting for the scale slot here means the promotion warps,
+                    // whose loop is the critical path, find the scales in place once
+                    // the K-block's partial is in TMEM and wait on one barrier only.
+                    const uint32_t slot = it % SRING, sph = (it / SRING) & 1;
+                    if (!mbar_wait(&ctl->full[s], ph, kWaitLimitNs) ||
+                        !mbar_wait(&ctl->sfull[slot], sph, kWaitLimitNs) ||
+                        !mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sA = smem_u32(smem + (size_t)s * STAGE_BYTES);
+                    const uint32_t sA = smem_u32(smem + (size_t)s * C::STAGE_BYTES);
                     const uint64_t adesc = sdesc_kmajor_sw128(sA);
-                    const uint64_t bdesc = sdesc_kmajor_sw128(sA + A_BYTES);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sA + C::A_BYTES);
                     const uint32_t d = tmem_base + b * BN;
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        umma_f8f6f4(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), IDESC, k > 0 ? 1u : 0u);
+                        umma_f8f6f4(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), C::IDESC,
+                                    k > 0 ? 1u : 0u);
                     umma_commit(&ctl->empty[s]);
                     umma_commit(&ctl->tfull[b]);
                 }
@@ -249,79 +302,114 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
             }
             // All MMAs this thread issued are complete before TMEM is released.
-            umma_commit(&ctl->mma_done);
-            mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
+            umma_commit(&ctl->mma_done[me]);
+            mbar_wait(&ctl->mma_done[me], 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp >= EPI_WARP0) {
-        // ------------------------------------------------ promotion epilogue
-        regs_alloc<REGS_EPI>();
-        const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int h = (warp - EPI_WARP0) >> 2;  // 128-column half of the 256-wide tile
-        const int row_in_tile = q * 32 + lane;
-        const int NB = N / 128;
-        uint32_t kbg = 0;
+    } else if (warp == SCALE_WARP) {
+        // ------------------------------------------------ scale producer
+        uint32_t sit = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<GROUPED>(t, M, N, cum, glo, ghi, G);
-            const int m = tl.m0 + row_in_tile;
-            const bool vrow = m < tl.row_end;
-            const int nb = tl.n0 / 128 + h;
-            const bool vcol = nb < NB;
-            const float* sbp = sb + ((size_t)tl.g * NB + (vcol ? nb : 0)) * KB;
-            const float* sap = sa + m;
-            float acc[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[cc][j] = 0.0f;
-            // scales prefetched two K-blocks ahead
-            float sa0 = vrow ? __ldg(sap) : 0.0f, sb0 = vcol ? __ldg(sbp) : 0.0f;
-            float sa1 = (vrow && KB > 1) ? __ldg(sap + ldsa) : 0.0f, sb1 = (vcol && KB > 1) ? __ldg(sbp + 1) : 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++kbg) {
-                const float sc = sa0 * sb0;
-                sa0 = sa1;
-                sb0 = sb1;
-                if (kb + 2 < KB) {
-                    sa1 = vrow ? __ldg(sap + (size_t)(kb + 2) * ldsa) : 0.0f;
-                    sb1 = vcol ? __ldg(sbp + kb + 2) : 0.0f;
-                }
-                const uint32_t b = kbg & 1, tph = (kbg >> 1) & 1;
-                bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs) && !*abort_flag;
+            const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const int nb0 = tl.n0 / 128;
+            for (int kb = 0; kb < KB; ++kb, ++sit) {
+                const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
+                bool got = mbar_wait(&ctl->sempty[slot], ph ^ 1, kWaitLimitNs);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) {
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
-                uint32_t v0[32], v1[32];
-                tmem_ld_x32(taddr, v0);
-                tmem_ld_wait();
-                tmem_ld_x32(taddr + 32, v1);
+                ScaleSlot& S = ctl->ring[slot];
+                const float* sak = sa + (size_t)kb * ldsa;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[0][j] = fmaf(__uint_as_float(v0[j]), sc, acc[0][j]);
-                tmem_ld_wait_after(acc[0]);
-                tmem_ld_x32(taddr + 64, v0);
+                for (int j = 0; j < 4; ++j) {
+                    const int r = lane + 32 * j, m = tl.m0 + r;
+                    const bool v = m < tl.row_end;
+                    cp_async_4(&S.sa[r], v ? sak + m : sa, v);
+                }
+                if (lane < 2) {
+                    // BN = 256 spans weight blocks nb0 and nb0 + 1; BN = 128 uses only nb0
+                    const int nb = nb0 + (BN == 256 ? lane : 0);
+                    const bool v = nb < NB;
+                    cp_async_4(&S.sb[lane], v ? sb + ((size_t)tl.g * NB + nb) * KB + kb : sb, v);
+                }
+                cp_async_arrive_noinc(&ctl->sfull[slot]);
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (!ok && lane == 0) {
+            record_timeout(status);
+            *abort_flag = 1;
+        }
+        __syncwarp();
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------ promotion epilogue
+        if constexpr (C::SPLIT_REGS) regs_alloc<C::REGS_EPI>();
+        const int q = warp & 3;                      // TMEM lane quarter this warp may access
+        const int sl = (warp - EPI_WARP0) >> 2;      // column slice of the tile
+        const int row_in_tile = q * 32 + lane;
+        const int sbi = (sl * C::EPI_COLS) / 128;    // which weight block of the tile (0 or 1)
+        uint32_t kbg = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const int m = tl.m0 + row_in_tile;
+            const int col0 = tl.n0 + sl * C::EPI_COLS;
+            const bool vrow = m < tl.row_end;
+            const bool vcol = col0 < N;
+            float acc[C::CHUNKS][32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[1][j] = fmaf(__uint_as_float(v1[j]), sc, acc[1][j]);
-                tmem_ld_wait_after(acc[1]);
-                tmem_ld_x32(taddr + 96, v1);
+            for (int cc = 0; cc < C::CHUNKS; ++cc)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[2][j] = fmaf(__uint_as_float(v0[j]), sc, acc[2][j]);
-                tmem_ld_wait_after(acc[2]);
-                // all four chunks are in registers: hand the buffer back
-                tc_fence_before_sync();
+                for (int j = 0; j < 32; ++j) acc[cc][j] = 0.0f;
+            for (int kb = 0; kb < KB; ++kb, ++kbg) {
+                const uint32_t slot = kbg % SRING, sph = (kbg / SRING) & 1;
+                const uint32_t b = kbg % C::NBUF, tph = (kbg / C::NBUF) & 1;
+                (void)sph;   // the issuer waited for the scale slot before this K-block's MMAs
+                bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const float sc = ctl->ring[slot].sa[row_in_tile] * ctl->ring[slot].sb[sbi];
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[b]);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[3][j] = fmaf(__uint_as_float(v1[j]), sc, acc[3][j]);
+                if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+                tc_fence_after_sync();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + sl * C::EPI_COLS;
+                uint32_t v0[32], v1[32];
+                if constexpr (C::CHUNKS == 1) {
+                    tmem_ld_x32(taddr, v0);
+                    tmem_ld_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                    fma_chunk(acc[0], v0, sc);
+                } else {
+                    // two round trips of two 32-column loads each
+                    tmem_ld_x32(taddr, v0);
+                    tmem_ld_x32(taddr + 32, v1);
+                    tmem_ld_wait();
+                    fma_chunk(acc[0], v0, sc);
+                    fma_chunk(acc[1], v1, sc);
+                    tmem_ld_x32(taddr + 64, v0);
+                    tmem_ld_x32(taddr + 96, v1);
+                    tmem_ld_wait();
+                    // all four chunks are in registers: hand the buffer back
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                    fma_chunk(acc[2], v0, sc);
+                    fma_chunk(acc[3], v1, sc);
+                }
             }
             if (!ok) break;
             if (vrow && vcol) {
-                uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + tl.n0 + h * 128);
+                uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < C::EPI_COLS / 8; ++j) {
                     uint32_t p[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -347,38 +435,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc(tmem_base, 512);
     }
+}
+
+template <int BN, bool GROUPED>
+cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
+    using C = Cfg<BN>;
+    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    auto kern = k_gemm_promote<BN, GROUPED>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done_mask & (1 << (dev & 31)))) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        // The setmaxnreg split is only safe if the CTA really starts with
+        // LAUNCH_REGS registers per thread; refuse to launch otherwise.
+        if (C::SPLIT_REGS && fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done_mask |= 1 << (dev & 31);
+    }
+    const int64_t NT = (a.N + BN - 1) / BN;
+    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
+    const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
+    kern<<<grid, C::THREADS, SMEM_BYTES, st>>>(*a.tm_a, *a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
+                                               a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
+    return cudaGetLastError();
 }
 
 }  // namespace promote
 
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
-    using namespace promote;
     if (a.M == 0) return cudaSuccess;
-    static int attr_done_mask[2] = {0, 0};   // bit per device ordinal (< 32)
     const bool grouped = a.offsets != nullptr;
-    auto kern = grouped ? k_gemm_promote<true> : k_gemm_promote<false>;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!(attr_done_mask[grouped] & (1 << (dev & 31)))) {
-        // The setmaxnreg split is only safe if the CTA really starts with
-        // LAUNCH_REGS registers per thread; refuse to launch otherwise.
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done_mask[grouped] |= 1 << (dev & 31);
-    }
-    const int64_t NT = (a.N + BN - 1) / BN;
-    int64_t tiles = grouped ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
-    const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(*a.tm_a, *a.tm_b, a.sa, a.ldsa, a.sb,
-                                            static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
-                                            (int)a.K, a.offsets, a.G, a.status);
-    return cudaGetLastError();
+    if (a.bn == 128) return grouped ? promote::launch<128, true>(a, st) : promote::launch<128, false>(a, st);
+    if (a.bn == 256) return grouped ? promote::launch<256, true>(a, st) : promote::launch<256, false>(a, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace fp8bs

@@ -49,6 +49,8 @@ struct Cfg {
     static constexpr uint32_t IDESC = idesc_e4m3_f32(BMW, NT);
 };
 
+constexpr int MAX_KB = 1024;   // K up to 131072: the CTA's weight scales are staged in shared memory
+
 struct __align__(8) Ctrl {
     uint64_t full[8];
     uint64_t empty[8];
@@ -58,6 +60,7 @@ struct __align__(8) Ctrl {
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t last;
+    float sw[MAX_KB];          // sB[tile, kb_begin + i]
 };
 
 template <int NT>
@@ -193,12 +196,14 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
         float acc[C::CPW];
 #pragma unroll
         for (int j = 0; j < C::CPW; ++j) acc[j] = 0.0f;
-        const float* sbp = sb + (size_t)tile * KB;
-        float sw_next = nkb > 0 ? __ldg(sbp + kb_begin) : 0.0f;
+        // this CTA's weight scales, loaded once (a dependent global load per
+        // K-block would put its latency on the critical path of the pipeline)
+        const float* sbp = sb + (size_t)tile * KB + kb_begin;
+        for (int i = ew * 32 + lane; i < nkb; i += 32 * C::EPI_WARPS) ctl->sw[i] = __ldg(sbp + i);
+        named_bar_sync(1, 32 * C::EPI_WARPS);
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
-            const float swv = sw_next;
-            if (i + 1 < nkb) sw_next = __ldg(sbp + kb_begin + i + 1);
+            const float swv = ctl->sw[i];
             const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1;
             const uint32_t b = i % C::NBUF, tph = (i / C::NBUF) & 1;
             bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs) && mbar_wait(&ctl->full[s], ph, kWaitLimitNs) &&

@@ -44,12 +44,14 @@ struct GemmArgs {
     void* workspace;
     size_t ws_bytes;
     int32_t splits;
+    int32_t bn;                     // promote kernel tile width (128 or 256)
     int* status;
     int sm_count;
 };
 
-// Dense / grouped kernel with per-K-block fp32 promotion (tcgen05, TMEM).
-constexpr int kPromoteBN = 256;
+// Dense / grouped kernel with per-K-block fp32 promotion (tcgen05, TMEM);
+// output tile 128 x bn with bn = 128 or 256 (promote_tile_n picks it).
+int promote_tile_n(int64_t M, int64_t N, int64_t K, int32_t G);
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st);
 
 // Skinny (decode) kernel: weights on the MMA's M side, tokens on N, split-K.
