@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         const int sbi = (sl * C::EPI_COLS) / 128;    // which weight block of the tile (0 or 1)
         uint32_t kbg = 0;
         bool ok = true;
+        bool ready = false;   // tfull of K-block kbg already seen complete (early probe)
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
             const int m = tl.m0 + row_in_tile;
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 const uint32_t slot = kbg % SRING, sph = (kbg / SRING) & 1;
                 const uint32_t b = kbg % C::NBUF, tph = (kbg / C::NBUF) & 1;
                 (void)sph;   // the issuer waited for the scale slot before this K-block's MMAs
-                bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs);
+                bool got = __all_sync(0xFFFFFFFFu, ready) || mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) {
                     ok = false;
@@ -380,12 +381,17 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + sl * C::EPI_COLS;
                 uint32_t v0[32], v1[32];
+                // The next K-block's partial is probed right after this one's buffer is
+                // released; the result is used at the top of the next iteration, so the
+                // probe's latency (a barrier test costs ~200 cycles) overlaps the FMAs.
+                const uint32_t kn = kbg + 1;
                 if constexpr (C::CHUNKS == 1) {
                     tmem_ld_x32(taddr, v0);
                     tmem_ld_wait();
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                    ready = mbar_test_wait(&ctl->tfull[kn % C::NBUF], (kn / C::NBUF) & 1);
                     fma_chunk(acc[0], v0, sc);
                 } else {
                     // two round trips of two 32-column loads each
@@ -401,6 +407,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                    ready = mbar_test_wait(&ctl->tfull[kn % C::NBUF], (kn / C::NBUF) & 1);
                     fma_chunk(acc[2], v0, sc);
                     fma_chunk(acc[3], v1, sc);
                 }

@@ -66,7 +66,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // `limit_ns` nanoseconds of global time and returns false; never spins forever.
 // Polls with the non-blocking test (a suspended try_wait was measured to wake
 // several hundred cycles after the phase completes, which the MMA pipeline
-// cannot hide); the timer is read only every 1024 polls.
+// cannot hide; keeping several tests in flight, or sleeping between tests,
+// measured slower); the timer is read only every 1024 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
 #pragma unroll 1
     for (int i = 0; i < 1024; ++i)
