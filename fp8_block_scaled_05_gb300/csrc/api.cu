@@ -342,6 +342,47 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                               const uint8_t* qb, int64_t ldb, const float* sb, void* c,
+                                               int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags,
+                                               fp8_stream_t stream) {
+    if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M, N, K, flags)) return e;
+    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
+    if (path != FP8_GEMM_PATH_AUTO && path != FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
+    if (M == 0) return FP8_OK;
+    if (M > 256 || K / 128 > 1024) return FP8_ERR_SHAPE;
+    if (ldb < K) return FP8_ERR_SHAPE;
+    if (ldb % 16) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    GemmArgs a{};
+    a.sa = sa;
+    a.ldsa = ldsa;
+    a.sb = sb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.offsets = nullptr;
+    a.G = 1;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = skinny_splits(M, N, K, d->sm_count);
+    if (skinny_workspace_bytes(M, N, K, a.splits) > kNoAllocScratchBytes) return FP8_ERR_WORKSPACE;
+    const int nt = skinny_tile_n(M);
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, nt, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  &a.tm_b))
+        return e;
+    if (fp8_status e = tensor_map(sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, M, K / 128, ldsa * 4, nt, 1,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE, &a.tm_sa))
+        return e;
+    return cuda_status(launch_gemm_skinny_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fp8_status fp8_last_device_status(fp8_stream_t stream) {
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;

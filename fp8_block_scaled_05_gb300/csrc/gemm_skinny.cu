@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -346,6 +347,66 @@ cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
         case 256: return skinny::launch_nt<256>(a, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Skinny GEMM on library-owned scratch (fp8_blockscaled_gemm_skinny_noalloc).
+//
+// The split-K tickets and fp32 partials live in a fixed array in device
+// memory that belongs to the library, so the caller passes no workspace and
+// nothing is allocated per call.  Every GPU that loads the library reserves
+// the array until the process exits.  All calls share it: two calls that
+// overlap on the GPU (different streams, no ordering between them) race on
+// it.  The array keeps whatever the last call left; the tickets must start at
+// zero, so they are cleared on the stream before every launch (the partials
+// are always written before they are read).
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_skinny_scratch[kNoAllocScratchBytes];
+
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+uint8_t* g_scratch_addr[kScratchDevices];   // device address of g_skinny_scratch, per device
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands for the symbol; the address the kernel needs
+// comes from cudaGetSymbolAddress, taken once per device with that device
+// current (the first call on a device does this).
+cudaError_t scratch_address(uint8_t** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_skinny_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_skinny_noalloc(GemmArgs a, cudaStream_t st) {
+    if (a.M == 0) return cudaSuccess;
+    const size_t need = skinny_workspace_bytes(a.M, a.N, a.K, a.splits);
+    if (need > kNoAllocScratchBytes) return cudaErrorInvalidValue;   // the caller checked this already
+    uint8_t* scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    if (need > 0) {
+        // ticket words of the split-K reduction (layout of the kernel's workspace)
+        const size_t tickets = ((size_t)(a.N / 128) * 4 + 255) & ~size_t(255);
+        e = cudaMemsetAsync(scratch, 0, tickets, st);
+        if (e != cudaSuccess) return e;
+    }
+    a.workspace = scratch;
+    a.ws_bytes = kNoAllocScratchBytes;
+    return launch_gemm_skinny(a, st);
 }
 
 }  // namespace fp8bs

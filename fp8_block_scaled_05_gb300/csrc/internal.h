@@ -60,4 +60,10 @@ int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count);
 size_t skinny_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 
+// Size of the library-owned scratch of the no-allocation skinny entry point.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB per device
+// Same launch as launch_gemm_skinny with a.workspace replaced by that scratch
+// (set up on the first call per device, ticket words cleared every call).
+cudaError_t launch_gemm_skinny_noalloc(GemmArgs a, cudaStream_t st);
+
 }  // namespace fp8bs

@@ -45,6 +45,8 @@ SIGNATURES = {
                                             _u32, _vp, _sz, _vp]),
     "fp8_blockscaled_grouped_gemm": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64,
                                                     _i64, _i64, _u32, _vp, _sz, _vp]),
+    "fp8_blockscaled_gemm_skinny_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64,
+                                                           _i64, _i64, _u32, _vp]),
     "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
@@ -172,6 +174,22 @@ def fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags: int = 0,
                                               M, _ptr(qb), _ptr(sb), _ptr(c), c.stride(0), N, K, int(flags),
                                               _ptr(workspace), ws_bytes, _stream(stream)),
            "fp8_blockscaled_grouped_gemm")
+
+
+def fp8_blockscaled_gemm_skinny_noalloc(qa, sa, qb, sb, c, flags: int = 0, stream=None) -> None:
+    """Decode-sized (M <= 256) GEMM on the library's own scratch: no
+    workspace argument and no allocation (see include/fp8bs.h)."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(c, torch.bfloat16, "c")
+    M, K = qa.shape
+    N = qb.shape[0]
+    _check(lib().fp8_blockscaled_gemm_skinny_noalloc(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb),
+                                                     qb.stride(0), _ptr(sb), _ptr(c), c.stride(0), M, N, K,
+                                                     int(flags), _stream(stream)),
+           "fp8_blockscaled_gemm_skinny_noalloc")
 
 
 def fp8_gemm_workspace_size(M: int, N: int, K: int, G: int = 1) -> int:

@@ -173,6 +173,41 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
                                         uint32_t flags, void *workspace, size_t ws_bytes,
                                         fp8_stream_t stream);
 
+/*
+ * Decode-sized GEMM (M <= 256) that allocates nothing and takes no workspace.
+ *
+ * The web pages have no counterpart: this is an interface convenience.  It
+ * computes the same C as fp8_blockscaled_gemm on the split-K skinny path
+ * (same kernels, same split count, same fixed-order reduction), but keeps the
+ * split-K tickets and fp32 partials in an 8 MiB array inside the library's own
+ * device memory instead of a caller-provided workspace.  It is meant for
+ * callers that cannot call cudaMalloc: plugins hosted by a runtime that
+ * reserves all device memory at start-up and fails or mis-accounts later
+ * allocations, and decode loops where cudaMalloc/cudaFree would synchronise
+ * the device.  Inputs and output are passed exactly as for
+ * fp8_blockscaled_gemm.
+ *
+ * - Every GPU that loads the library holds the 8 MiB array until the process
+ *   exits.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the array, and it keeps what the last call left in it.
+ *   The call clears the ticket words on `stream` before its launch.  Calls
+ *   that overlap on the GPU (unordered streams) race on the array: order them.
+ * - The scratch needed is 256-byte-rounded 4*N/128 bytes of tickets plus
+ *   splits * (N/128) * NT * 128 * 4 bytes of partials (NT = M rounded up to
+ *   16, 32, 64, 128 or 256; splits as reported by fp8_gemm_plan).  Sizes that
+ *   need more than 8 MiB return FP8_ERR_WORKSPACE without launching.
+ *   M > 256 returns FP8_ERR_SHAPE.
+ * - flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_SKINNY (plus FP8_GEMM_SCALES_POW2).
+ */
+FP8BS_API fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t *qa, int64_t lda, const float *sa,
+                                                         int64_t ldsa, const uint8_t *qb, int64_t ldb,
+                                                         const float *sb, void *c, int64_t ldc, int64_t M,
+                                                         int64_t N, int64_t K, uint32_t flags,
+                                                         fp8_stream_t stream);
+
 /* Bytes of workspace fp8_blockscaled_gemm (G == 1) or
  * fp8_blockscaled_grouped_gemm (G > 1) needs for these sizes; 0 when none. */
 FP8BS_API size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t G);
