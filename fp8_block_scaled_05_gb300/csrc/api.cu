@@ -201,7 +201,7 @@ const char* fp8_status_string(fp8_status st) {
 fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq, float* s,
                                int64_t lds, fp8_scale_mode mode, fp8_stream_t stream) {
     if (fp8_status e = check_mode(mode)) return e;
-    if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 21) || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 31) - 1 || K > (1ll << 26)) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
     if (!x || !q || !s) return FP8_ERR_NULL;
     if (ldx < K || ldq < K || lds < M) return FP8_ERR_SHAPE;

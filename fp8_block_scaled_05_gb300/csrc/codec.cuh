@@ -139,13 +139,32 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)r;
 }
 
+// Codes of two elements, e4m3(RN(x/s)) each.
+//
+// Fast path for mode 0: q0 = RN(x r) is within 1.5 ulp of x/s, so the
+// correctly rounded quotient t = RN(x/s) is within 2 ulp of q0 and lies
+// strictly between q0 (1 - 2^-21) and q0 (1 + 2^-21) (both products, rounded,
+// stay at least 3.5 ulp away from q0).  E4M3 conversion is monotone, so when
+// those two ends convert to the same code, t converts to it as well.  Only
+// pairs whose interval contains an E4M3 rounding boundary (a few in a
+// million) take the two-step corrected quotient.
+__device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
+    if (bs.mode == 1) return e4m3x2(xa * bs.r, xb * bs.r);
+    if (bs.mode == 0) {
+        const float qa = xa * bs.r, qb = xb * bs.r;
+        constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
+        const uint32_t lo = e4m3x2(qa * kLo, qb * kLo), hi = e4m3x2(qa * kHi, qb * kHi);
+        if (lo == hi) return lo;
+    }
+    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
+}
+
 // Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes).
 __device__ __forceinline__ uint2 quant8(const uint4 &v, const BlockScale &bs) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t p[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        p[i] = e4m3x2(quotient_rn(bf16lo_to_f32(w[i]), bs), quotient_rn(bf16hi_to_f32(w[i]), bs));
+    for (int i = 0; i < 4; ++i) p[i] = quant_pair(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), bs);
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 

@@ -20,29 +20,30 @@
 namespace fp8bs {
 
 // ---------------------------------------------------------------------------
-// 1x128 activations.  CTA tile: 32 rows x 8 K-blocks.  Warp w owns rows
-// 4w..4w+3; a warp-wide 512-byte load covers two adjacent K-blocks of one
-// row, half-warp h handling K-block 2p+h.  A warp therefore holds 32 blocks
-// (16 "items" i = 4r+p per half).  Their amax values are reduced with a
-// butterfly reduce-scatter over each half (15 shuffles instead of 64), after
-// which lane 16h+i holds the amax of item i of half h and computes that one
-// block's scale; the other lanes fetch (s, 1/s) with two shuffles per item.
-// Scales are gathered in shared memory and written K-block-major (32
-// consecutive rows per 128-byte store).
+// 1x128 activations.  CTA tile: 16 rows x 8 K-blocks.  Warp w owns rows
+// 2w, 2w+1; a warp-wide 512-byte load covers two adjacent K-blocks of one
+// row, half-warp h handling K-block 2p+h.  A warp therefore holds 16 blocks
+// (8 "items" i = 4r+p per half).  Their amax values are reduced over each
+// half with one plain exchange and a butterfly reduce-scatter (15 shuffles
+// instead of 32), after which lane 16h+(i mod 8) holds the amax of item i of
+// half h and computes that one block's scale; the other lanes fetch (s, 1/s)
+// with two shuffles per item.  Scales are gathered in shared memory and
+// written K-block-major (16 consecutive rows per store).
 // ---------------------------------------------------------------------------
-constexpr int kActRows = 32;
+constexpr int kActRowsPerWarp = 2;
+constexpr int kActRows = 8 * kActRowsPerWarp;
 constexpr int kActKB = 8;
-constexpr int kActRowsPerWarp = 4;
 constexpr int kActPairs = kActKB / 2;
-constexpr int kActItems = kActRowsPerWarp * kActPairs;   // 16 blocks per half-warp
+constexpr int kActItems = kActRowsPerWarp * kActPairs;   // blocks per half-warp
+static_assert(kActItems <= 16 && (kActItems & (kActItems - 1)) == 0, "items per half-warp");
 
 __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
                                                          int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int64_t lds, int pow2) {
     __shared__ float s_tile[kActKB][kActRows];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
-    const int64_t m0 = (int64_t)blockIdx.y * kActRows;
-    const int64_t kb0 = (int64_t)blockIdx.x * kActKB;
+    const int64_t m0 = (int64_t)blockIdx.x * kActRows;
+    const int64_t kb0 = (int64_t)blockIdx.y * kActKB;
 
     uint4 v[kActItems];
 #pragma unroll
@@ -56,11 +57,16 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
             v[i] = make_uint4(0, 0, 0, 0);
     }
 
-    // Butterfly reduce-scatter: after the step with offset o, a lane keeps the
-    // items whose index bit o matches its own lane bit o.
     uint32_t a[kActItems];
 #pragma unroll
     for (int i = 0; i < kActItems; ++i) a[i] = absmax8(0u, v[i]);
+    // Plain exchange over the lane bits above the item count...
+#pragma unroll
+    for (int o = 8; o >= kActItems; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < kActItems; ++j) a[j] = max_u16x2(a[j], __shfl_xor_sync(0xFFFFFFFFu, a[j], o));
+    // ...then a butterfly reduce-scatter: after the step with offset o, a lane
+    // keeps the items whose index bit o matches its own lane bit o.
 #pragma unroll
     for (int o = kActItems / 2; o >= 1; o >>= 1) {
         const bool upper = (lane & o) != 0;
@@ -71,9 +77,9 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
             a[j] = max_u16x2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
         }
     }
-    // this lane's block: item l16 of half `half`
+    // this lane's block: item (l16 mod kActItems) of half `half`
     const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), pow2 != 0);
-    {
+    if (l16 < kActItems) {
         const int r = l16 / kActPairs, p = l16 % kActPairs;
         const int rl = warp * kActRowsPerWarp + r;
         if (m0 + rl < M && kb0 + 2 * p + half < KB) s_tile[2 * p + half][rl] = own.s;
@@ -92,16 +98,18 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
         }
     }
     __syncthreads();
-    const int kbl = threadIdx.x >> 5, rl = threadIdx.x & 31;
-    const int64_t kb = kb0 + kbl, m = m0 + rl;
-    if (kb < KB && m < M) s[kb * lds + m] = s_tile[kbl][rl];
+    if (threadIdx.x < kActKB * kActRows) {
+        const int kbl = threadIdx.x / kActRows, rl = threadIdx.x % kActRows;
+        const int64_t kb = kb0 + kbl, m = m0 + rl;
+        if (kb < KB && m < M) s[kb * lds + m] = s_tile[kbl][rl];
+    }
 }
 
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                    float* s, int64_t lds, bool pow2, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
     const int64_t KB = K / 128;
-    dim3 grid((unsigned)((KB + kActKB - 1) / kActKB), (unsigned)((M + kActRows - 1) / kActRows));
+    dim3 grid((unsigned)((M + kActRows - 1) / kActRows), (unsigned)((KB + kActKB - 1) / kActKB));
     k_quant_act_1x128<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds,
                                             pow2 ? 1 : 0);
     return cudaGetLastError();

@@ -95,7 +95,7 @@ typedef enum {
  * s   device, fp32 [K/128][lds]: the scale of row m, K-block kb is s[kb * lds + m]
  *     (K-block-major so that a GEMM reads the scales of consecutive rows
  *     contiguously); lds >= M, lds % 4 == 0, 16-byte aligned.
- * M >= 0 (M == 0 is a no-op), K > 0 and K % 128 == 0, M * K < 2^40.
+ * M >= 0 (M == 0 is a no-op; M < 2^31), 0 < K <= 2^26 and K % 128 == 0.
  */
 FP8BS_API fp8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
                                uint8_t *q, int64_t ldq, float *s, int64_t lds,
