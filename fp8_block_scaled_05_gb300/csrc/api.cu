@@ -288,9 +288,6 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, 128,
                                       CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
             return e;
-        if (fp8_status e = tensor_map(sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, M, K / 128, ldsa * 4, nt, 1,
-                                      CU_TENSOR_MAP_SWIZZLE_NONE, &a.tm_sa))
-            return e;
         return cuda_status(launch_gemm_skinny(a, st));
     }
     a.bn = promote_tile_n(M, N, K, 1);
@@ -376,9 +373,6 @@ fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, c
         return e;
     if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B,
                                   &a.tm_b))
-        return e;
-    if (fp8_status e = tensor_map(sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, M, K / 128, ldsa * 4, nt, 1,
-                                  CU_TENSOR_MAP_SWIZZLE_NONE, &a.tm_sa))
         return e;
     return cuda_status(launch_gemm_skinny_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -8,7 +8,8 @@
 // is the latency-critical one).
 //
 // The operands are swapped: 128 weight rows fill the MMA's M side and the
-// tokens, padded to NT in {16, 32, 64, 128, 256}, are its N side, so
+// tokens, padded to NT in {16, 32, 64, 128} (more than 128 tokens run as
+// 128-token chunks on the grid's z dimension), are its N side, so
 // D[n, m] = sum_k qb[n, k] qa[m, k] lands in TMEM with lane = weight row and
 // column = token.  The K-blocks are split over `splits` CTAs per 128-row
 // weight tile so that the weight stream is spread over every SM; the last
@@ -32,22 +33,31 @@ namespace skinny {
 
 constexpr int BMW = 128;     // weight rows per CTA (MMA M)
 constexpr int BK = 128;
+constexpr int EPI_WARP0 = 4;
 
 template <int NT>
 struct Cfg {
     static constexpr int W_BYTES = BMW * BK;
     static constexpr int A_BYTES = NT * BK;
-    static constexpr int S_BYTES = 1024;                       // NT fp32 scales, padded for alignment
-    static constexpr int STAGE_BYTES = W_BYTES + A_BYTES + S_BYTES;
+    static constexpr int STAGE_BYTES = W_BYTES + A_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
-    static constexpr int NBUF = NT >= 256 ? 2 : (NT >= 128 ? 4 : 4);
-    static constexpr int TMEM_USED = NBUF * NT;
-    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : (TMEM_USED <= 64 ? 64 : (TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512)));
-    static constexpr int EPI_WARPS = NT >= 128 ? 8 : 4;
-    static constexpr int CPW = NT / (EPI_WARPS / 4);           // token columns per epilogue warp
+    // Promotion groups: group g takes the K-blocks i with i % NG == g, each
+    // into its own accumulators (combined in group order at the end), so the
+    // per-K-block barrier latency of one group overlaps the others' work.
+    static constexpr int NG = NT <= 16 ? 4 : (NT <= 64 ? 2 : 1);
+    static constexpr int SLICES = NT >= 128 ? 2 : 1;           // column slices per TMEM lane quarter
+    static constexpr int GROUP_WARPS = 4 * SLICES;
+    static constexpr int EPI_WARPS = NG * GROUP_WARPS;
+    static constexpr int CPW = NT / SLICES;                    // token columns per promotion warp
     static constexpr int CHUNK = CPW >= 128 ? 16 : (CPW < 32 ? CPW : 32);
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int SA_REGS = (CPW + 31) / 32;            // activation scales held per lane
+    static constexpr int NBUF = (512 / NT) < (2 * NG > 4 ? 2 * NG : 4) ? (512 / NT) : (2 * NG > 4 ? 2 * NG : 4);
+    static constexpr int TMEM_COLS = NBUF * NT < 32 ? 32 : NBUF * NT;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr uint32_t IDESC = idesc_e4m3_f32(BMW, NT);
+    static_assert(NBUF % NG == 0 && NBUF % 2 == 0 && NBUF <= 8, "buffer ownership");
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
+    static_assert((NG - 1) * NT * BMW * 4 <= STAGES * STAGE_BYTES, "group combine fits the drained ring");
 };
 
 constexpr int MAX_KB = 1024;   // K up to 131072: the CTA's weight scales are staged in shared memory
@@ -55,9 +65,9 @@ constexpr int MAX_KB = 1024;   // K up to 131072: the CTA's weight scales are st
 struct __align__(8) Ctrl {
     uint64_t full[8];
     uint64_t empty[8];
-    uint64_t tfull[4];
-    uint64_t tempty[4];
-    uint64_t mma_done;
+    uint64_t tfull[8];
+    uint64_t tempty[8];
+    uint64_t mma_done[2];
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t last;
@@ -86,10 +96,12 @@ __device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, uint32_t (&r)[
 template <>
 __device__ __forceinline__ void tmem_ld_chunk<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_x16(taddr, r); }
 
+// Warp roles: 0 TMA producer; 1 and 2 MMA issuers (alternate K-blocks, warp 1
+// owns TMEM); 3 idle; 4.. promotion groups of GROUP_WARPS warps.
 template <int NT>
 __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
-                  const __grid_constant__ CUtensorMap tm_sa, const float* __restrict__ sb,
+                  const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
                   uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K, int splits,
                   uint8_t* __restrict__ ws, int* status) {
     using C = Cfg<NT>;
@@ -100,6 +112,10 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK, NB = N / BMW;
     const int tile = blockIdx.x, split = blockIdx.y;
+    // token chunk: tokens tok0 .. tok0 + NT - 1 (M > 128 runs as several chunks)
+    const int tok0 = blockIdx.z * NT;
+    const int Mc = M - tok0;                         // tokens of this chunk (may exceed NT)
+    const int ptile = blockIdx.z * NB + tile;        // tile index of the partials and tickets
     const int kb_begin = (int)((int64_t)split * KB / splits);
     const int kb_end = (int)((int64_t)(split + 1) * KB / splits);
     const int nkb = kb_end - kb_begin;
@@ -107,18 +123,18 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1 + C::EPI_WARPS);
+            mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < C::NBUF; ++b) {
             mbar_init(&ctl->tfull[b], 1);
-            mbar_init(&ctl->tempty[b], C::EPI_WARPS);
+            mbar_init(&ctl->tempty[b], C::GROUP_WARPS);
         }
-        mbar_init(&ctl->mma_done, 1);
+        mbar_init(&ctl->mma_done[0], 1);
+        mbar_init(&ctl->mma_done[1], 1);
         ctl->abort_flag = 0;
         mbar_init_fence();
         tma_prefetch_desc(&tm_w);
         tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_sa);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
@@ -138,15 +154,14 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
             for (int i = 0; i < nkb; ++i, ++it) {
                 const int kb = kb_begin + i;
                 const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
-                if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs) || *abort_flag) {
+                if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 uint8_t* st = smem + (size_t)s * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&ctl->full[s], C::W_BYTES + C::A_BYTES + NT * 4);
+                mbar_arrive_expect_tx(&ctl->full[s], C::W_BYTES + C::A_BYTES);
                 tma_load_2d_hint(st, &tm_w, &ctl->full[s], kb * BK, tile * BMW, evict_first);
-                tma_load_2d(st + C::W_BYTES, &tm_a, &ctl->full[s], kb * BK, 0);
-                tma_load_2d(st + C::W_BYTES + C::A_BYTES, &tm_sa, &ctl->full[s], 0, kb);
+                tma_load_2d(st + C::W_BYTES, &tm_a, &ctl->full[s], kb * BK, tok0);
             }
             if (!ok) {
                 record_timeout(status);
@@ -157,14 +172,15 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
         if (lane == 0) {
+            const int me = warp - 1;
             bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
+            for (int i = me; i < nkb; i += 2) {
                 const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1;
                 const uint32_t b = i % C::NBUF, tph = (i / C::NBUF) & 1;
-                if (!mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs) ||
-                    !mbar_wait(&ctl->full[s], ph, kWaitLimitNs) || *abort_flag) {
+                if (!mbar_wait(&ctl->full[s], ph, kWaitLimitNs) ||
+                    !mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
@@ -183,16 +199,17 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
                 record_timeout(status);
                 *abort_flag = 1;
             }
-            umma_commit(&ctl->mma_done);
-            mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
+            umma_commit(&ctl->mma_done[me]);
+            mbar_wait(&ctl->mma_done[me], 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
-        const int ew = warp - 2;
+    } else if (warp >= EPI_WARP0) {
+        const int ew = warp - EPI_WARP0;
+        const int grp = ew / C::GROUP_WARPS;
         const int q = warp & 3;
-        const int cw = ew >> 2;                 // which CPW-wide column slice
-        const int col0 = cw * C::CPW;
-        const int row = q * 32 + lane;          // weight row within the tile
+        const int sl = (ew % C::GROUP_WARPS) >> 2;   // which CPW-wide column slice
+        const int col0 = sl * C::CPW;
+        const int row = q * 32 + lane;               // weight row within the tile
         const int n = tile * BMW + row;
         float acc[C::CPW];
 #pragma unroll
@@ -203,80 +220,130 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
         for (int i = ew * 32 + lane; i < nkb; i += 32 * C::EPI_WARPS) ctl->sw[i] = __ldg(sbp + i);
         named_bar_sync(1, 32 * C::EPI_WARPS);
         bool ok = true;
-        for (int i = 0; i < nkb; ++i) {
-            const float swv = ctl->sw[i];
-            const uint32_t s = i % C::STAGES, ph = (i / C::STAGES) & 1;
+        bool ready = false;
+        for (int i = grp; i < nkb; i += C::NG) {
+            const int kb = kb_begin + i;
             const uint32_t b = i % C::NBUF, tph = (i / C::NBUF) & 1;
-            bool got = mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs) && mbar_wait(&ctl->full[s], ph, kWaitLimitNs) &&
-                       !*abort_flag;
+            // activation scales of this K-block: lane l holds column col0 + 32 r + l
+            float sav[C::SA_REGS];
+#pragma unroll
+            for (int r = 0; r < C::SA_REGS; ++r) {
+                const int col = col0 + 32 * r + lane;
+                sav[r] = (col < Mc && 32 * r + lane < C::CPW) ? __ldg(sa + (size_t)kb * ldsa + tok0 + col) : 0.0f;
+            }
+            const float swv = ctl->sw[i];
+            bool got = __all_sync(0xFFFFFFFFu, ready) || mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs);
             got = __all_sync(0xFFFFFFFFu, got);
             if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const float* s_sa = reinterpret_cast<const float*>(smem + (size_t)s * C::STAGE_BYTES + C::W_BYTES + C::A_BYTES);
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * NT + col0;
 #pragma unroll
             for (int cc = 0; cc < C::CPW / C::CHUNK; ++cc) {
                 uint32_t v[C::CHUNK];
                 tmem_ld_chunk<C::CHUNK>(taddr + cc * C::CHUNK, v);
                 tmem_ld_wait();
+                if (cc == C::CPW / C::CHUNK - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                    const int in = i + C::NG;
+                    ready = mbar_test_wait(&ctl->tfull[in % C::NBUF], (in / C::NBUF) & 1);
+                }
 #pragma unroll
                 for (int j = 0; j < C::CHUNK; ++j) {
-                    const float sc = s_sa[col0 + cc * C::CHUNK + j] * swv;
-                    acc[cc * C::CHUNK + j] = fmaf(__uint_as_float(v[j]), sc, acc[cc * C::CHUNK + j]);
+                    const int jj = cc * C::CHUNK + j;
+                    const float sc = __shfl_sync(0xFFFFFFFFu, sav[jj >> 5], jj & 31) * swv;
+                    acc[jj] = fmaf(__uint_as_float(v[j]), sc, acc[jj]);
                 }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&ctl->tempty[b]);
-                mbar_arrive(&ctl->empty[s]);
             }
         }
-        if (!ok) {
-            if (lane == 0) {
-                record_timeout(status);
-                *abort_flag = 1;
-            }
-        } else if (splits == 1) {
-            if (n < N) {
+        if (!ok && lane == 0) {
+            record_timeout(status);
+            *abort_flag = 1;
+        }
+        // Every group is done with TMEM and every MMA has completed, so the
+        // operand ring is drained: combine the groups through it, in group order.
+        named_bar_sync(1, 32 * C::EPI_WARPS);
+        ok = !*abort_flag;
+        if (C::NG > 1) {
+            float* xs = reinterpret_cast<float*>(smem);
+            if (grp > 0) {
 #pragma unroll
-                for (int j = 0; j < C::CPW; ++j) {
-                    const int m = col0 + j;
-                    if (m < M) c[(size_t)m * ldc + n] = f32_to_bf16_rn(acc[j]);
+                for (int j = 0; j < C::CPW; ++j) xs[((size_t)(grp - 1) * NT + col0 + j) * BMW + row] = acc[j];
+            }
+            named_bar_sync(1, 32 * C::EPI_WARPS);
+            if (grp == 0) {
+                for (int g2 = 1; g2 < C::NG; ++g2) {
+#pragma unroll
+                    for (int j = 0; j < C::CPW; ++j) acc[j] += xs[((size_t)(g2 - 1) * NT + col0 + j) * BMW + row];
                 }
             }
-        } else {
-            // Partials: ws layout [tickets: NB int32, padded to 256 B]
-            //                     [splits][NB][NT][128] fp32 (row fastest, coalesced).
-            int32_t* tickets = reinterpret_cast<int32_t*>(ws);
-            float* part = reinterpret_cast<float*>(ws + (((size_t)NB * 4 + 255) & ~size_t(255)));
-            float* mine = part + (((size_t)split * NB + tile) * NT) * BMW;
-#pragma unroll
-            for (int j = 0; j < C::CPW; ++j) mine[(size_t)(col0 + j) * BMW + row] = acc[j];
-            __threadfence();
-            named_bar_sync(1, 32 * C::EPI_WARPS);
-            if (ew == 0 && lane == 0) {
-                const int prev = atomicAdd(&tickets[tile], 1);
-                ctl->last = (prev == splits - 1);
-            }
-            named_bar_sync(1, 32 * C::EPI_WARPS);
-            if (ctl->last) {
-                __threadfence();
+        }
+        if (grp == 0 && ok) {
+            if (splits == 1) {
                 if (n < N) {
-#pragma unroll 4
+#pragma unroll
                     for (int j = 0; j < C::CPW; ++j) {
                         const int m = col0 + j;
-                        if (m >= M) break;
-                        float sum = 0.0f;
-                        for (int sp = 0; sp < splits; ++sp)
-                            sum += __ldcg(part + (((size_t)sp * NB + tile) * NT + m) * BMW + row);
-                        c[(size_t)m * ldc + n] = f32_to_bf16_rn(sum);
+                        if (m < Mc) c[(size_t)(tok0 + m) * ldc + n] = f32_to_bf16_rn(acc[j]);
                     }
                 }
-                if (ew == 0 && lane == 0) tickets[tile] = 0;   // leave the ticket zero for the next call
+            } else {
+                // Partials: ws layout [tickets: TC*NB int32, padded to 256 B]
+                //                     [splits][TC*NB][NT][128] fp32 (row fastest, coalesced),
+                // TC = gridDim.z token chunks.
+                const int PT = gridDim.z * NB;
+                int32_t* tickets = reinterpret_cast<int32_t*>(ws);
+                float* part = reinterpret_cast<float*>(ws + (((size_t)PT * 4 + 255) & ~size_t(255)));
+                float* mine = part + (((size_t)split * PT + ptile) * NT) * BMW;
+#pragma unroll
+                for (int j = 0; j < C::CPW; ++j) mine[(size_t)(col0 + j) * BMW + row] = acc[j];
+                __threadfence();
+                named_bar_sync(2, 32 * C::GROUP_WARPS);
+                if (ew == 0 && lane == 0) {
+                    const int prev = atomicAdd(&tickets[ptile], 1);
+                    ctl->last = (prev == splits - 1);
+                }
+                named_bar_sync(2, 32 * C::GROUP_WARPS);
+                if (ctl->last) {
+                    __threadfence();
+                    // Sum the splits in split order (this CTA's own partial is still in
+                    // registers).  Per split and 32-column chunk all loads are issued
+                    // before any add, so the chunk costs one L2 round trip.
+                    constexpr int RC = C::CPW < 32 ? C::CPW : 32;
+#pragma unroll
+                    for (int j0 = 0; j0 < C::CPW; j0 += RC) {   // unrolled: acc stays in registers
+                        if (col0 + j0 >= Mc) continue;
+                        float tot[RC];
+#pragma unroll
+                        for (int j = 0; j < RC; ++j) tot[j] = 0.0f;
+#pragma unroll 1
+                        for (int sp = 0; sp < splits; ++sp) {
+                            if (sp == split) {
+#pragma unroll
+                                for (int j = 0; j < RC; ++j) tot[j] += acc[j0 + j];
+                            } else {
+                                const float* p = part + (((size_t)sp * PT + ptile) * NT + col0 + j0) * BMW + row;
+                                float v[RC];
+#pragma unroll
+                                for (int j = 0; j < RC; ++j) v[j] = __ldcg(p + (size_t)j * BMW);
+#pragma unroll
+                                for (int j = 0; j < RC; ++j) tot[j] += v[j];
+                            }
+                        }
+                        if (n < N) {
+#pragma unroll
+                            for (int j = 0; j < RC; ++j) {
+                                const int m = col0 + j0 + j;
+                                if (m < Mc) c[(size_t)(tok0 + m) * ldc + n] = f32_to_bf16_rn(tot[j]);
+                            }
+                        }
+                    }
+                    if (ew == 0 && lane == 0) tickets[ptile] = 0;   // leave the ticket zero for the next call
+                }
             }
         }
     }
@@ -301,9 +368,9 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_done_mask |= 1 << (dev & 31);
     }
-    dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits);
+    dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits, (unsigned)((a.M + NT - 1) / NT));
     k_gemm_skinny<NT><<<grid, C::THREADS, smem_bytes<NT>(), st>>>(
-        *a.tm_b, *a.tm_a, *a.tm_sa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
+        *a.tm_b, *a.tm_a, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
         a.splits, static_cast<uint8_t*>(a.workspace), a.status);
     return cudaGetLastError();
 }
@@ -314,14 +381,17 @@ int skinny_tile_n(int64_t M) {
     if (M <= 16) return 16;
     if (M <= 32) return 32;
     if (M <= 64) return 64;
-    if (M <= 128) return 128;
-    if (M <= 256) return 256;
+    if (M <= 256) return 128;   // 129..256 tokens run as two 128-token chunks
     return 0;
 }
 
+static int64_t skinny_chunks(int64_t M) {
+    const int nt = skinny_tile_n(M);
+    return nt ? (M + nt - 1) / nt : 0;
+}
+
 int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count) {
-    (void)M;
-    const int64_t tiles = N / 128, KB = K / 128;
+    const int64_t tiles = (N / 128) * (skinny_chunks(M) > 0 ? skinny_chunks(M) : 1), KB = K / 128;
     int64_t s = sm_count / (tiles > 0 ? tiles : 1);
     if (s > KB / 2) s = KB / 2;     // at least two K-blocks per split
     if (s > 32) s = 32;
@@ -333,8 +403,8 @@ size_t skinny_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     (void)K;
     const int nt = skinny_tile_n(M);
     if (nt == 0 || splits <= 1) return 0;
-    const int64_t NB = N / 128;
-    return (((size_t)NB * 4 + 255) & ~size_t(255)) + (size_t)splits * NB * nt * 128 * sizeof(float);
+    const int64_t PT = (N / 128) * skinny_chunks(M);
+    return (((size_t)PT * 4 + 255) & ~size_t(255)) + (size_t)splits * PT * nt * 128 * sizeof(float);
 }
 
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
@@ -344,7 +414,6 @@ cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
         case 32: return skinny::launch_nt<32>(a, st);
         case 64: return skinny::launch_nt<64>(a, st);
         case 128: return skinny::launch_nt<128>(a, st);
-        case 256: return skinny::launch_nt<256>(a, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -400,7 +469,7 @@ cudaError_t launch_gemm_skinny_noalloc(GemmArgs a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (need > 0) {
         // ticket words of the split-K reduction (layout of the kernel's workspace)
-        const size_t tickets = ((size_t)(a.N / 128) * 4 + 255) & ~size_t(255);
+        const size_t tickets = ((size_t)(a.N / 128) * skinny_chunks(a.M) * 4 + 255) & ~size_t(255);
         e = cudaMemsetAsync(scratch, 0, tickets, st);
         if (e != cudaSuccess) return e;
     }

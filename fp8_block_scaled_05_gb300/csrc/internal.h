@@ -32,7 +32,6 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int
 struct GemmArgs {
     const CUtensorMap* tm_a;        // qa [rows, K] uint8, box {128, 128}, 128B swizzle
     const CUtensorMap* tm_b;        // qb [rows, K] uint8, box {128, BN}, 128B swizzle
-    const CUtensorMap* tm_sa;       // sa [KB, ldsa] fp32 (skinny / MX paths only)
     const float* sa;
     int64_t ldsa;
     const float* sb;

@@ -2,10 +2,10 @@
 
 Runs one entry point on one shape, `--warmup` times untimed and `--iters`
 times timed with CUDA events on the launching stream (L2 flushed before each
-timed launch unless --no-flush; all iterations are enqueued before one
-synchronize so host launch overhead does not land inside the event pairs),
-and prints one JSON line with the mean time and the achieved rate
-(algorithmic bytes or FLOPs).  Also the command used for
+timed launch unless --no-flush; the call is replayed from a CUDA graph and all
+iterations are enqueued before one synchronize, so host launch overhead does
+not land inside the event pairs), and prints one JSON line with the mean time
+and the achieved rate (algorithmic bytes or FLOPs).  Also the command used for
 ncu captures of a single kernel.
 
   python -m fp8_block_scaled_05_gb300.kbench --kernel gemm --M 4096 --N 28672 --K 4096
@@ -34,6 +34,7 @@ def main(argv=None):
     p.add_argument("--iters", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--no-flush", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="launch through the Python wrapper every iteration")
     a = p.parse_args(argv)
 
     _build.build()
@@ -76,18 +77,28 @@ def main(argv=None):
         run = lambda: ops.grouped_gemm(qa, sa, offs, qw, sw, a.pow2, out=c)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
 
-    for _ in range(a.warmup):
+    for _ in range(max(a.warmup, 1)):
         run()
     torch.cuda.synchronize()
-    # Enqueue every iteration before waiting once, so that the host's launch
-    # overhead overlaps the GPU work (the flush takes longer than one launch)
-    # and each event pair brackets only the kernel.
+    timed = run
+    if not a.no_graph:
+        # The library call is captured once into a CUDA graph (its one-time
+        # set-up already happened in the warm-up), so a timed iteration costs
+        # the host one replay: the host stays ahead of the GPU and no launch
+        # gap lands inside the event pair (the Python wrapper alone takes
+        # longer than a decode-sized kernel).
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        timed = graph.replay
+        timed()
+        torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.iters)]
     for e0, e1 in evs:
         if flush is not None:
             flush.zero_()
         e0.record()
-        run()
+        timed()
         e1.record()
     torch.cuda.synchronize()
     times = [e0.elapsed_time(e1) for e0, e1 in evs]

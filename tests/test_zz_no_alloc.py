@@ -58,9 +58,10 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(ops):
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch(ops):
-    # M = 256, N = 4096, K = 14336 needs ~16 MiB of split-K partials: more
-    # than the fixed scratch, so the call must refuse before launching.
-    M, N, K = 256, 4096, 14336
+    # M = 128, N = 2048, K = 16384 splits K nine ways: ~9.4 MB of split-K
+    # partials, more than the fixed scratch, so the call must refuse before
+    # launching.
+    M, N, K = 128, 2048, 16384
     qa = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
     sa = torch.ones((K // 128, M), dtype=torch.float32, device="cuda")
     qw = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
