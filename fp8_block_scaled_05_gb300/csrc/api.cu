@@ -131,11 +131,21 @@ fp8_status check_mode(int mode) { return (mode == FP8_SCALE_FP32_AMAX || mode ==
 
 constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_MASK;
 
+// Path of a dense GEMM: the one forced by the flags, else the skinny kernel
+// for M <= 256, else the MX kernel when the caller promises power-of-two
+// scales and the promote kernel otherwise.
 uint32_t plan_path(int64_t M, int64_t K, uint32_t flags) {
     const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
     if (forced != FP8_GEMM_PATH_AUTO) return forced;
     if (M <= 256 && K <= 128 * 1024) return FP8_GEMM_PATH_SKINNY;
-    return FP8_GEMM_PATH_PROMOTE;
+    return (flags & FP8_GEMM_SCALES_POW2) ? FP8_GEMM_PATH_MX : FP8_GEMM_PATH_PROMOTE;
+}
+
+// Path of a grouped GEMM: forced, else MX for power-of-two scales, else promote.
+uint32_t grouped_path(uint32_t flags) {
+    const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
+    if (forced != FP8_GEMM_PATH_AUTO) return forced;
+    return (flags & FP8_GEMM_SCALES_POW2) ? FP8_GEMM_PATH_MX : FP8_GEMM_PATH_PROMOTE;
 }
 
 // Shared validation of the GEMM operands (both forms).
@@ -254,7 +264,6 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     if (ldb < K) return FP8_ERR_SHAPE;
     if (ldb % 16) return FP8_ERR_ALIGN;
     const uint32_t path = plan_path(M, K, flags);
-    if (path == FP8_GEMM_PATH_MX) return FP8_ERR_NOT_IMPLEMENTED;
     if (path == FP8_GEMM_PATH_SKINNY && (M > 256 || K / 128 > 1024)) return FP8_ERR_SHAPE;
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
@@ -290,14 +299,15 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
             return e;
         return cuda_status(launch_gemm_skinny(a, st));
     }
-    a.bn = promote_tile_n(M, N, K, 1);
+    const bool mx = path == FP8_GEMM_PATH_MX;
+    a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
     if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
-    return cuda_status(launch_gemm_promote(a, st));
+    return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
 fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,
@@ -308,8 +318,8 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     (void)ws_bytes;
     if (G < 1 || G > 1024) return FP8_ERR_SHAPE;
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M_total, N, K, flags)) return e;
-    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
-    if (path != FP8_GEMM_PATH_AUTO && path != FP8_GEMM_PATH_PROMOTE) return FP8_ERR_NOT_IMPLEMENTED;
+    const uint32_t path = grouped_path(flags);
+    if (path == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
     if (M_total == 0) return FP8_OK;
     if (!offsets) return FP8_ERR_NULL;
     if ((int64_t)G * N > INT32_MAX) return FP8_ERR_SHAPE;
@@ -329,14 +339,16 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.status = d->status;
     a.sm_count = d->sm_count;
     a.splits = 1;
-    a.bn = promote_tile_n(M_total, N, K, G);
+    const bool mx = path == FP8_GEMM_PATH_MX;
+    a.bn = mx ? 256 : promote_tile_n(M_total, N, K, G);
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M_total, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
     if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, (uint64_t)G * N, K, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
-    return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
 fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,

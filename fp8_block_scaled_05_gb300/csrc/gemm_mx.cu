@@ -1,0 +1,374 @@
+// Block-scaled FP8 GEMM for power-of-two scales, dense and grouped (MoE),
+// with the scales applied by the tensor core itself.
+//
+//   C[m, n] = bf16( sum_kb sA[kb, m] * sB[n/128, kb] * P[m, n, kb] ),
+//   P[m, n, kb] = sum_{k in kb} dec(qa[m, k]) dec(qb[n, k])
+//
+// The same layer as the promote kernel; it applies when every scale is a
+// power of two, the option that restricts FP8 scale factors to powers of two
+// (upppp.jp NeMo RL FP8 article, §設定方法; greentreeone.com page, §Почему
+// это важно).  A power of two is exactly a UE8M0 scale factor, so
+// tcgen05.mma kind::mxf8f6f4.block_scale multiplies each 32-wide K slice by
+// 2^(ea + eb - 254) inside the tensor core and the whole K range accumulates
+// in one fp32 TMEM accumulator: there is no per-K-block promotion.  Each
+// 1x128 (activation) or 128x128 (weight) scale is used by the four K = 32
+// instructions of its K-block.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles, 16 warps):
+//   warp 0      TMA producer: qa tile 128x128 and qb tile 256x128 per K-block
+//               into a 4-stage, 192 KB shared-memory ring (128-byte swizzle).
+//   warp 1      MMA issuer (one thread) and TMEM owner: four tcgen05.mma
+//               (M=128, N=256, K=32) per K-block into the accumulator, TMEM
+//               columns [0, 256).
+//   warps 4..7  scale-factor writers, one per TMEM lane quarter: for each
+//               group of four K-blocks they convert the scales to UE8M0
+//               bytes (byte j = K-block 4g + j, selected per instruction by
+//               the descriptor's scale-factor id) and store them with
+//               tcgen05.st into a 4-slot ring at TMEM columns [256, 320):
+//               A's scale of row m in lane m, column m/32 of the slot; B's
+//               scale of weight row n in lane 32q + n%32, column 8 + n/32,
+//               in every lane quarter q.  A scale that is not a power of two
+//               in [2^-127, 2^127] is reported in the status word.
+//   warps 8..15 epilogue, two per lane quarter (128 columns each): once per
+//               tile they read the accumulator in two 64-column round trips,
+//               hand TMEM back after the second (the next tile's MMAs start
+//               while they finish storing) and store bf16 rows; 128 registers
+//               per thread (512-thread CTA).
+// Every wait is bounded; a wait that runs out records a timeout in the status
+// word and the kernel unwinds (waiting, bounded, for its own copies and MMAs).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace fp8bs {
+namespace mx {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int STAGES = 4;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int KB_PER_SF = 4;                     // K-blocks per scale-factor group (one byte each)
+constexpr int SF_SLOTS = 4;                      // scale-factor groups in flight
+constexpr uint32_t SF_COL0 = 256;                // first TMEM column of the scale-factor ring
+constexpr uint32_t SF_SLOT_COLS = 16;            // A: columns +0..+3, B: columns +8..+15
+constexpr int SF_WARP0 = 4;
+constexpr int EPI_WARP0 = 8, EPI_WARPS = 8;
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 512
+constexpr int MAX_GROUPS = 1024;
+constexpr uint32_t IDESC = idesc_mx_e4m3(BM, BN, 0, 0);
+static_assert(SF_COL0 + SF_SLOTS * SF_SLOT_COLS <= 512, "TMEM columns");
+
+// Status word code for a scale that is not an exact power of two (the value
+// of FP8_ERR_SCALE_MODE).
+constexpr int kStatusBadScale = 4;
+
+struct __align__(16) Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t sfull[SF_SLOTS];
+    uint64_t sempty[SF_SLOTS];
+    uint64_t tfull;
+    uint64_t tempty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t n_tiles;
+};
+
+constexpr size_t SMEM_BYTES =
+    1024 /*align slack*/ + (size_t)RING_BYTES + sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+
+__device__ __forceinline__ void record(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Two fp32 bit patterns -> a packed bf16 pair (round to nearest even), `lo`
+// in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
+}
+
+// fp32 power of two -> UE8M0 byte (2^(e-127)); 2^-127 is the fp32 subnormal
+// 0x00400000, whose exponent field 0 is the right byte.  `bad` is set for
+// anything else (zero, negative, non-power-of-two, inf, NaN).
+__device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
+    const uint32_t b = __float_as_uint(s);
+    const uint32_t e = b >> 23;
+    const bool ok = ((b & 0x7FFFFFu) == 0u && e >= 1u && e <= 254u) || b == 0x00400000u;
+    bad |= !ok;
+    return ok ? e : 127u;
+}
+
+template <bool GROUPED>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
+              int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)RING_BYTES);
+    int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
+    int32_t* glo = cum + (MAX_GROUPS + 1);
+    int32_t* ghi = glo + (MAX_GROUPS + 1);
+
+    const int warp = (int)warp_id(), lane = (int)lane_id();
+    const int KB = K / BK;
+    const int NT = (N + BN - 1) / BN;
+    const int NB = N / 128;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int s = 0; s < SF_SLOTS; ++s) {
+            mbar_init(&ctl->sfull[s], 4);   // one arrival per scale-factor warp
+            mbar_init(&ctl->sempty[s], 1);
+        }
+        mbar_init(&ctl->tfull, 1);
+        mbar_init(&ctl->tempty, EPI_WARPS);
+        mbar_init(&ctl->mma_done, 1);
+        mbar_init_fence();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 3) {
+        if (GROUPED) {
+            const int total = build_group_table<BM>(offsets, G, M, NT, cum, glo, ghi);
+            if (lane == 0) ctl->n_tiles = total;
+        } else if (lane == 0) {
+            ctl->n_tiles = ((M + BM - 1) / BM) * NT;
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int n_tiles = ctl->n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sA = smem + (size_t)s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);
+                    tma_load_2d(sA, &tm_a, &ctl->full[s], kb * BK, tl.m0);
+                    tma_load_2d(sA + A_BYTES, &tm_b, &ctl->full[s], kb * BK, tl.brow);
+                }
+            }
+            if (!ok) {
+                record(status, kStatusTimeout);
+                // Let the copies already issued land before the CTA can exit.
+                const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+                for (uint32_t j = it - n; j < it; ++j)
+                    mbar_wait(&ctl->full[j % STAGES], (j / STAGES) & 1, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, gi = 0, tt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tt) {
+                // The accumulator is free once the epilogue has copied the
+                // previous tile out of it.
+                if (!mbar_wait(&ctl->tempty, (tt & 1) ^ 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                uint32_t slot = 0;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
+                    const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+                    if (byte == 0) {
+                        slot = gi % SF_SLOTS;
+                        if (!mbar_wait(&ctl->sfull[slot], (gi / SF_SLOTS) & 1, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!mbar_wait(&ctl->full[s], ph, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sA = smem_u32(smem + (size_t)s * STAGE_BYTES);
+                    const uint64_t adesc = sdesc_kmajor_sw128(sA);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sA + A_BYTES);
+                    const uint32_t sfa = tmem_base + SF_COL0 + slot * SF_SLOT_COLS;
+                    const uint32_t idesc = IDESC | (byte << 4) | (byte << 29);   // B, A scale-factor byte id
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        umma_mxf8f6f4(tmem_base, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc, sfa,
+                                      sfa + 8, (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(&ctl->empty[s]);
+                    if (byte == KB_PER_SF - 1 || kb == KB - 1) {
+                        umma_commit(&ctl->sempty[slot]);
+                        ++gi;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&ctl->tfull);
+            }
+            if (!ok) record(status, kStatusTimeout);
+            // All MMAs this thread issued are complete before TMEM is released.
+            umma_commit(&ctl->mma_done);
+            mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
+        // ------------------------------------------------ scale-factor writers
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        uint32_t gi = 0;
+        bool ok = true, bad = false;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const int m = tl.m0 + q * 32 + lane;
+            const bool vrow = m < tl.row_end;
+            const int nb0 = tl.n0 / 128;
+            const float* sb0 = sb + ((size_t)tl.g * NB + nb0) * KB;
+            for (int kb0 = 0; kb0 < KB; kb0 += KB_PER_SF, ++gi) {
+                // Scales first (their latency overlaps the wait for the slot).
+                float fa[KB_PER_SF], fb0[KB_PER_SF], fb1[KB_PER_SF];
+#pragma unroll
+                for (int j = 0; j < KB_PER_SF; ++j) {
+                    const int kb = kb0 + j;
+                    fa[j] = (kb < KB && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
+                    fb0[j] = kb < KB ? sb0[kb] : 1.0f;
+                    fb1[j] = (kb < KB && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
+                }
+                uint32_t wa = 0, wb0 = 0, wb1 = 0;
+#pragma unroll
+                for (int j = 0; j < KB_PER_SF; ++j) {
+                    wa |= ue8m0(fa[j], bad) << (8 * j);
+                    wb0 |= ue8m0(fb0[j], bad) << (8 * j);
+                    wb1 |= ue8m0(fb1[j], bad) << (8 * j);
+                }
+                const uint32_t slot = gi % SF_SLOTS;
+                bool got = mbar_wait(&ctl->sempty[slot], ((gi / SF_SLOTS) & 1) ^ 1, kWaitLimitNs);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t col = tmem_base + lane_base + SF_COL0 + slot * SF_SLOT_COLS;
+                const uint32_t vb[8] = {wb0, wb0, wb0, wb0, wb1, wb1, wb1, wb1};
+                tmem_st_x1(col + (uint32_t)q, wa);
+                tmem_st_x8(col + 8, vb);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sfull[slot]);
+            }
+        }
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) record(status, kStatusBadScale);
+        if (!ok && lane == 0) record(status, kStatusTimeout);
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quarter this warp may access
+        const int h = (warp - EPI_WARP0) >> 2;   // column half of the tile
+        uint32_t tt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tt) {
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const int m = tl.m0 + q * 32 + lane;
+            const int col0 = tl.n0 + h * 128;
+            bool got = mbar_wait(&ctl->tfull, tt & 1, kWaitLimitNs);
+            got = __all_sync(0xFFFFFFFFu, got);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+            // Two round trips of 64 columns; the first half is stored while the
+            // second is read, and TMEM is handed back as soon as the second
+            // round trip has landed.
+            const bool store = m < tl.row_end && col0 < N;
+            uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_x32(taddr + 64 * r, v0);
+                tmem_ld_x32(taddr + 64 * r + 32, v1);
+                tmem_ld_wait();
+                if (r == 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tempty);
+                }
+                uint32_t p[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+                    p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+                }
+                if (store) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[8 * r + j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                }
+            }
+        }
+        if (!ok && lane == 0) record(status, kStatusTimeout);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <bool GROUPED>
+cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
+    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    auto kern = k_gemm_mx<GROUPED>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done_mask & (1 << (dev & 31)))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done_mask |= 1 << (dev & 31);
+    }
+    const int64_t NT = (a.N + BN - 1) / BN;
+    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
+    const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(*a.tm_a, *a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
+                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace mx
+
+cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st) {
+    if (a.M == 0) return cudaSuccess;
+    return a.offsets != nullptr ? mx::launch<true>(a, st) : mx::launch<false>(a, st);
+}
+
+}  // namespace fp8bs

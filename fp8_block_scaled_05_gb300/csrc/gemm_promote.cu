@@ -44,6 +44,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace fp8bs {
 namespace promote {
@@ -103,44 +104,6 @@ struct __align__(16) Ctrl {
 constexpr size_t SMEM_BYTES =
     1024 /*align slack*/ + (size_t)RING_BYTES + sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
 
-struct Tile {
-    int32_t m0, row_end, brow, n0, g;
-};
-
-// Tile t -> coordinates.  Dense: m-tiles vary fastest so that CTAs running at
-// the same time share the weight tile.  Grouped: tiles of expert g follow
-// those of expert g-1; inside an expert, m-tiles vary fastest.
-template <int BN, bool GROUPED>
-__device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* cum, const int32_t* glo,
-                                            const int32_t* ghi, int G) {
-    Tile r;
-    if (!GROUPED) {
-        const int MT = (M + BM - 1) / BM;
-        const int mt = t % MT, nt = t / MT;
-        r.m0 = mt * BM;
-        r.row_end = M;
-        r.brow = nt * BN;
-        r.n0 = nt * BN;
-        r.g = 0;
-    } else {
-        int lo = 0, hi = G;   // largest g with cum[g] <= t
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cum[mid] <= t) lo = mid; else hi = mid;
-        }
-        const int g = lo;
-        const int local = t - cum[g];
-        const int MTg = (ghi[g] - glo[g] + BM - 1) / BM;
-        const int mt = local % MTg, nt = local / MTg;
-        r.m0 = glo[g] + mt * BM;
-        r.row_end = ghi[g];
-        r.brow = g * N + nt * BN;
-        r.n0 = nt * BN;
-        r.g = g;
-    }
-    return r;
-}
-
 __device__ __forceinline__ void record_timeout(int* status) {
     if (status) atomicCAS(status, 0, kStatusTimeout);
 }
@@ -195,29 +158,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     }
     if (warp == 3) {
         if (GROUPED) {
-            // Per-expert row ranges (clamped to [0, M]) and the running tile count.
-            int carry = 0;
-            if (lane == 0) cum[0] = 0;
-            for (int g0 = 0; g0 < G; g0 += 32) {
-                const int g = g0 + lane;
-                int lo = 0, hi = 0, tiles = 0;
-                if (g < G) {
-                    lo = min(max(offsets[g], 0), M);
-                    hi = min(max(offsets[g + 1], lo), M);
-                    tiles = ((hi - lo + BM - 1) / BM) * NT;
-                    glo[g] = lo;
-                    ghi[g] = hi;
-                }
-                int incl = tiles;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                if (g < G) cum[g + 1] = carry + incl;
-                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            if (lane == 0) ctl->n_tiles = carry;
+            const int total = build_group_table<BM>(offsets, G, M, NT, cum, glo, ghi);
+            if (lane == 0) ctl->n_tiles = total;
         } else if (lane == 0) {
             ctl->n_tiles = ((M + BM - 1) / BM) * NT;
         }
@@ -238,7 +180,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
@@ -311,7 +253,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         uint32_t sit = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
             const int nb0 = tl.n0 / 128;
             for (int kb = 0; kb < KB; ++kb, ++sit) {
                 const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
@@ -355,7 +297,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         bool ok = true;
         bool ready = false;   // tfull of K-block kbg already seen complete (early probe)
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
             const int m = tl.m0 + row_in_tile;
             const int col0 = tl.n0 + sl * C::EPI_COLS;
             const bool vrow = m < tl.row_end;

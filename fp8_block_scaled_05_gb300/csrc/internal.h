@@ -53,6 +53,12 @@ struct GemmArgs {
 int promote_tile_n(int64_t M, int64_t N, int64_t K, int32_t G);
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st);
 
+// Dense / grouped kernel for power-of-two scales: the tensor core applies the
+// scales as UE8M0 block scale factors (tcgen05.mma kind::mxf8f6f4); output
+// tile 128 x 256, a.tm_b with box {128, 256}.  Every scale must be a power of
+// two in [2^-127, 2^127]; others are reported in the status word.
+cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st);
+
 // Skinny (decode) kernel: weights on the MMA's M side, tokens on N, split-K.
 int skinny_tile_n(int64_t M);                         // padded token count, 0 if M > 256
 int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count);

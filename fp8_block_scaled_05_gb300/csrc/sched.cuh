@@ -1,0 +1,78 @@
+// Output-tile schedule shared by the persistent large-M GEMM kernels (dense
+// and grouped): tile index -> (rows, weight rows, output columns, expert).
+#pragma once
+#include <cstdint>
+
+namespace fp8bs {
+
+struct Tile {
+    int32_t m0, row_end, brow, n0, g;
+};
+
+// Tile t -> coordinates.  Dense: m-tiles vary fastest so that CTAs running at
+// the same time share the weight tile.  Grouped: tiles of expert g follow
+// those of expert g-1; inside an expert, m-tiles vary fastest.  cum[g] is the
+// number of tiles of experts before g; [glo[g], ghi[g]) are g's rows.
+template <int BM, int BN, bool GROUPED>
+__device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* cum, const int32_t* glo,
+                                            const int32_t* ghi, int G) {
+    Tile r;
+    if (!GROUPED) {
+        const int MT = (M + BM - 1) / BM;
+        const int mt = t % MT, nt = t / MT;
+        r.m0 = mt * BM;
+        r.row_end = M;
+        r.brow = nt * BN;
+        r.n0 = nt * BN;
+        r.g = 0;
+    } else {
+        int lo = 0, hi = G;   // largest g with cum[g] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int g = lo;
+        const int local = t - cum[g];
+        const int MTg = (ghi[g] - glo[g] + BM - 1) / BM;
+        const int mt = local % MTg, nt = local / MTg;
+        r.m0 = glo[g] + mt * BM;
+        r.row_end = ghi[g];
+        r.brow = g * N + nt * BN;
+        r.n0 = nt * BN;
+        r.g = g;
+    }
+    return r;
+}
+
+// Executed by one whole warp: per-expert row ranges (offsets clamped to
+// [0, M], each range starting where the previous ends or later) and the
+// running tile count; returns the total number of tiles on every lane.
+template <int BM>
+__device__ __forceinline__ int build_group_table(const int32_t* __restrict__ offsets, int G, int M, int NT,
+                                                 int32_t* cum, int32_t* glo, int32_t* ghi) {
+    const int lane = threadIdx.x & 31;
+    int carry = 0;
+    if (lane == 0) cum[0] = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        int tiles = 0;
+        if (g < G) {
+            const int lo = min(max(offsets[g], 0), M);
+            const int hi = min(max(offsets[g + 1], lo), M);
+            tiles = ((hi - lo + BM - 1) / BM) * NT;
+            glo[g] = lo;
+            ghi[g] = hi;
+        }
+        int incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (g < G) cum[g + 1] = carry + incl;
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    return carry;
+}
+
+}  // namespace fp8bs

@@ -73,8 +73,10 @@ def main(argv=None):
         qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
         qw = torch.randint(0, 0x7E, (G, N, K), dtype=torch.uint8, device=dev, generator=g)
         sw = torch.rand((G, N // 128, K // 128), generator=g, device=dev) * 1e-3
+        if a.pow2:
+            sw = torch.exp2(torch.ceil(torch.log2(sw)))
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        run = lambda: ops.grouped_gemm(qa, sa, offs, qw, sw, a.pow2, out=c)  # noqa: E731
+        run = lambda: ops.grouped_gemm(qa, sa, offs, qw, sw, a.pow2, a.path, out=c)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
 
     for _ in range(max(a.warmup, 1)):

@@ -259,11 +259,12 @@ def gemm(qa, sa, qb, sb, pow2: bool = False, path: str = "auto", out: torch.Tens
     return c
 
 
-def grouped_gemm(qa, sa, offsets, qb, sb, pow2: bool = False, out=None, stream=None):
+def grouped_gemm(qa, sa, offsets, qb, sb, pow2: bool = False, path: str = "auto", out=None, stream=None):
+    """Grouped (per-expert) block-scaled GEMM; allocates C (bf16 [M, N])."""
     M, K = qa.shape
     N = qb.shape[1]
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    flags = FP8_GEMM_SCALES_POW2 if pow2 else 0
+    flags = PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0)
     fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags, None, stream)
     return c
 

@@ -124,11 +124,19 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  *   C[m, n] = bf16_RN( sum_kb  sA[kb, m] * sB[n/128, kb] * P[m, n, kb] ),
  *   P[m, n, kb] = sum_{k in kb} dec(qa[m, k]) * dec(qb[n, k])
  *
- * Each K-block's partial P is accumulated in fp32 by the tensor cores and
- * promoted into an fp32 running sum with the scale product (or, with
- * FP8_GEMM_SCALES_POW2 and the MX path, scaled by the hardware).  The order
- * of the fp32 additions is not specified; results agree with an exact
- * evaluation to fp32 accumulation error plus bf16 output rounding.
+ * Promote and skinny paths: each K-block's partial P is accumulated in fp32
+ * by the tensor cores and promoted into an fp32 running sum with the scale
+ * product.  MX path (power-of-two scales only): the tensor core applies the
+ * scales itself as UE8M0 block scale factors and accumulates the whole K range
+ * in fp32.  The order of the fp32 additions is not specified; results agree
+ * with an exact evaluation to fp32 accumulation error plus bf16 output
+ * rounding.
+ *
+ * Path choice with FP8_GEMM_PATH_AUTO: M <= 256 -> skinny; otherwise MX when
+ * FP8_GEMM_SCALES_POW2 is set, else promote.  FP8_GEMM_PATH_MX without
+ * FP8_GEMM_SCALES_POW2 returns FP8_ERR_SCALE_MODE.  On the MX path a scale that
+ * is not a power of two in [2^-127, 2^127] breaks the promise: the output is
+ * unspecified and the device status word reads FP8_ERR_SCALE_MODE.
  *
  * qa  device, uint8 [M, K], row pitch lda (>= K, % 16 == 0)
  * sa  device, fp32 [K/128][ldsa] as written by fp8_quant_act_1x128 (ldsa >= M, % 4 == 0)
@@ -165,6 +173,9 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
  * qb       device, uint8 [G][N][K] contiguous;  sb device fp32 [G][N/128][K/128] contiguous
  * c        device, bf16 [M_total, N], row pitch ldc
  * Empty experts are allowed.  G >= 1, N and K multiples of 128.
+ * flags: FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_AUTO, _PROMOTE or _MX (AUTO picks
+ *     MX when FP8_GEMM_SCALES_POW2 is set, else promote);
+ *     FP8_GEMM_PATH_SKINNY returns FP8_ERR_NOT_IMPLEMENTED.
  */
 FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
                                         const int32_t *offsets, int32_t G, int64_t M_total,
@@ -195,10 +206,12 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
  * - All calls share the array, and it keeps what the last call left in it.
  *   The call clears the ticket words on `stream` before its launch.  Calls
  *   that overlap on the GPU (unordered streams) race on the array: order them.
- * - The scratch needed is 256-byte-rounded 4*N/128 bytes of tickets plus
- *   splits * (N/128) * NT * 128 * 4 bytes of partials (NT = M rounded up to
- *   16, 32, 64, 128 or 256; splits as reported by fp8_gemm_plan).  Sizes that
- *   need more than 8 MiB return FP8_ERR_WORKSPACE without launching.
+ * - The scratch needed is 256-byte-rounded 4*T bytes of tickets plus
+ *   splits * T * NT * 128 * 4 bytes of partials, where NT = M rounded up to
+ *   16, 32, 64 or 128 (128 for M > 64), T = (N/128) * ceil(M / NT) (tokens
+ *   beyond 128 run as further 128-token chunks), and splits is as reported by
+ *   fp8_gemm_plan.  Sizes that need more than 8 MiB return
+ *   FP8_ERR_WORKSPACE without launching.
  *   M > 256 returns FP8_ERR_SHAPE.
  * - flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_SKINNY (plus FP8_GEMM_SCALES_POW2).
  */

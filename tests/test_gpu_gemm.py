@@ -50,8 +50,8 @@ def _run(ops, qa, sa, qw, sw, path, pow2=False):
     return bf16_to_np(c)
 
 
-@pytest.mark.parametrize("path", ["promote", "skinny"])
-@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("path,pow2", [("promote", False), ("promote", True), ("skinny", False),
+                                       ("skinny", True), ("mx", True)])
 def test_tiny(ops, path, pow2):
     case = I.tiny()
     qa, sa = O.quant_act_1x128(bf16_to_np(case.a), pow2)
@@ -76,7 +76,7 @@ def test_skinny_ragged(ops, M):
     assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"skinny M={M}")
 
 
-@pytest.mark.parametrize("path", ["promote", "skinny"])
+@pytest.mark.parametrize("path", ["promote", "skinny", "mx"])
 def test_exact_integer_gemm(ops, path):
     """Codes decoding to {-1, 0, 1}, K = 256, and a power-of-two scale that is
     the same for both K-blocks of a row (and of a weight tile row): every
@@ -92,8 +92,61 @@ def test_exact_integer_gemm(ops, path):
     ref = O.gemm_ref(qa, sa, qw, sw)
     ints = ref / (sa[:, :1].astype(np.float64) * np.repeat(sw[:, 0], 128)[None, :])
     assert np.array_equal(ints, np.round(ints)) and np.all(np.abs(ints) <= 256)
-    c = _run(ops, qa, sa, qw, sw, path)
+    c = _run(ops, qa, sa, qw, sw, path, pow2=path == "mx")
     assert np.array_equal(c, ref)
+
+
+# ------------------------------------------------------------ MX (pow2 scales)
+@pytest.mark.parametrize("M,N,K", [(300, 640, 1152), (128, 256, 128), (129, 128, 256), (513, 384, 512),
+                                   (1000, 1280, 384), (257, 768, 640), (1, 256, 256), (64, 512, 2048)])
+def test_mx_ragged(ops, M, N, K):
+    """Ragged M, N = 128 mod 256 (half-empty last tile), K-block counts that
+    are not multiples of the four scale bytes per TMEM word, M below 256."""
+    qa, sa, qw, sw = _case(M, N, K, seed=M + N + 1, pow2=True)
+    c = _run(ops, qa, sa, qw, sw, "mx", pow2=True)
+    assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"mx {M}x{N}x{K}")
+
+
+def test_mx_matches_promote_on_pow2_scales(ops):
+    """Both large-M kernels compute the same C from the same power-of-two
+    operands; each is within tolerance of the oracle and of the other."""
+    qa, sa, qw, sw = _case(384, 1024, 2048, seed=5, pow2=True)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    c_mx = _run(ops, qa, sa, qw, sw, "mx", pow2=True)
+    c_pr = _run(ops, qa, sa, qw, sw, "promote", pow2=True)
+    assert_gemm_close(c_mx, ref, "mx")
+    assert_gemm_close(c_pr, ref, "promote")
+    assert_gemm_close(c_mx, c_pr.astype(np.float64), "mx vs promote")
+
+
+def test_mx_extreme_scale_range(ops):
+    """Rows whose magnitudes span 2^-60 .. 2^60 (activation scales from
+    2^-69 to 2^52) against weights of 2^-20 .. 2^20 per 128-row block: the
+    hardware's UE8M0 exponents must reach both ends.  Checked row by row so
+    that small rows are not hidden behind large ones."""
+    M, N, K = 256, 512, 512
+    a = I.normal_bf16(I.stream(41, 1), (M, K)).float() * torch.exp2(torch.linspace(-60, 60, M).round())[:, None]
+    w = I.normal_bf16(I.stream(41, 2), (N, K)).float() * torch.exp2(torch.tensor([-20.0, -7.0, 9.0, 20.0])
+                                                                    ).repeat_interleave(128)[:, None]
+    qa, sa = O.quant_act_1x128(bf16_to_np(a.to(torch.bfloat16)), True)
+    qw, sw = O.quant_weight_128x128(bf16_to_np(w.to(torch.bfloat16)), True)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    c = _run(ops, qa, sa, qw, sw, "mx", pow2=True)
+    for r in range(M):
+        for nb in range(N // 128):
+            cols = slice(128 * nb, 128 * nb + 128)
+            assert_gemm_close(c[r, cols], ref[r, cols], f"mx row {r} block {nb}")
+
+
+@pytest.mark.parametrize("where", ["sa", "sb"])
+def test_mx_reports_a_scale_that_is_not_a_power_of_two(ops, where):
+    qa, sa, qw, sw = _case(256, 256, 512, seed=3, pow2=True)
+    dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
+    (dsa if where == "sa" else dsw).view(-1)[1] *= 0.75
+    ops.gemm(dqa, dsa, dqw, dsw, pow2=True, path="mx")
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 4   # FP8_ERR_SCALE_MODE
+    assert ops.fp8_last_device_status() == 0   # reading clears it
 
 
 def test_rejects_bad_arguments(ops):
@@ -111,15 +164,17 @@ def test_rejects_bad_arguments(ops):
 
 
 # ------------------------------------------------------------ full sizes
-@pytest.mark.parametrize("layer", ["qkv", "down"])
-def test_llama_full_size_sampled_rows(ops, layer):
-    """Llama-3.1-8B layer shapes, whole path on the GPU (quantisers + GEMM),
-    checked on sampled output rows against the oracle."""
+@pytest.mark.parametrize("layer,pow2", [("qkv", False), ("down", False), ("gate_up", True), ("down", True)])
+def test_llama_full_size_sampled_rows(ops, layer, pow2):
+    """Llama-3.1-8B layer shapes, whole path on the GPU (quantisers + GEMM;
+    power-of-two scales take the MX kernel), checked on sampled output rows
+    against the oracle."""
     case = I.llama8b_layers(layers=[layer])[0]
-    y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda())
+    y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda(), pow2=pow2)
     torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
     rows = np.sort(np.random.Generator(np.random.PCG64(8)).choice(case.a.shape[0], 24, replace=False))
-    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]))
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
     qw_o, sw_o = qw.cpu().numpy(), sw.cpu().numpy()
     ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
@@ -139,50 +194,57 @@ def test_decode_full_size(ops, M):
 
 
 # ------------------------------------------------------------ grouped
-def _grouped_inputs(offsets, N, K, seed):
+def _grouped_inputs(offsets, N, K, seed, pow2=False):
     G = len(offsets) - 1
     M = int(offsets[-1])
     a = I.normal_bf16(I.stream(seed, 1), (M, K))
     w = I.normal_bf16(I.stream(seed, 2), (G, N, K), std=0.02)
-    qa, sa = O.quant_act_1x128(bf16_to_np(a))
-    qs = [O.quant_weight_128x128(bf16_to_np(w[g])) for g in range(G)]
+    qa, sa = O.quant_act_1x128(bf16_to_np(a), pow2)
+    qs = [O.quant_weight_128x128(bf16_to_np(w[g]), pow2) for g in range(G)]
     qw = np.stack([q for q, _ in qs])
     sw = np.stack([s for _, s in qs])
     return qa, sa, qw, sw
 
 
-def _run_grouped(ops, qa, sa, offsets, qw, sw):
+def _run_grouped(ops, qa, sa, offsets, qw, sw, pow2=False, path="auto"):
     dqa, dsa, _, _ = _to_dev(qa, sa, qw[0], sw[0])
     c = ops.grouped_gemm(dqa, dsa, torch.tensor(offsets, dtype=torch.int32, device="cuda"),
-                         torch.from_numpy(qw).cuda(), torch.from_numpy(sw).cuda())
+                         torch.from_numpy(qw).cuda(), torch.from_numpy(sw).cuda(), pow2, path)
     torch.cuda.synchronize()
     assert ops.fp8_last_device_status() == 0
     return bf16_to_np(c)
 
 
+@pytest.mark.parametrize("path", ["promote", "mx"])
 @pytest.mark.parametrize("offsets", [[0, 5, 5, 140, 140, 300, 301], [0, 0, 0, 128], [0, 1000],
                                      [0, 129, 258, 387, 516]])
-def test_grouped_ragged_with_empty_experts(ops, offsets):
+def test_grouped_ragged_with_empty_experts(ops, offsets, path):
+    # N = 384: the MX kernel's 256-wide tiles end half outside an expert's
+    # weights (the extra rows belong to the next expert or lie past the end).
     N, K = 384, 512
-    qa, sa, qw, sw = _grouped_inputs(offsets, N, K, seed=len(offsets))
-    c = _run_grouped(ops, qa, sa, offsets, qw, sw)
-    assert_gemm_close(c, O.grouped_gemm_ref(qa, sa, offsets, qw, sw), f"grouped {offsets}")
+    pow2 = path == "mx"
+    qa, sa, qw, sw = _grouped_inputs(offsets, N, K, seed=len(offsets), pow2=pow2)
+    c = _run_grouped(ops, qa, sa, offsets, qw, sw, pow2, path)
+    assert_gemm_close(c, O.grouped_gemm_ref(qa, sa, offsets, qw, sw), f"grouped {path} {offsets}")
 
 
-def test_grouped_moe_full_size_sampled_rows(ops):
-    """Qwen3-30B-A3B-shaped experts (gate+up: K 2048, N 1536), Zipf routing."""
+@pytest.mark.parametrize("pow2", [False, True])
+def test_grouped_moe_full_size_sampled_rows(ops, pow2):
+    """Qwen3-30B-A3B-shaped experts (gate+up: K 2048, N 1536), Zipf routing;
+    power-of-two scales take the MX kernel."""
     m = I.moe_case(with_weights=False)
     G, N, K = 128, 1536, 2048
     w = I.normal_bf16(I.stream(0, 82), (G, N, K), std=0.02)
     x = m.a_gate_up.cuda()
-    qa, sa = ops.quant_act(x)
+    qa, sa = ops.quant_act(x, pow2)
     qw = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
     sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
     wd = w.cuda()
+    mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
     for g in range(G):
-        ops.fp8_quant_weight_128x128(wd[g], qw[g], sw[g])
+        ops.fp8_quant_weight_128x128(wd[g], qw[g], sw[g], mode)
     offs = torch.from_numpy(m.offsets).cuda()
-    c = ops.grouped_gemm(qa, sa, offs, qw, sw)
+    c = ops.grouped_gemm(qa, sa, offs, qw, sw, pow2)
     torch.cuda.synchronize()
     assert ops.fp8_last_device_status() == 0
     rng = np.random.Generator(np.random.PCG64(9))
@@ -190,7 +252,7 @@ def test_grouped_moe_full_size_sampled_rows(ops):
     # include the first and last row of a few experts (tile edges)
     rows = np.unique(np.concatenate([rows, m.offsets[1:6] - 1, m.offsets[:5]]))
     rows = rows[rows < x.shape[0]]
-    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_gate_up[rows]))
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_gate_up[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
     grp = np.searchsorted(m.offsets, rows, side="right") - 1
     qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
