@@ -92,10 +92,11 @@ std::mutex g_tm_mu;
 std::unordered_map<TmKey, CUtensorMap, TmKeyHash> g_tm_cache;
 
 // 2-D row-major tensor [d1 rows][d0 elements], row pitch in bytes, box
-// {b0, b1}.  Descriptors are cached by all of these; entries stay valid
-// because a descriptor depends on nothing else.
+// {b0, b1}.  Descriptors are cached by all of these (a descriptor depends on
+// nothing else) and copied out under the lock, so a later eviction of the
+// cache cannot invalidate a caller's copy.
 fp8_status tensor_map(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t pitch_bytes,
-                      uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz, const CUtensorMap** out) {
+                      uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz, CUtensorMap* out) {
     TmKey key;
     std::memset(&key, 0, sizeof(key));
     key.ptr = reinterpret_cast<uint64_t>(ptr);
@@ -109,7 +110,7 @@ fp8_status tensor_map(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, u
     std::lock_guard<std::mutex> lk(g_tm_mu);
     auto it = g_tm_cache.find(key);
     if (it != g_tm_cache.end()) {
-        *out = &it->second;
+        *out = it->second;
         return FP8_OK;
     }
     if (g_tm_cache.size() > 4096) g_tm_cache.clear();
@@ -122,8 +123,8 @@ fp8_status tensor_map(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, u
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return FP8_ERR_CUDA;
-    auto ins = g_tm_cache.emplace(key, m);
-    *out = &ins.first->second;
+    g_tm_cache.emplace(key, m);
+    *out = m;
     return FP8_OK;
 }
 
@@ -301,6 +302,11 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
+    if (mx) {
+        if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
+                                      CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+            return e;
+    }
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
@@ -341,6 +347,11 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.splits = 1;
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M_total, N, K, G);
+    if (mx) {
+        if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M_total, ldc * 2, 32, 32,
+                                      CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+            return e;
+    }
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M_total, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;

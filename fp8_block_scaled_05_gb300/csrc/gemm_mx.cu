@@ -20,6 +20,13 @@
 //   warp 1      MMA issuer (one thread) and TMEM owner: four tcgen05.mma
 //               (M=128, N=256, K=32) per K-block into the accumulator, TMEM
 //               columns [0, 256).
+//   warp 2      gatekeeper (one thread): does every barrier wait the MMAs
+//               depend on (operands landed, scale factors written, the
+//               accumulator drained) and publishes the count of K-blocks
+//               ready in a shared word.  The issuer only polls that word: a
+//               barrier test costs ~200 cycles, and one thread that both
+//               waited and issued left the tensor core idle for about 40% of
+//               each K-block's 512 cycles.
 //   warps 4..7  scale-factor writers, one per TMEM lane quarter: for each
 //               group of four K-blocks they convert the scales to UE8M0
 //               bytes (byte j = K-block 4g + j, selected per instruction by
@@ -30,10 +37,16 @@
 //               in every lane quarter q.  A scale that is not a power of two
 //               in [2^-127, 2^127] is reported in the status word.
 //   warps 8..15 epilogue, two per lane quarter (128 columns each): once per
-//               tile they read the accumulator in two 64-column round trips,
-//               hand TMEM back after the second (the next tile's MMAs start
-//               while they finish storing) and store bf16 rows; 128 registers
-//               per thread (512-thread CTA).
+//               tile they read the accumulator in three round trips, packing
+//               it to bf16, hand TMEM back (the next tile's MMAs start
+//               while they store) and write the 32 x 128 block as four 32 x 32
+//               TMA stores through a 2 KB shared-memory buffer per warp
+//               (64-byte swizzle, so the row-per-thread writes into it are
+//               free of bank conflicts).  Stores straight from registers, one
+//               16-byte piece of 32 different rows per instruction, slowed the
+//               whole kernel by a quarter.  A grouped tile that ends inside an
+//               expert stores its rows one by one instead, up to the expert's
+//               last row (a TMA store would clip only at M).
 // Every wait is bounded; a wait that runs out records a timeout in the status
 // word and the kernel unwinds (waiting, bounded, for its own copies and MMAs).
 #include <cstdint>
@@ -53,10 +66,12 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int STAGES = 4;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int EPI_BUF_BYTES = 32 * 64;           // one 32 x 32 bf16 block per epilogue warp
 constexpr int KB_PER_SF = 4;                     // K-blocks per scale-factor group (one byte each)
 constexpr int SF_SLOTS = 4;                      // scale-factor groups in flight
 constexpr uint32_t SF_COL0 = 256;                // first TMEM column of the scale-factor ring
 constexpr uint32_t SF_SLOT_COLS = 16;            // A: columns +0..+3, B: columns +8..+15
+constexpr int GATE_WARP = 2;
 constexpr int SF_WARP0 = 4;
 constexpr int EPI_WARP0 = 8, EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 512
@@ -78,10 +93,13 @@ struct __align__(16) Ctrl {
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t n_tiles;
+    uint32_t ready;      // K-blocks (counted over this CTA's tiles) cleared for issue
+    uint32_t pad_;
 };
 
-constexpr size_t SMEM_BYTES =
-    1024 /*align slack*/ + (size_t)RING_BYTES + sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)RING_BYTES + (size_t)EPI_WARPS * EPI_BUF_BYTES +
+                               sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
@@ -109,11 +127,12 @@ __device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
 template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
+              const __grid_constant__ CUtensorMap tm_c, const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
               int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)RING_BYTES);
+    uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)EPI_WARPS * EPI_BUF_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
     int32_t* glo = cum + (MAX_GROUPS + 1);
     int32_t* ghi = glo + (MAX_GROUPS + 1);
@@ -135,9 +154,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(&ctl->tfull, 1);
         mbar_init(&ctl->tempty, EPI_WARPS);
         mbar_init(&ctl->mma_done, 1);
+        ctl->ready = 0;
         mbar_init_fence();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_c);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, 512);
@@ -185,8 +206,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == GATE_WARP) {
+        // ------------------------------------------------ gatekeeper
         if (lane == 0) {
             uint32_t it = 0, gi = 0, tt = 0;
             bool ok = true;
@@ -197,19 +218,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
-                uint32_t slot = 0;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     const uint32_t byte = (uint32_t)kb % KB_PER_SF;
-                    if (byte == 0) {
-                        slot = gi % SF_SLOTS;
-                        if (!mbar_wait(&ctl->sfull[slot], (gi / SF_SLOTS) & 1, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
+                    if (byte == 0 && !mbar_wait(&ctl->sfull[gi % SF_SLOTS], (gi / SF_SLOTS) & 1, kWaitLimitNs)) {
+                        ok = false;
+                        break;
                     }
-                    if (!mbar_wait(&ctl->full[s], ph, kWaitLimitNs)) {
+                    if (!mbar_wait(&ctl->full[it % STAGES], (it / STAGES) & 1, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_shared(&ctl->ready, it + 1);
+                    if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
+                }
+            }
+            if (!ok) record(status, kStatusTimeout);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, gi = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+                    const uint32_t slot = gi % SF_SLOTS;
+                    if (!wait_counter(&ctl->ready, it + 1, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -305,35 +341,63 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
-            // Two round trips of 64 columns; the first half is stored while the
-            // second is read, and TMEM is handed back as soon as the second
-            // round trip has landed.
-            const bool store = m < tl.row_end && col0 < N;
-            uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            // Three round trips (64, 32 and 32 columns), packed to bf16 pairs as
+            // they arrive so that at most 64 raw values are live; TMEM goes back
+            // before any store.
+            uint32_t p[64];
+            {
                 uint32_t v0[32], v1[32];
-                tmem_ld_x32(taddr + 64 * r, v0);
-                tmem_ld_x32(taddr + 64 * r + 32, v1);
+                tmem_ld_x32(taddr, v0);
+                tmem_ld_x32(taddr + 32, v1);
                 tmem_ld_wait();
-                if (r == 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->tempty);
-                }
-                uint32_t p[32];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
                     p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
                 }
-                if (store) {
+            }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[8 * r + j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            for (int r = 2; r < 4; ++r) {
+                uint32_t v[32];
+                tmem_ld_x32(taddr + 32 * r, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) p[16 * r + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty);
+            if (col0 >= N) continue;   // the half of a 256-wide tile past N
+            const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
+            if (!GROUPED || rows_here == 32) {
+                // Row `lane` of the block, 16-byte piece k of 32-column chunk cc,
+                // goes to offset lane*64 + ((k ^ ((lane >> 1) & 3)) << 4): the
+                // 64-byte swizzle the tensor map declares.
+                uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j = 16 * cc + 4 * k;
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(p[j], p[j + 1], p[j + 2], p[j + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, tl.m0 + q * 32);
+                        bulk_commit_group();
+                    }
                 }
+            } else if (lane < rows_here) {
+                uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
             }
         }
+        if (lane == 0) bulk_wait_group<0>();   // stores complete before the CTA exits
         if (!ok && lane == 0) record(status, kStatusTimeout);
     }
 
@@ -359,7 +423,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(*a.tm_a, *a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
                                             (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
     return cudaGetLastError();
 }

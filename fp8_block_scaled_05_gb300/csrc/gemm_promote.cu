@@ -409,7 +409,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
-    kern<<<grid, C::THREADS, SMEM_BYTES, st>>>(*a.tm_a, *a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
+    kern<<<grid, C::THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
                                                a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
     return cudaGetLastError();
 }

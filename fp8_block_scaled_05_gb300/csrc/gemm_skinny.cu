@@ -370,7 +370,7 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t st) {
     }
     dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits, (unsigned)((a.M + NT - 1) / NT));
     k_gemm_skinny<NT><<<grid, C::THREADS, smem_bytes<NT>(), st>>>(
-        *a.tm_b, *a.tm_a, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
+        a.tm_b, a.tm_a, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
         a.splits, static_cast<uint8_t*>(a.workspace), a.status);
     return cudaGetLastError();
 }

@@ -30,8 +30,9 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int
 
 // ------------------------------------------------------------- GEMMs
 struct GemmArgs {
-    const CUtensorMap* tm_a;        // qa [rows, K] uint8, box {128, 128}, 128B swizzle
-    const CUtensorMap* tm_b;        // qb [rows, K] uint8, box {128, BN}, 128B swizzle
+    CUtensorMap tm_a;               // qa [rows, K] uint8, box {128, 128}, 128B swizzle
+    CUtensorMap tm_b;               // qb [rows, K] uint8, box {128, BN}, 128B swizzle
+    CUtensorMap tm_c;               // MX path: c [rows, N] bf16, box {32, 32}, 64B swizzle
     const float* sa;
     int64_t ldsa;
     const float* sb;
@@ -55,7 +56,7 @@ cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st);
 
 // Dense / grouped kernel for power-of-two scales: the tensor core applies the
 // scales as UE8M0 block scale factors (tcgen05.mma kind::mxf8f6f4); output
-// tile 128 x 256, a.tm_b with box {128, 256}.  Every scale must be a power of
+// tile 128 x 256, a.tm_b with box {128, 256}, a.tm_c as noted above.  Every scale must be a power of
 // two in [2^-127, 2^127]; others are reported in the status word.
 cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st);
 

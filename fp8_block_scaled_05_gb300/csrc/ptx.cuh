@@ -81,6 +81,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// Release store / acquire load of a shared-memory word (CTA scope): a flag
+// one thread publishes after its own waits, for another thread to poll.
+__device__ __forceinline__ void st_release_shared(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Waits until the shared word *p (advanced with st_release_shared) reaches at
+// least `target`; gives up after `limit_ns` nanoseconds and returns false.
+__device__ __forceinline__ bool wait_counter(const uint32_t *p, uint32_t target, uint64_t limit_ns) {
+#pragma unroll 1
+    for (int i = 0; i < 1024; ++i)
+        if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 1024; ++i)
+            if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // 4-byte asynchronous global -> shared copy; with valid == false nothing is
 // read and the destination is zero-filled.
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, bool valid) {
@@ -131,6 +158,31 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// 2-D tiled store shared -> global (bulk-group completion).  Rows and
+// columns outside the tensor are not written; c0 must be >= 0 and a multiple
+// of 16 bytes' worth of elements.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until this thread's bulk groups, all but the newest N, have finished
+// reading their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until this thread's bulk groups, all but the newest N, are complete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
