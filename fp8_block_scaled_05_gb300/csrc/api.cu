@@ -302,11 +302,9 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
-    if (mx) {
-        if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
-                                      CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
-            return e;
-    }
+    if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+        return e;
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
@@ -347,11 +345,9 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.splits = 1;
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M_total, N, K, G);
-    if (mx) {
-        if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M_total, ldc * 2, 32, 32,
-                                      CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
-            return e;
-    }
+    if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M_total, ldc * 2, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+        return e;
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M_total, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;

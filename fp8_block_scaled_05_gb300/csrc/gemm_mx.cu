@@ -17,16 +17,20 @@
 // Design (one CTA per SM, persistent over 128 x 256 output tiles, 16 warps):
 //   warp 0      TMA producer: qa tile 128x128 and qb tile 256x128 per K-block
 //               into a 4-stage, 192 KB shared-memory ring (128-byte swizzle).
-//   warp 1      MMA issuer (one thread) and TMEM owner: four tcgen05.mma
-//               (M=128, N=256, K=32) per K-block into the accumulator, TMEM
-//               columns [0, 256).
-//   warp 2      gatekeeper (one thread): does every barrier wait the MMAs
-//               depend on (operands landed, scale factors written, the
-//               accumulator drained) and publishes the count of K-blocks
-//               ready in a shared word.  The issuer only polls that word: a
-//               barrier test costs ~200 cycles, and one thread that both
-//               waited and issued left the tensor core idle for about 40% of
-//               each K-block's 512 cycles.
+//   warp 1      MMA issuer and TMEM owner: four tcgen05.mma (M=128, N=256,
+//               K=32) per K-block into the accumulator, TMEM columns [0, 256),
+//               issued by lane 0.
+//   warp 2      gatekeeper: does every barrier wait the MMAs depend on
+//               (accumulator drained, scale factors written, operands landed)
+//               and then meets the issuer warp at a named barrier, once per
+//               K-block.  A wait with acquire semantics (an mbarrier test, an
+//               acquire load) in a thread that has MMAs in flight stalls it
+//               until they complete, ~600 cycles past the 512 a K-block takes;
+//               a named barrier does not, and it orders memory between the
+//               two warps.  The named barrier has no time limit, so the
+//               gatekeeper never leaves its loop early: after a wait runs out it
+//               sets an abort flag and keeps meeting the issuer, which then
+//               issues nothing.
 //   warps 4..7  scale-factor writers, one per TMEM lane quarter: for each
 //               group of four K-blocks they convert the scales to UE8M0
 //               bytes (byte j = K-block 4g + j, selected per instruction by
@@ -47,8 +51,11 @@
 //               whole kernel by a quarter.  A grouped tile that ends inside an
 //               expert stores its rows one by one instead, up to the expert's
 //               last row (a TMA store would clip only at M).
-// Every wait is bounded; a wait that runs out records a timeout in the status
-// word and the kernel unwinds (waiting, bounded, for its own copies and MMAs).
+// The scale-factor writers and the epilogue sleep in their waits (they are off
+// the critical path, and spinning warps slowed the MMA feed by ~5%); the
+// producer and the gatekeeper spin.  Every wait is bounded; a wait that runs
+// out records a timeout in the status word and the kernel unwinds (waiting,
+// bounded, for its own copies and MMAs).
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -71,7 +78,8 @@ constexpr int KB_PER_SF = 4;                     // K-blocks per scale-factor gr
 constexpr int SF_SLOTS = 4;                      // scale-factor groups in flight
 constexpr uint32_t SF_COL0 = 256;                // first TMEM column of the scale-factor ring
 constexpr uint32_t SF_SLOT_COLS = 16;            // A: columns +0..+3, B: columns +8..+15
-constexpr int GATE_WARP = 2;
+constexpr int ISSUE_WARP = 1, GATE_WARP = 2;
+constexpr uint32_t kIssueBar = 1;                // named barrier: gatekeeper + issuer warps
 constexpr int SF_WARP0 = 4;
 constexpr int EPI_WARP0 = 8, EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 512
@@ -93,12 +101,12 @@ struct __align__(16) Ctrl {
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t n_tiles;
-    uint32_t ready;      // K-blocks (counted over this CTA's tiles) cleared for issue
-    uint32_t pad_;
+    volatile int32_t abort_issue;   // set by the gatekeeper after a wait ran out
+    int32_t pad_;
 };
 
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)RING_BYTES + (size_t)EPI_WARPS * EPI_BUF_BYTES +
-                               sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+                               sizeof(Ctrl) + (size_t)(MAX_GROUPS + 1) * sizeof(int32_t);
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record(int* status, int code) {
@@ -134,8 +142,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
     Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)EPI_WARPS * EPI_BUF_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
-    int32_t* glo = cum + (MAX_GROUPS + 1);
-    int32_t* ghi = glo + (MAX_GROUPS + 1);
 
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK;
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(&ctl->tfull, 1);
         mbar_init(&ctl->tempty, EPI_WARPS);
         mbar_init(&ctl->mma_done, 1);
-        ctl->ready = 0;
+        ctl->abort_issue = 0;
         mbar_init_fence();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (warp == 3) {
         if (GROUPED) {
-            const int total = build_group_table<BM>(offsets, G, M, NT, cum, glo, ghi);
+            const int total = build_group_table<BM>(offsets, G, M, NT, cum);
             if (lane == 0) ctl->n_tiles = total;
         } else if (lane == 0) {
             ctl->n_tiles = ((M + BM - 1) / BM) * NT;
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
@@ -208,47 +214,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else if (warp == GATE_WARP) {
         // ------------------------------------------------ gatekeeper
-        if (lane == 0) {
-            uint32_t it = 0, gi = 0, tt = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tt) {
-                // The accumulator is free once the epilogue has copied the
-                // previous tile out of it.
-                if (!mbar_wait(&ctl->tempty, (tt & 1) ^ 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t byte = (uint32_t)kb % KB_PER_SF;
-                    if (byte == 0 && !mbar_wait(&ctl->sfull[gi % SF_SLOTS], (gi / SF_SLOTS) & 1, kWaitLimitNs)) {
-                        ok = false;
-                        break;
+        uint32_t it = 0, gi = 0, tt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tt) {
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+                if (lane == 0 && ok) {
+                    ok = (kb > 0 || mbar_wait(&ctl->tempty, (tt & 1) ^ 1, kWaitLimitNs)) &&
+                         (byte > 0 || mbar_wait(&ctl->sfull[gi % SF_SLOTS], (gi / SF_SLOTS) & 1, kWaitLimitNs)) &&
+                         mbar_wait(&ctl->full[it % STAGES], (it / STAGES) & 1, kWaitLimitNs);
+                    if (!ok) {
+                        ctl->abort_issue = 1;
+                        record(status, kStatusTimeout);
                     }
-                    if (!mbar_wait(&ctl->full[it % STAGES], (it / STAGES) & 1, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    st_release_shared(&ctl->ready, it + 1);
-                    if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
                 }
+                named_bar_sync(kIssueBar, 64);   // K-block `it` may be issued
+                if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
             }
-            if (!ok) record(status, kStatusTimeout);
         }
-        __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == ISSUE_WARP) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, gi = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t byte = (uint32_t)kb % KB_PER_SF;
-                    const uint32_t slot = gi % SF_SLOTS;
-                    if (!wait_counter(&ctl->ready, it + 1, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
+        uint32_t it = 0, gi = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const uint32_t s = it % STAGES;
+                const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+                const uint32_t slot = gi % SF_SLOTS;
+                named_bar_sync(kIssueBar, 64);
+                if (lane == 0 && !ctl->abort_issue) {
                     tc_fence_after_sync();
                     const uint32_t sA = smem_u32(smem + (size_t)s * STAGE_BYTES);
                     const uint64_t adesc = sdesc_kmajor_sw128(sA);
@@ -260,15 +253,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         umma_mxf8f6f4(tmem_base, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc, sfa,
                                       sfa + 8, (kb > 0 || k > 0) ? 1u : 0u);
                     umma_commit(&ctl->empty[s]);
-                    if (byte == KB_PER_SF - 1 || kb == KB - 1) {
-                        umma_commit(&ctl->sempty[slot]);
-                        ++gi;
-                    }
+                    if (byte == KB_PER_SF - 1 || kb == KB - 1) umma_commit(&ctl->sempty[slot]);
+                    if (kb == KB - 1) umma_commit(&ctl->tfull);
                 }
-                if (!ok) break;
-                umma_commit(&ctl->tfull);
+                __syncwarp();
+                if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
             }
-            if (!ok) record(status, kStatusTimeout);
+        }
+        if (lane == 0) {
             // All MMAs this thread issued are complete before TMEM is released.
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, kWaitLimitNs);
@@ -281,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t gi = 0;
         bool ok = true, bad = false;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
             const int m = tl.m0 + q * 32 + lane;
             const bool vrow = m < tl.row_end;
             const int nb0 = tl.n0 / 128;
@@ -304,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     wb1 |= ue8m0(fb1[j], bad) << (8 * j);
                 }
                 const uint32_t slot = gi % SF_SLOTS;
-                bool got = mbar_wait(&ctl->sempty[slot], ((gi / SF_SLOTS) & 1) ^ 1, kWaitLimitNs);
+                bool got = mbar_wait_sleep(&ctl->sempty[slot], ((gi / SF_SLOTS) & 1) ^ 1, kWaitLimitNs);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) {
                     ok = false;
@@ -327,20 +319,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int h = (warp - EPI_WARP0) >> 2;   // column half of the tile
+        const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
         uint32_t tt = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tt) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
             const int m = tl.m0 + q * 32 + lane;
             const int col0 = tl.n0 + h * 128;
-            bool got = mbar_wait(&ctl->tfull, tt & 1, kWaitLimitNs);
+            bool got = mbar_wait_sleep(&ctl->tfull, tt & 1, kWaitLimitNs);
             got = __all_sync(0xFFFFFFFFu, got);
             if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+            const uint32_t taddr = tacc;
             // Three round trips (64, 32 and 32 columns), packed to bf16 pairs as
             // they arrive so that at most 64 raw values are live; TMEM goes back
             // before any store.

@@ -54,7 +54,7 @@ constexpr int EPI_WARP0 = 4;                 // first promotion warp
 constexpr int SCALE_WARP = 2;
 constexpr int MAX_GROUPS = 1024;
 constexpr int SRING = 8;                     // scale ring slots
-constexpr int RING_BYTES = 192 * 1024;       // operand ring
+constexpr int EPI_BUF_BYTES = 32 * 64;       // one 32 x 32 bf16 output block per promotion warp
 
 template <int BN_>
 struct Cfg {
@@ -62,7 +62,8 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;   // 4 (BN 256) or 6 (BN 128)
+    static constexpr int STAGES = 4;                          // 192 KB (BN 256) or 128 KB (BN 128)
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int NBUF = 512 / BN;                     // TMEM accumulator buffers
     static constexpr int EPI_WARPS = BN == 128 ? 16 : 8;
     static constexpr int SLICES = EPI_WARPS / 4;              // column slices per TMEM lane quarter
@@ -101,8 +102,12 @@ struct __align__(16) Ctrl {
     ScaleSlot ring[SRING];
 };
 
-constexpr size_t SMEM_BYTES =
-    1024 /*align slack*/ + (size_t)RING_BYTES + sizeof(Ctrl) + (size_t)3 * (MAX_GROUPS + 1) * sizeof(int32_t);
+template <int BN>
+constexpr size_t smem_bytes() {
+    return 1024 /*align slack*/ + (size_t)Cfg<BN>::RING_BYTES + (size_t)Cfg<BN>::EPI_WARPS * EPI_BUF_BYTES +
+           sizeof(Ctrl) + (size_t)(MAX_GROUPS + 1) * sizeof(int32_t);
+}
+static_assert(smem_bytes<256>() <= 232448 && smem_bytes<128>() <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record_timeout(int* status) {
     if (status) atomicCAS(status, 0, kStatusTimeout);
@@ -116,16 +121,16 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[
 template <int BN, bool GROUPED>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_c,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (size_t)RING_BYTES);
+    uint8_t* epi_buf = smem + (size_t)C::RING_BYTES;   // 1024-byte aligned
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)C::EPI_WARPS * EPI_BUF_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
-    int32_t* glo = cum + (MAX_GROUPS + 1);
-    int32_t* ghi = glo + (MAX_GROUPS + 1);
 
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK;
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         mbar_init_fence();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_c);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, 512);
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     }
     if (warp == 3) {
         if (GROUPED) {
-            const int total = build_group_table<BM>(offsets, G, M, NT, cum, glo, ghi);
+            const int total = build_group_table<BM>(offsets, G, M, NT, cum);
             if (lane == 0) ctl->n_tiles = total;
         } else if (lane == 0) {
             ctl->n_tiles = ((M + BM - 1) / BM) * NT;
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         uint32_t sit = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
             const int nb0 = tl.n0 / 128;
             for (int kb = 0; kb < KB; ++kb, ++sit) {
                 const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         bool ok = true;
         bool ready = false;   // tfull of K-block kbg already seen complete (early probe)
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, glo, ghi, G);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
             const int m = tl.m0 + row_in_tile;
             const int col0 = tl.n0 + sl * C::EPI_COLS;
             const bool vrow = m < tl.row_end;
@@ -355,7 +361,38 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 }
             }
             if (!ok) break;
-            if (vrow && vcol) {
+            if (!vcol) continue;
+            const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
+            if (!GROUPED || rows_here == 32) {
+                // 32 x 32 blocks through this warp's 2 KB buffer and TMA stores:
+                // row `lane`, 16-byte piece k at lane*64 + ((k ^ ((lane >> 1) & 3))
+                // << 4), the 64-byte swizzle of the output tensor map.  (Stores
+                // straight from registers put one 16-byte piece of 32 rows in each
+                // instruction and held these warps for thousands of cycles.)
+                uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
+#pragma unroll
+                for (int cc = 0; cc < C::CHUNKS; ++cc) {
+                    if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t p[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = 8 * k + 2 * e;
+                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[e]) : "f"(acc[cc][col + 1]), "f"(acc[cc][col]));
+                        }
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, tl.m0 + q * 32);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (vrow) {
                 uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
 #pragma unroll
                 for (int j = 0; j < C::EPI_COLS / 8; ++j) {
@@ -372,6 +409,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait_group<0>();   // stores complete before the CTA exits
         if (!ok) {
             if (lane == 0) {
                 record_timeout(status);
@@ -402,14 +440,14 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         // The setmaxnreg split is only safe if the CTA really starts with
         // LAUNCH_REGS registers per thread; refuse to launch otherwise.
         if (C::SPLIT_REGS && fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<BN>());
         if (e != cudaSuccess) return e;
         attr_done_mask |= 1 << (dev & 31);
     }
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
-    kern<<<grid, C::THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
+    kern<<<grid, C::THREADS, smem_bytes<BN>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
                                                a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
     return cudaGetLastError();
 }

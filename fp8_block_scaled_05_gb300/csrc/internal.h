@@ -32,7 +32,7 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int
 struct GemmArgs {
     CUtensorMap tm_a;               // qa [rows, K] uint8, box {128, 128}, 128B swizzle
     CUtensorMap tm_b;               // qb [rows, K] uint8, box {128, BN}, 128B swizzle
-    CUtensorMap tm_c;               // MX path: c [rows, N] bf16, box {32, 32}, 64B swizzle
+    CUtensorMap tm_c;               // promote / MX: c [rows, N] bf16, box {32, 32}, 64B swizzle
     const float* sa;
     int64_t ldsa;
     const float* sb;

@@ -81,6 +81,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// Waits until the phase with the given parity has completed, sleeping in
+// mbarrier.try_wait (the thread is suspended until the phase completes or
+// the hint runs out) instead of spinning.  For waits off the critical path:
+// spinning warps take issue slots and shared-memory bandwidth from the warps
+// that feed the tensor core, but a suspended thread wakes a few hundred
+// cycles after the phase completes.  Gives up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Release store / acquire load of a shared-memory word (CTA scope): a flag
 // one thread publishes after its own waits, for another thread to poll.
 __device__ __forceinline__ void st_release_shared(uint32_t *p, uint32_t v) {

@@ -9,13 +9,21 @@ struct Tile {
     int32_t m0, row_end, brow, n0, g;
 };
 
+// Rows [lo, hi) of expert g: the offsets clamped to [0, M], each range
+// starting where the previous one ends or later.
+__device__ __forceinline__ void group_rows(const int32_t* __restrict__ offsets, int g, int M, int& lo, int& hi) {
+    lo = min(max(offsets[g], 0), M);
+    hi = min(max(offsets[g + 1], lo), M);
+}
+
 // Tile t -> coordinates.  Dense: m-tiles vary fastest so that CTAs running at
 // the same time share the weight tile.  Grouped: tiles of expert g follow
 // those of expert g-1; inside an expert, m-tiles vary fastest.  cum[g] is the
-// number of tiles of experts before g; [glo[g], ghi[g]) are g's rows.
+// number of tiles of experts before g (shared memory, from
+// build_group_table).
 template <int BM, int BN, bool GROUPED>
-__device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* cum, const int32_t* glo,
-                                            const int32_t* ghi, int G) {
+__device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* cum,
+                                            const int32_t* __restrict__ offsets, int G) {
     Tile r;
     if (!GROUPED) {
         const int MT = (M + BM - 1) / BM;
@@ -32,11 +40,13 @@ __device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* 
             if (cum[mid] <= t) lo = mid; else hi = mid;
         }
         const int g = lo;
+        int rlo, rhi;
+        group_rows(offsets, g, M, rlo, rhi);
         const int local = t - cum[g];
-        const int MTg = (ghi[g] - glo[g] + BM - 1) / BM;
+        const int MTg = (rhi - rlo + BM - 1) / BM;
         const int mt = local % MTg, nt = local / MTg;
-        r.m0 = glo[g] + mt * BM;
-        r.row_end = ghi[g];
+        r.m0 = rlo + mt * BM;
+        r.row_end = rhi;
         r.brow = g * N + nt * BN;
         r.n0 = nt * BN;
         r.g = g;
@@ -44,12 +54,12 @@ __device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* 
     return r;
 }
 
-// Executed by one whole warp: per-expert row ranges (offsets clamped to
-// [0, M], each range starting where the previous ends or later) and the
-// running tile count; returns the total number of tiles on every lane.
+// Executed by one whole warp: the running tile count cum[0..G] of the
+// experts (NT output-column tiles per row tile); returns the total number of
+// tiles on every lane.
 template <int BM>
 __device__ __forceinline__ int build_group_table(const int32_t* __restrict__ offsets, int G, int M, int NT,
-                                                 int32_t* cum, int32_t* glo, int32_t* ghi) {
+                                                 int32_t* cum) {
     const int lane = threadIdx.x & 31;
     int carry = 0;
     if (lane == 0) cum[0] = 0;
@@ -57,11 +67,9 @@ __device__ __forceinline__ int build_group_table(const int32_t* __restrict__ off
         const int g = g0 + lane;
         int tiles = 0;
         if (g < G) {
-            const int lo = min(max(offsets[g], 0), M);
-            const int hi = min(max(offsets[g + 1], lo), M);
+            int lo, hi;
+            group_rows(offsets, g, M, lo, hi);
             tiles = ((hi - lo + BM - 1) / BM) * NT;
-            glo[g] = lo;
-            ghi[g] = hi;
         }
         int incl = tiles;
 #pragma unroll
