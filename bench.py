@@ -53,6 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-pow2", action="store_true", help="skip the power-of-two scale-mode measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -277,19 +278,37 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     launches_per_step = 3 * len(layers)
 
-    def step(events=None):
+    def step(events=None, pow2=False):
+        mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+        flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
         for i, L in enumerate(layers):
             if events is not None:
                 events[3 * i].record(stream)
-            ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
+            ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], mode, stream)
             if events is not None:
                 events[3 * i + 1].record(stream)
-            ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
+            ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream)
             if events is not None:
                 events[3 * i + 2].record(stream)
-            ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, None, stream)
+            ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, None, stream)
         if events is not None:
             events[3 * len(layers)].record(stream)
+
+    def timed(pow2, steps):
+        """Runs `steps` flushed steps; returns (per-step ms, per-kernel mean ms)."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * len(layers) + 1)] for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for k in range(steps):
+                flush.zero_()
+                step(evs[k], pow2)
+        torch.cuda.synchronize(dev)
+        step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps)]
+        kern = {}
+        for i, L in enumerate(layers):
+            for j, kname in enumerate(("quant_act", "quant_weight", "gemm")):
+                ms = [evs[k][3 * i + j].elapsed_time(evs[k][3 * i + j + 1]) for k in range(steps)]
+                kern[f"{L['name']}.{kname}"] = sum(ms) / len(ms)
+        return step_ms, kern
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -300,27 +319,14 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise SystemExit(f"device status after warm-up: {ops.status_string(st)}")
 
-    nev = 3 * len(layers) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
-    with torch.cuda.stream(stream):
-        for k in range(args.steps):
-            flush.zero_()
-            step(evs[k])
-    torch.cuda.synchronize(dev)
+    step_ms, kern = timed(False, args.steps)
     clk = clocks.stop()
     barrier(world)
-
-    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
-    kern = {}
-    for i, L in enumerate(layers):
-        for j, kname in enumerate(("quant_act", "quant_weight", "gemm")):
-            ms = [evs[k][3 * i + j].elapsed_time(evs[k][3 * i + j + 1]) for k in range(args.steps)]
-            kern[f"{L['name']}.{kname}"] = sum(ms) / len(ms)
     total_ms = reduce_max(sum(step_ms), world, dev)
     value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
 
@@ -382,6 +388,29 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": e2e_ms / e2e_steps}
 
+    # ---------------- the optional power-of-two scale mode on the same workload:
+    # quantisers in pow2 mode, GEMM with the pow2 promise (the MX kernel).  A
+    # separate timed region, reported beside the headline.
+    pow2 = None
+    if not args.no_pow2:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.zero_()
+                step(None, True)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        p_ms, p_kern = timed(True, args.steps)
+        barrier(world)
+        p_total = reduce_max(sum(p_ms), world, dev)
+        p_gemm_ms = sum(p_kern[f"{L['name']}.gemm"] for L in layers)
+        plan = ops.fp8_gemm_plan(layers[0]["M"], layers[0]["N"], layers[0]["K"], ops.FP8_GEMM_SCALES_POW2)[0]
+        pow2 = {"scale": "pow2 (2^ceil(log2(amax/448)))", "gemm_path": {v: k for k, v in ops.PATHS.items()}[plan],
+                "value": flops_step * args.steps * world / (p_total / 1e3) / 1e12, "unit": UNIT,
+                "ms_per_step": p_total / args.steps,
+                "gemm_only_tflops": flops_step / (p_gemm_ms / 1e3) / 1e12,
+                "gemm_frac_fp8": flops_step / (p_gemm_ms / 1e3) / 1e12 / fp8_peak,
+                "kernels_ms": p_kern, "gpu_launches": launches_per_step * args.steps}
+
     st = ops.fp8_last_device_status(stream)
     if st != 0:
         raise SystemExit(f"device status after the timed region: {ops.status_string(st)}")
@@ -411,6 +440,7 @@ def run_ours(args, world, rank, local):
             "kernels": kernels_out,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "pow2": pow2,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
