@@ -114,8 +114,7 @@ __device__ __forceinline__ void record_timeout(int* status) {
 }
 
 __device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[32], float sc) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v[j]), sc, acc[j]);
+    fma32_packed(acc, v, sc);
 }
 
 template <int BN, bool GROUPED>

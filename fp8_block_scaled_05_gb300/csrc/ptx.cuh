@@ -369,6 +369,22 @@ __device__ __forceinline__ void tmem_ld_wait_after(float (&a)[32]) {
                  : "memory");
 }
 
+// acc[j] = fma(v[j], sc, acc[j]) for 32 fp32 values, as 16 packed
+// fma.rn.f32x2 (each lane an IEEE fma.rn.f32, so the result is bit-identical
+// to fmaf): half the issue slots of 32 scalar FMAs.
+__device__ __forceinline__ void fma32_packed(float (&acc)[32], const uint32_t (&v)[32], float sc) {
+    uint64_t s;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s) : "f"(sc));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint64_t a, x;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc[2 * j]), "f"(acc[2 * j + 1]));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(v[2 * j]), "r"(v[2 * j + 1]));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(s));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * j]), "=f"(acc[2 * j + 1]) : "l"(a));
+    }
+}
+
 // Per-warpgroup register reallocation (all four warps of the warpgroup
 // execute it).  The sum over warpgroups must stay within the registers the
 // CTA was launched with.
