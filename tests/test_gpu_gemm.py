@@ -181,9 +181,28 @@ def test_llama_full_size_sampled_rows(ops, layer, pow2):
     assert_gemm_close(bf16_to_np(y[rows]), ref, f"llama {layer}")
 
 
+@pytest.mark.parametrize("layer", ["gate_up", "down", "o_proj"])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_qwen_prefill_full_size_sampled_rows(ops, layer, pow2):
+    """Qwen3-8B-shaped prefill (M 16384, Student-t nu = 4 activations), both
+    scale modes: fp32 scales take the promote kernel, power-of-two scales the
+    MX kernel.  Whole path on the GPU, checked on sampled output rows."""
+    case = I.qwen_prefill_layers(layers=[layer])[0]
+    y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda(), pow2=pow2)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    M = case.a.shape[0]
+    rows = np.unique(np.concatenate([np.random.Generator(np.random.PCG64(11)).choice(M, 24, replace=False),
+                                     [0, 127, 128, M - 1]]))
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
+    assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
+    ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
+    assert_gemm_close(bf16_to_np(y[rows]), ref, f"qwen prefill {layer} pow2={pow2}")
+
+
+@pytest.mark.parametrize("K,N", [(14336, 4096), (4096, 6144)])
 @pytest.mark.parametrize("M", [1, 8, 64, 256])
-def test_decode_full_size(ops, M):
-    K, N = 14336, 4096
+def test_decode_full_size(ops, M, K, N):
     case = I.decode_case(M, K, N)
     y, (qa, sa), (qw, sw) = ops.linear(case.a.cuda(), case.w.cuda())
     torch.cuda.synchronize()
@@ -258,3 +277,34 @@ def test_grouped_moe_full_size_sampled_rows(ops, pow2):
     qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
     ref = np.stack([O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], qw_n[g], sw_n[g])[0] for i, g in enumerate(grp)])
     assert_gemm_close(bf16_to_np(c[rows]), ref, "moe gate_up")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_grouped_moe_down_full_size_sampled_rows(ops, pow2):
+    """Qwen3-30B-A3B-shaped expert down projection (K 768: six K-blocks, so the
+    MX kernel's last scale-factor group is partial; N 2048), Zipf routing."""
+    m = I.moe_case(with_weights=False)
+    G, N, K = 128, 2048, 768
+    w = I.normal_bf16(I.stream(0, 83), (G, N, K), std=0.02)
+    x = m.a_down.cuda()
+    qa, sa = ops.quant_act(x, pow2)
+    qw = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    wd = w.cuda()
+    mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+    for g in range(G):
+        ops.fp8_quant_weight_128x128(wd[g], qw[g], sw[g], mode)
+    offs = torch.from_numpy(m.offsets).cuda()
+    c = ops.grouped_gemm(qa, sa, offs, qw, sw, pow2)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    rng = np.random.Generator(np.random.PCG64(19))
+    rows = np.sort(rng.choice(x.shape[0], 32, replace=False))
+    rows = np.unique(np.concatenate([rows, m.offsets[1:6] - 1, m.offsets[:5]]))
+    rows = rows[rows < x.shape[0]]
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_down[rows]), pow2)
+    assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
+    grp = np.searchsorted(m.offsets, rows, side="right") - 1
+    qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
+    ref = np.stack([O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], qw_n[g], sw_n[g])[0] for i, g in enumerate(grp)])
+    assert_gemm_close(bf16_to_np(c[rows]), ref, "moe down")
