@@ -362,31 +362,62 @@ def run_ours(args, world, rank, local):
         h2d = sum(a.numel() * 2 + w.numel() * 2 for a, w, _ in host)
         d2h = sum(c.numel() * 2 for _, _, c in host)
         e2e_steps = max(3, args.steps // 4)
+        # Three streams: host->device copies, the library's kernels, and
+        # device->host copies, ordered per layer by events, so that one
+        # layer's transfers overlap another layer's kernels.  Every step still
+        # copies its inputs in from pinned host memory and its results out.
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        nl = len(layers)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        prev_done = [None] * nl     # kernels of layer i (previous step) finished reading a_i, w_i
+        prev_out = [None] * nl      # previous step's result of layer i copied out
 
         def e2e_step():
-            for L, (ah, wh, ch) in zip(layers, host):
-                L["a"].copy_(ah, non_blocking=True)
-                L["w"].copy_(wh, non_blocking=True)
+            for i, (L, (ah, wh, ch)) in enumerate(zip(layers, host)):
+                if prev_done[i] is not None:
+                    s_in.wait_event(prev_done[i])
+                with torch.cuda.stream(s_in):
+                    L["a"].copy_(ah, non_blocking=True)
+                    L["w"].copy_(wh, non_blocking=True)
+                    e_in = ev()
+                    e_in.record(s_in)
+                stream.wait_event(e_in)
+                if prev_out[i] is not None:
+                    stream.wait_event(prev_out[i])
                 ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
                 ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
                 ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, None, stream)
-                ch.copy_(L["c"], non_blocking=True)
+                e_k = ev()
+                e_k.record(stream)
+                prev_done[i] = e_k
+                s_out.wait_event(e_k)
+                with torch.cuda.stream(s_out):
+                    ch.copy_(L["c"], non_blocking=True)
+                    e_o = ev()
+                    e_o.record(s_out)
+                prev_out[i] = e_o
 
-        with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        stream.wait_event(e0)
+        s_out.wait_event(e0)
+        for _ in range(e2e_steps):
             e2e_step()
-            torch.cuda.synchronize(dev)
-            barrier(world)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(e2e_steps):
-                e2e_step()
-            e1.record(stream)
+        stream.wait_event(prev_out[-1])
+        for e in prev_out:
+            stream.wait_event(e)
+        e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
         e2e = {"value": flops_step * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "ms_per_step": e2e_ms / e2e_steps}
+               "ms_per_step": e2e_ms / e2e_steps,
+               "pipelining": "host->device copies, kernels and device->host copies on three streams, "
+                             "ordered per layer by events"}
 
     # ---------------- the optional power-of-two scale mode on the same workload:
     # quantisers in pow2 mode, GEMM with the pow2 promise (the MX kernel).  A
