@@ -272,7 +272,8 @@ def run_ours(args, world, rank, local):
                  sa=torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev),
                  qw=torch.empty((N, K), dtype=torch.uint8, device=dev),
                  sw=torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
-                 c=torch.empty((M, N), dtype=torch.bfloat16, device=dev))
+                 c=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                 ws=ops.workspace_for(M, N, K, 1, dev))
         layers.append(L)
     flops_step = sum(2.0 * L["M"] * L["N"] * L["K"] for L in layers)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -290,7 +291,7 @@ def run_ours(args, world, rank, local):
             ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream)
             if events is not None:
                 events[3 * i + 2].record(stream)
-            ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, None, stream)
+            ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, L["ws"], stream)
         if events is not None:
             events[3 * len(layers)].record(stream)
 
@@ -386,7 +387,7 @@ def run_ours(args, world, rank, local):
                     stream.wait_event(prev_out[i])
                 ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
                 ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
-                ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, None, stream)
+                ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, L["ws"], stream)
                 e_k = ev()
                 e_k.record(stream)
                 prev_done[i] = e_k

@@ -253,8 +253,11 @@ size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t G) {
     if (G != 1 || M <= 0 || N <= 0 || K <= 0) return 0;
     int32_t sp = 1;
     const uint32_t path = fp8_gemm_plan(M, N, K, FP8_GEMM_PATH_AUTO, &sp);
-    if (path != FP8_GEMM_PATH_SKINNY) return 0;
-    return skinny_workspace_bytes(M, N, K, sp);
+    if (path == FP8_GEMM_PATH_SKINNY) return skinny_workspace_bytes(M, N, K, sp);
+    int sms = 152;
+    DeviceInfo* d;
+    if (current_device(&d) == FP8_OK) sms = d->sm_count;
+    return promote_workspace_bytes(M, N, K, sms);
 }
 
 fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa, const uint8_t* qb,
@@ -302,6 +305,11 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
+    if (!mx && workspace && aligned16(workspace)) {
+        // optional: lets the promote kernel split its last wave of tiles
+        a.workspace = workspace;
+        a.ws_bytes = ws_bytes;
+    }
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
         return e;

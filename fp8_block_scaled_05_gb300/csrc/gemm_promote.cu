@@ -117,13 +117,53 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[
     fma32_packed(acc, v, sc);
 }
 
+// Tail split: the last, partial wave of output tiles (dense only) is split
+// along K so that it fills the GPU.  Tiles [0, n_full) are computed whole;
+// each tile n_full + i is computed as `parts` items over K-block ranges
+// [p KB / parts, (p + 1) KB / parts), whose fp32 results meet in `part`
+// ([tile][part][column][row]) and are added in part order by the warp that
+// completes the tile slice's ticket.  parts <= 1: no split.
+struct SplitTail {
+    int n_full;
+    int parts;
+    float* part;
+    int* ticket;      // one per (split tile, promotion warp); zero between calls
+};
+
+struct Item {
+    int tile, kb0, kb1, part, parts;
+};
+
+__host__ __device__ __forceinline__ int work_items(int n_tiles, const SplitTail& sp) {
+    return sp.parts > 1 ? sp.n_full + (n_tiles - sp.n_full) * sp.parts : n_tiles;
+}
+
+__device__ __forceinline__ Item decode_item(int t, const SplitTail& sp, int KB) {
+    Item w;
+    if (sp.parts <= 1 || t < sp.n_full) {
+        w.tile = t;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.part = 0;
+        w.parts = 1;
+    } else {
+        const int j = t - sp.n_full;
+        w.tile = sp.n_full + j / sp.parts;
+        w.part = j % sp.parts;
+        w.parts = sp.parts;
+        w.kb0 = w.part * KB / sp.parts;
+        w.kb1 = (w.part + 1) * KB / sp.parts;
+    }
+    return w;
+}
+
 template <int BN, bool GROUPED>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
-                   const int32_t* __restrict__ offsets, int G, int* status) {
+                   const int32_t* __restrict__ offsets, int G, int* status, SplitTail split) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,6 +214,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const int n_tiles = ctl->n_tiles;
+    const int n_items = work_items(n_tiles, split);
     volatile int32_t* abort_flag = &ctl->abort_flag;
 
     if constexpr (C::SPLIT_REGS) {
@@ -184,9 +225,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+                const Item w = decode_item(t, split, KB);
+                const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
                         ok = false;
@@ -214,8 +256,9 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             const uint32_t me = warp == 1 ? 0u : 1u;   // takes K-blocks it with it % 2 == me
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+                const Item w = decode_item(t, split, KB);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     if ((it & 1) != me) continue;
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
                     const uint32_t b = it % C::NBUF, tph = (it / C::NBUF) & 1;
@@ -257,10 +300,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         // ------------------------------------------------ scale producer
         uint32_t sit = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item w = decode_item(t, split, KB);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
             const int nb0 = tl.n0 / 128;
-            for (int kb = 0; kb < KB; ++kb, ++sit) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++sit) {
                 const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
                 bool got = mbar_wait(&ctl->sempty[slot], ph ^ 1, kWaitLimitNs);
                 got = __all_sync(0xFFFFFFFFu, got);
@@ -301,8 +345,9 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         uint32_t kbg = 0;
         bool ok = true;
         bool ready = false;   // tfull of K-block kbg already seen complete (early probe)
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item w = decode_item(t, split, KB);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
             const int m = tl.m0 + row_in_tile;
             const int col0 = tl.n0 + sl * C::EPI_COLS;
             const bool vrow = m < tl.row_end;
@@ -312,7 +357,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             for (int cc = 0; cc < C::CHUNKS; ++cc)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[cc][j] = 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++kbg) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++kbg) {
                 const uint32_t slot = kbg % SRING, sph = (kbg / SRING) & 1;
                 const uint32_t b = kbg % C::NBUF, tph = (kbg / C::NBUF) & 1;
                 (void)sph;   // the issuer waited for the scale slot before this K-block's MMAs
@@ -361,6 +406,45 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             }
             if (!ok) break;
             if (!vcol) continue;
+            if (w.parts > 1) {
+                // A K-split tile of the last wave: publish this part of the
+                // warp's 32 x EPI_COLS block, and the warp that completes the
+                // block's ticket adds the parts in part order and stores it.
+                const int wslot = (w.tile - split.n_full) * C::EPI_WARPS + (warp - EPI_WARP0);
+                float* part0 = split.part + (size_t)(w.tile - split.n_full) * w.parts * (BM * BN) +
+                               (size_t)(sl * C::EPI_COLS) * BM + q * 32 + lane;   // [part][col][row]
+                float* dst = part0 + (size_t)w.part * (BM * BN);
+#pragma unroll
+                for (int cc = 0; cc < C::CHUNKS; ++cc)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) __stcg(dst + (cc * 32 + j) * BM, acc[cc][j]);
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&split.ticket[wslot], 1) == w.parts - 1;
+                if (!__shfl_sync(0xFFFFFFFFu, last, 0)) continue;
+                __threadfence();
+                if (lane == 0) split.ticket[wslot] = 0;   // ready for the next call
+                // every part, this warp's included, is read back and added in part
+                // order, one 32-column chunk at a time
+#pragma unroll
+                for (int cc = 0; cc < C::CHUNKS; ++cc) {
+                    float sum[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+#pragma unroll 1
+                    for (int pp = 0; pp < w.parts; ++pp) {
+                        const float* src = part0 + (size_t)pp * (BM * BN) + (size_t)(cc * 32) * BM;
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + j * BM);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sum[j] += v[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[cc][j] = sum[j];
+                }
+            }
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
                 // 32 x 32 blocks through this warp's 2 KB buffer and TMA stores:
@@ -446,12 +530,52 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
+    SplitTail split{0, 1, nullptr, nullptr};
+    if (!GROUPED) {
+        const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN);
+        if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
+            split.n_full = (int)tp.n_full;
+            split.parts = tp.parts;
+            split.ticket = static_cast<int*>(a.workspace);
+            split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
+        }
+    }
     kern<<<grid, C::THREADS, smem_bytes<BN>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
-                                               a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
+                                               a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split);
     return cudaGetLastError();
 }
 
 }  // namespace promote
+
+// Split of the last wave (dense): with `grid` = min(tiles, SMs) persistent
+// CTAs, the first (tiles / grid) * grid tiles fill whole waves; the L left
+// over are split along K into min(grid / L, KB / 8, 4) parts when that is at
+// least 2.
+TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn) {
+    TailPlan tp{0, 1, 0, 0};
+    if (M <= 0 || bn <= 0 || sm_count <= 0) return tp;
+    const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+    const int64_t grid = tiles < sm_count ? tiles : sm_count;
+    const int64_t full = (tiles / grid) * grid, left = tiles - full;
+    if (left == 0 || full == 0) return tp;
+    // At least 8 K-blocks per part and at most 4 parts: each extra part costs
+    // the warp that completes a tile another 16 KB read of fp32 partials, and
+    // 8 parts of 4 K-blocks measured slower than no split.
+    int64_t parts = grid / left;
+    if (parts > (K / 128) / 8) parts = (K / 128) / 8;
+    if (parts > 4) parts = 4;
+    if (parts < 2) return tp;
+    const int epi_warps = bn == 128 ? 16 : 8;
+    tp.n_full = full;
+    tp.parts = (int)parts;
+    tp.ticket_bytes = ((size_t)left * epi_warps * sizeof(int) + 255) & ~size_t(255);
+    tp.bytes = tp.ticket_bytes + (size_t)left * parts * 128 * bn * sizeof(float);
+    return tp;
+}
+
+size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
+    return tail_plan(M, N, K, sm_count, promote_tile_n(M, N, K, 1)).bytes;
+}
 
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;

@@ -145,11 +145,18 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  * c   device, bf16 [M, N], row pitch ldc (>= N, % 8 == 0)
  * M >= 0 (0 is a no-op), N, K > 0 and multiples of 128.  All pointers 16-byte aligned.
  * flags: FP8_GEMM_SCALES_POW2 | one FP8_GEMM_PATH_* value.
- * workspace: device scratch of at least fp8_gemm_workspace_size(M, N, K, 1) bytes
- *     (may be NULL when that size is 0).  Its first bytes hold split-K
- *     semaphores that must be zero before the first use; every completed
- *     call leaves them zero again (allocate it zero-filled once and reuse it).
- *     Calls that share a workspace must not run concurrently.
+ * workspace: device scratch of fp8_gemm_workspace_size(M, N, K, 1) bytes (may be
+ *     NULL when that size is 0).  Its first bytes hold split-K semaphores that
+ *     must be zero before the first use; every completed call leaves them zero
+ *     again (allocate it zero-filled once and reuse it).  Calls that share a
+ *     workspace must not run concurrently.
+ *     - Skinny path (M <= 256): required; smaller or NULL returns
+ *       FP8_ERR_WORKSPACE.
+ *     - Promote path: optional.  With it, when the output tiles do not fill
+ *       whole waves of the GPU's SMs, the tiles of the last wave are split
+ *       along K and their fp32 parts added in a fixed order; without it (or
+ *       if it is too small) every tile is computed whole.
+ *     - MX path: unused.
  */
 FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
                                 const uint8_t *qb, int64_t ldb, const float *sb,
