@@ -305,8 +305,8 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
     a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
-    if (!mx && workspace && aligned16(workspace)) {
-        // optional: lets the promote kernel split its last wave of tiles
+    if (workspace && aligned16(workspace)) {
+        // optional: lets the kernel split its last wave of tiles
         a.workspace = workspace;
         a.ws_bytes = ws_bytes;
     }

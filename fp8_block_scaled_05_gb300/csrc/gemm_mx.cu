@@ -136,7 +136,8 @@ template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_c, const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
-              int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status) {
+              int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status,
+              SplitTail split) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
@@ -183,15 +184,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const int n_tiles = ctl->n_tiles;
+    const int n_items = work_items(n_tiles, split);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+                const Item w = decode_item(t, split, KB);
+                const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
                         ok = false;
@@ -216,11 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ gatekeeper
         uint32_t it = 0, gi = 0, tt = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tt) {
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tt) {
+            const Item w = decode_item(t, split, KB);
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                const uint32_t byte = (uint32_t)(kb - w.kb0) % KB_PER_SF;
                 if (lane == 0 && ok) {
-                    ok = (kb > 0 || mbar_wait(&ctl->tempty, (tt & 1) ^ 1, kWaitLimitNs)) &&
+                    ok = (kb > w.kb0 || mbar_wait(&ctl->tempty, (tt & 1) ^ 1, kWaitLimitNs)) &&
                          (byte > 0 || mbar_wait(&ctl->sfull[gi % SF_SLOTS], (gi / SF_SLOTS) & 1, kWaitLimitNs)) &&
                          mbar_wait(&ctl->full[it % STAGES], (it / STAGES) & 1, kWaitLimitNs);
                     if (!ok) {
@@ -229,16 +233,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 named_bar_sync(kIssueBar, 64);   // K-block `it` may be issued
-                if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
+                if (byte == KB_PER_SF - 1 || kb == w.kb1 - 1) ++gi;
             }
         }
     } else if (warp == ISSUE_WARP) {
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, gi = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+            const Item w = decode_item(t, split, KB);
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
-                const uint32_t byte = (uint32_t)kb % KB_PER_SF;
+                const uint32_t byte = (uint32_t)(kb - w.kb0) % KB_PER_SF;
                 const uint32_t slot = gi % SF_SLOTS;
                 named_bar_sync(kIssueBar, 64);
                 if (lane == 0 && !ctl->abort_issue) {
@@ -251,13 +256,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
                         umma_mxf8f6f4(tmem_base, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc, sfa,
-                                      sfa + 8, (kb > 0 || k > 0) ? 1u : 0u);
+                                      sfa + 8, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     umma_commit(&ctl->empty[s]);
-                    if (byte == KB_PER_SF - 1 || kb == KB - 1) umma_commit(&ctl->sempty[slot]);
-                    if (kb == KB - 1) umma_commit(&ctl->tfull);
+                    if (byte == KB_PER_SF - 1 || kb == w.kb1 - 1) umma_commit(&ctl->sempty[slot]);
+                    if (kb == w.kb1 - 1) umma_commit(&ctl->tfull);
                 }
                 __syncwarp();
-                if (byte == KB_PER_SF - 1 || kb == KB - 1) ++gi;
+                if (byte == KB_PER_SF - 1 || kb == w.kb1 - 1) ++gi;
             }
         }
         if (lane == 0) {
@@ -272,21 +277,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t gi = 0;
         bool ok = true, bad = false;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item w = decode_item(t, split, KB);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
             const int m = tl.m0 + q * 32 + lane;
             const bool vrow = m < tl.row_end;
             const int nb0 = tl.n0 / 128;
             const float* sb0 = sb + ((size_t)tl.g * NB + nb0) * KB;
-            for (int kb0 = 0; kb0 < KB; kb0 += KB_PER_SF, ++gi) {
+            for (int kb0 = w.kb0; kb0 < w.kb1; kb0 += KB_PER_SF, ++gi) {
                 // Scales first (their latency overlaps the wait for the slot).
                 float fa[KB_PER_SF], fb0[KB_PER_SF], fb1[KB_PER_SF];
 #pragma unroll
                 for (int j = 0; j < KB_PER_SF; ++j) {
                     const int kb = kb0 + j;
-                    fa[j] = (kb < KB && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
-                    fb0[j] = kb < KB ? sb0[kb] : 1.0f;
-                    fb1[j] = (kb < KB && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
+                    fa[j] = (kb < w.kb1 && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
+                    fb0[j] = kb < w.kb1 ? sb0[kb] : 1.0f;
+                    fb1[j] = (kb < w.kb1 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
                 }
                 uint32_t wa = 0, wb0 = 0, wb1 = 0;
 #pragma unroll
@@ -320,10 +326,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int h = (warp - EPI_WARP0) >> 2;   // column half of the tile
         const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+        uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
+        // One 32 x 32 bf16 block (16 packed pairs per lane) through this warp's
+        // buffer and a TMA store.  Row `lane`, 16-byte piece k goes to offset
+        // lane*64 + ((k ^ ((lane >> 1) & 3)) << 4): the 64-byte swizzle the
+        // tensor map declares.
+        auto store_block = [&](const uint32_t* pk, int col, int row) {
+            if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tm_c, buf, col, row);
+                bulk_commit_group();
+            }
+        };
         uint32_t tt = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tt) {
-            const Tile tl = decode_tile<BM, BN, GROUPED>(t, M, N, cum, offsets, G);
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tt) {
+            const Item w = decode_item(t, split, KB);
+            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
             const int m = tl.m0 + q * 32 + lane;
             const int col0 = tl.n0 + h * 128;
             bool got = mbar_wait_sleep(&ctl->tfull, tt & 1, kWaitLimitNs);
@@ -334,6 +360,58 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tacc;
+            if (w.parts > 1) {
+                // A K-split tile of the last wave (this CTA's last item): the fp32
+                // part goes straight from TMEM to the workspace, and the warp that
+                // completes this slice's ticket adds the parts in part order.
+                const bool live = col0 < N;
+                float* part0 = split.part + (size_t)(w.tile - split.n_full) * w.parts * (BM * BN) +
+                               (size_t)(h * 128) * BM + q * 32 + lane;   // [part][col][row]
+                float* dst = part0 + (size_t)w.part * (BM * BN);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld_x32(taddr + 32 * cc, v);
+                    tmem_ld_wait();
+                    if (live) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) __stcg(dst + (cc * 32 + jj) * BM, __uint_as_float(v[jj]));
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty);
+                if (!live) continue;
+                const int wslot = (w.tile - split.n_full) * EPI_WARPS + (warp - EPI_WARP0);
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&split.ticket[wslot], 1) == w.parts - 1;
+                if (!__shfl_sync(0xFFFFFFFFu, last, 0)) continue;
+                __threadfence();
+                if (lane == 0) split.ticket[wslot] = 0;   // ready for the next call
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    float sum[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) sum[jj] = 0.0f;
+#pragma unroll 1
+                    for (int pp = 0; pp < w.parts; ++pp) {
+                        const float* src = part0 + (size_t)pp * (BM * BN) + (size_t)(cc * 32) * BM;
+                        float v[32];
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) v[jj] = __ldcg(src + jj * BM);
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) sum[jj] += v[jj];
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        pk[jj] = pack_bf16x2(__float_as_uint(sum[2 * jj]), __float_as_uint(sum[2 * jj + 1]));
+                    store_block(pk, col0 + 32 * cc, tl.m0 + q * 32);
+                }
+                continue;
+            }
             // Three round trips (64, 32 and 32 columns), packed to bf16 pairs as
             // they arrive so that at most 64 raw values are live; TMEM goes back
             // before any store.
@@ -344,9 +422,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_x32(taddr + 32, v1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
-                    p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+                for (int jj = 0; jj < 16; ++jj) {
+                    p[jj] = pack_bf16x2(v0[2 * jj], v0[2 * jj + 1]);
+                    p[16 + jj] = pack_bf16x2(v1[2 * jj], v1[2 * jj + 1]);
                 }
             }
 #pragma unroll
@@ -355,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_x32(taddr + 32 * r, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) p[16 * r + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                for (int jj = 0; jj < 16; ++jj) p[16 * r + jj] = pack_bf16x2(v[2 * jj], v[2 * jj + 1]);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -363,31 +441,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (col0 >= N) continue;   // the half of a 256-wide tile past N
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
-                // Row `lane` of the block, 16-byte piece k of 32-column chunk cc,
-                // goes to offset lane*64 + ((k ^ ((lane >> 1) & 3)) << 4): the
-                // 64-byte swizzle the tensor map declares.
-                uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int j = 16 * cc + 4 * k;
-                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
-                            make_uint4(p[j], p[j + 1], p[j + 2], p[j + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, tl.m0 + q * 32);
-                        bulk_commit_group();
-                    }
-                }
+                for (int cc = 0; cc < 4; ++cc) store_block(p + 16 * cc, col0 + 32 * cc, tl.m0 + q * 32);
             } else if (lane < rows_here) {
                 uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                for (int jj = 0; jj < 16; ++jj)
+                    dst[jj] = make_uint4(p[4 * jj], p[4 * jj + 1], p[4 * jj + 2], p[4 * jj + 3]);
             }
         }
         if (lane == 0) bulk_wait_group<0>();   // stores complete before the CTA exits
@@ -416,8 +476,18 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
+    SplitTail split{0, 1, nullptr, nullptr};
+    if (!GROUPED) {
+        const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kMxMaxParts);
+        if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
+            split.n_full = (int)tp.n_full;
+            split.parts = tp.parts;
+            split.ticket = static_cast<int*>(a.workspace);
+            split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
+        }
+    }
     kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
-                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status);
+                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split);
     return cudaGetLastError();
 }
 

@@ -117,46 +117,6 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[
     fma32_packed(acc, v, sc);
 }
 
-// Tail split: the last, partial wave of output tiles (dense only) is split
-// along K so that it fills the GPU.  Tiles [0, n_full) are computed whole;
-// each tile n_full + i is computed as `parts` items over K-block ranges
-// [p KB / parts, (p + 1) KB / parts), whose fp32 results meet in `part`
-// ([tile][part][column][row]) and are added in part order by the warp that
-// completes the tile slice's ticket.  parts <= 1: no split.
-struct SplitTail {
-    int n_full;
-    int parts;
-    float* part;
-    int* ticket;      // one per (split tile, promotion warp); zero between calls
-};
-
-struct Item {
-    int tile, kb0, kb1, part, parts;
-};
-
-__host__ __device__ __forceinline__ int work_items(int n_tiles, const SplitTail& sp) {
-    return sp.parts > 1 ? sp.n_full + (n_tiles - sp.n_full) * sp.parts : n_tiles;
-}
-
-__device__ __forceinline__ Item decode_item(int t, const SplitTail& sp, int KB) {
-    Item w;
-    if (sp.parts <= 1 || t < sp.n_full) {
-        w.tile = t;
-        w.kb0 = 0;
-        w.kb1 = KB;
-        w.part = 0;
-        w.parts = 1;
-    } else {
-        const int j = t - sp.n_full;
-        w.tile = sp.n_full + j / sp.parts;
-        w.part = j % sp.parts;
-        w.parts = sp.parts;
-        w.kb0 = w.part * KB / sp.parts;
-        w.kb1 = (w.part + 1) * KB / sp.parts;
-    }
-    return w;
-}
-
 template <int BN, bool GROUPED>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -532,7 +492,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
     if (!GROUPED) {
-        const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN);
+        const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kPromoteMaxParts);
         if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
             split.n_full = (int)tp.n_full;
             split.parts = tp.parts;
@@ -549,21 +509,25 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
 
 // Split of the last wave (dense): with `grid` = min(tiles, SMs) persistent
 // CTAs, the first (tiles / grid) * grid tiles fill whole waves; the L left
-// over are split along K into min(grid / L, KB / 8, 4) parts when that is at
-// least 2.
-TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn) {
+// over are split along K into min(grid / L, KB / 8, max_parts) parts when
+// that is at least 2 (promote: 4; MX, whose single accumulator is held while
+// a part is written out: 2, and only when L >= grid / 4).
+TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts) {
     TailPlan tp{0, 1, 0, 0};
     if (M <= 0 || bn <= 0 || sm_count <= 0) return tp;
     const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
     const int64_t grid = tiles < sm_count ? tiles : sm_count;
     const int64_t full = (tiles / grid) * grid, left = tiles - full;
     if (left == 0 || full == 0) return tp;
-    // At least 8 K-blocks per part and at most 4 parts: each extra part costs
-    // the warp that completes a tile another 16 KB read of fp32 partials, and
-    // 8 parts of 4 K-blocks measured slower than no split.
+    // MX: a last wave under a quarter of the SMs measured slower split than
+    // whole (Llama qkv: 8 tiles left, 77 -> 80 us).
+    if (max_parts <= kMxMaxParts && left * 4 < grid) return tp;
+    // At least 8 K-blocks per part and at most max_parts parts: each extra part
+    // costs the warp that completes a tile another 16 KB read of fp32
+    // partials (8 parts of 4 K-blocks measured slower than no split).
     int64_t parts = grid / left;
     if (parts > (K / 128) / 8) parts = (K / 128) / 8;
-    if (parts > 4) parts = 4;
+    if (parts > max_parts) parts = max_parts;
     if (parts < 2) return tp;
     const int epi_warps = bn == 128 ? 16 : 8;
     tp.n_full = full;
@@ -573,8 +537,12 @@ TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn) {
     return tp;
 }
 
+// Enough for the last-wave split of either large-M kernel (promote: its tile
+// width; MX: 256).
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
-    return tail_plan(M, N, K, sm_count, promote_tile_n(M, N, K, 1)).bytes;
+    const size_t p = tail_plan(M, N, K, sm_count, promote_tile_n(M, N, K, 1), kPromoteMaxParts).bytes;
+    const size_t x = tail_plan(M, N, K, sm_count, 256, kMxMaxParts).bytes;
+    return p > x ? p : x;
 }
 
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {

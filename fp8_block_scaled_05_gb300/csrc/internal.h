@@ -54,15 +54,16 @@ struct GemmArgs {
 int promote_tile_n(int64_t M, int64_t N, int64_t K, int32_t G);
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st);
 
-// Dense promote kernel: the last, partial wave of tiles is split along K when
-// the caller's workspace holds `bytes` (tickets first, then fp32 parts).
+// Dense promote and MX kernels: the last, partial wave of tiles is split along
+// K when the caller's workspace holds `bytes` (tickets first, then fp32 parts).
 struct TailPlan {
     int64_t n_full;       // tiles computed whole
     int parts;            // parts per remaining tile (1: no split)
     size_t ticket_bytes;  // zero-initialised tickets at the start of the workspace
     size_t bytes;         // workspace needed for the split (0 when none)
 };
-TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn);
+constexpr int kPromoteMaxParts = 4, kMxMaxParts = 2;
+TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts);
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
 
 // Dense / grouped kernel for power-of-two scales: the tensor core applies the

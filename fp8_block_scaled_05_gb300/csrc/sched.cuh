@@ -83,4 +83,45 @@ __device__ __forceinline__ int build_group_table(const int32_t* __restrict__ off
     return carry;
 }
 
+// Tail split of the persistent large-M kernels: the last, partial wave of
+// output tiles (dense only) is split along K so that it fills the GPU.
+// Tiles [0, n_full) are computed whole; each tile n_full + i is computed as
+// `parts` items over K-block ranges [p KB / parts, (p + 1) KB / parts), whose
+// fp32 results meet in `part` ([tile][part][column][row]) and are added in
+// part order by the warp that completes the tile slice's ticket (one slice
+// per epilogue warp).  parts <= 1: no split.
+struct SplitTail {
+    int n_full;
+    int parts;
+    float* part;
+    int* ticket;      // one per (split tile, epilogue warp); zero between calls
+};
+
+struct Item {
+    int tile, kb0, kb1, part, parts;
+};
+
+__host__ __device__ __forceinline__ int work_items(int n_tiles, const SplitTail& sp) {
+    return sp.parts > 1 ? sp.n_full + (n_tiles - sp.n_full) * sp.parts : n_tiles;
+}
+
+__device__ __forceinline__ Item decode_item(int t, const SplitTail& sp, int KB) {
+    Item w;
+    if (sp.parts <= 1 || t < sp.n_full) {
+        w.tile = t;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.part = 0;
+        w.parts = 1;
+    } else {
+        const int j = t - sp.n_full;
+        w.tile = sp.n_full + j / sp.parts;
+        w.part = j % sp.parts;
+        w.parts = sp.parts;
+        w.kb0 = w.part * KB / sp.parts;
+        w.kb1 = (w.part + 1) * KB / sp.parts;
+    }
+    return w;
+}
+
 }  // namespace fp8bs

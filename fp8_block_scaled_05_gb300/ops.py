@@ -253,9 +253,9 @@ def gemm(qa, sa, qb, sb, pow2: bool = False, path: str = "auto", out: torch.Tens
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
     flags = PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0)
     # The size query follows the automatic plan: for M <= 256 the split-K
-    # skinny kernel, above it the promote kernel's last-wave split (optional,
+    # skinny kernel, above it the large-M kernels' last-wave split (optional,
     # so a plan mismatch only costs that split).
-    ws = workspace_for(M, N, K, 1, qa.device) if path in ("auto", "skinny", "promote") else None
+    ws = workspace_for(M, N, K, 1, qa.device)
     fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags, ws, stream)
     return c
 

@@ -152,11 +152,10 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  *     workspace must not run concurrently.
  *     - Skinny path (M <= 256): required; smaller or NULL returns
  *       FP8_ERR_WORKSPACE.
- *     - Promote path: optional.  With it, when the output tiles do not fill
- *       whole waves of the GPU's SMs, the tiles of the last wave are split
- *       along K and their fp32 parts added in a fixed order; without it (or
- *       if it is too small) every tile is computed whole.
- *     - MX path: unused.
+ *     - Promote and MX paths: optional.  With it, when the output tiles do
+ *       not fill whole waves of the GPU's SMs, the tiles of the last wave are
+ *       split along K and their fp32 parts added in a fixed order; without it
+ *       (or if it is too small) every tile is computed whole.
  */
 FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
                                 const uint8_t *qb, int64_t ldb, const float *sb,

@@ -68,27 +68,30 @@ def test_promote_ragged(ops, M, N, K):
     assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"promote {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("path", ["promote", "mx"])
 @pytest.mark.parametrize("M", [1200, 1280])
-def test_promote_last_wave_split(ops, M):
+def test_last_wave_split(ops, M, path):
     """10 x 16 = 160 output tiles on 152 SMs: the 8 tiles of the last wave are
     split along K into 2 parts (16 K-blocks: at least 8 per part) whose fp32
     results are added in part order.
     Checked against the oracle, bit-identical on a second call (fixed order),
     and within tolerance without a workspace (no split)."""
     N, K = 4096, 2048
-    qa, sa, qw, sw = _case(M, N, K, seed=M)
+    pow2 = path == "mx"
+    qa, sa, qw, sw = _case(M, N, K, seed=M, pow2=pow2)
     ref = O.gemm_ref(qa, sa, qw, sw)
     dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
     assert ops.fp8_gemm_workspace_size(M, N, K, 1) > 0
-    c1 = ops.gemm(dqa, dsa, dqw, dsw, path="promote")
-    c2 = ops.gemm(dqa, dsa, dqw, dsw, path="promote")
+    c1 = ops.gemm(dqa, dsa, dqw, dsw, pow2=pow2, path=path)
+    c2 = ops.gemm(dqa, dsa, dqw, dsw, pow2=pow2, path=path)
     c0 = torch.empty_like(c1)
-    ops.fp8_blockscaled_gemm(dqa, dsa, dqw, dsw, c0, ops.FP8_GEMM_PATH_PROMOTE, None)
+    flags = ops.PATHS[path] | (ops.FP8_GEMM_SCALES_POW2 if pow2 else 0)
+    ops.fp8_blockscaled_gemm(dqa, dsa, dqw, dsw, c0, flags, None)
     torch.cuda.synchronize()
     assert ops.fp8_last_device_status() == 0
     assert torch.equal(c1, c2)
-    assert_gemm_close(bf16_to_np(c1), ref, f"promote split M={M}")
-    assert_gemm_close(bf16_to_np(c0), ref, f"promote unsplit M={M}")
+    assert_gemm_close(bf16_to_np(c1), ref, f"{path} split M={M}")
+    assert_gemm_close(bf16_to_np(c0), ref, f"{path} unsplit M={M}")
 
 
 @pytest.mark.parametrize("M", [1, 2, 8, 16, 17, 33, 64, 100, 128, 200, 256])
