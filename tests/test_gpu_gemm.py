@@ -68,14 +68,14 @@ def test_promote_ragged(ops, M, N, K):
     assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"promote {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("path", ["promote", "mx"])
-@pytest.mark.parametrize("M", [1200, 1280])
+@pytest.mark.parametrize("path,M", [("promote", 1200), ("promote", 1280), ("mx", 1500), ("mx", 1536)])
 def test_last_wave_split(ops, M, path):
-    """10 x 16 = 160 output tiles on 152 SMs: the 8 tiles of the last wave are
-    split along K into 2 parts (16 K-blocks: at least 8 per part) whose fp32
-    results are added in part order.
-    Checked against the oracle, bit-identical on a second call (fixed order),
-    and within tolerance without a workspace (no split)."""
+    """Output tiles that do not fill whole waves of 152 SMs: promote, 10 x 16 =
+    160 tiles, the 8 of the last wave split along K into 2 parts (16 K-blocks,
+    at least 8 per part); MX, 12 x 16 = 192 tiles, the 40 of the last wave (at
+    least a quarter of the SMs) split into 2.  The fp32 parts are added in
+    part order.  Checked against the oracle, bit-identical on a second call
+    (fixed order), and within tolerance without a workspace (no split)."""
     N, K = 4096, 2048
     pow2 = path == "mx"
     qa, sa, qw, sw = _case(M, N, K, seed=M, pow2=pow2)
