@@ -304,7 +304,7 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         return cuda_status(launch_gemm_skinny(a, st));
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
-    a.bn = mx ? 256 : promote_tile_n(M, N, K, 1);
+    a.bn = mx ? kMxTileN : promote_tile_n(M, N, K, 1);
     if (workspace && aligned16(workspace)) {
         // optional: lets the kernel split its last wave of tiles
         a.workspace = workspace;
@@ -352,7 +352,7 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.sm_count = d->sm_count;
     a.splits = 1;
     const bool mx = path == FP8_GEMM_PATH_MX;
-    a.bn = mx ? 256 : promote_tile_n(M_total, N, K, G);
+    a.bn = mx ? kMxTileN : promote_tile_n(M_total, N, K, G);
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M_total, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
         return e;

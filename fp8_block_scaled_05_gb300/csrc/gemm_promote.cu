@@ -532,7 +532,8 @@ TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int ma
     const int epi_warps = bn == 128 ? 16 : 8;
     tp.n_full = full;
     tp.parts = (int)parts;
-    tp.ticket_bytes = ((size_t)left * epi_warps * sizeof(int) + 255) & ~size_t(255);
+    if (left * epi_warps > kMaxTickets) return tp;
+    tp.ticket_bytes = kTicketBytes;
     tp.bytes = tp.ticket_bytes + (size_t)left * parts * 128 * bn * sizeof(float);
     return tp;
 }
@@ -541,7 +542,7 @@ TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int ma
 // width; MX: 256).
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
     const size_t p = tail_plan(M, N, K, sm_count, promote_tile_n(M, N, K, 1), kPromoteMaxParts).bytes;
-    const size_t x = tail_plan(M, N, K, sm_count, 256, kMxMaxParts).bytes;
+    const size_t x = tail_plan(M, N, K, sm_count, kMxTileN, kMxMaxParts).bytes;
     return p > x ? p : x;
 }
 

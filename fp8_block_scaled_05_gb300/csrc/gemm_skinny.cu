@@ -292,12 +292,12 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
                     }
                 }
             } else {
-                // Partials: ws layout [tickets: TC*NB int32, padded to 256 B]
+                // Partials: ws layout [tickets: TC*NB int32 in the fixed ticket region]
                 //                     [splits][TC*NB][NT][128] fp32 (row fastest, coalesced),
                 // TC = gridDim.z token chunks.
                 const int PT = gridDim.z * NB;
                 int32_t* tickets = reinterpret_cast<int32_t*>(ws);
-                float* part = reinterpret_cast<float*>(ws + (((size_t)PT * 4 + 255) & ~size_t(255)));
+                float* part = reinterpret_cast<float*>(ws + kTicketBytes);
                 float* mine = part + (((size_t)split * PT + ptile) * NT) * BMW;
 #pragma unroll
                 for (int j = 0; j < C::CPW; ++j) mine[(size_t)(col0 + j) * BMW + row] = acc[j];
@@ -392,6 +392,7 @@ static int64_t skinny_chunks(int64_t M) {
 
 int skinny_splits(int64_t M, int64_t N, int64_t K, int sm_count) {
     const int64_t tiles = (N / 128) * (skinny_chunks(M) > 0 ? skinny_chunks(M) : 1), KB = K / 128;
+    if (tiles > kMaxTickets) return 1;   // more tiles than ticket words: no split
     int64_t s = sm_count / (tiles > 0 ? tiles : 1);
     if (s > KB / 2) s = KB / 2;     // at least two K-blocks per split
     if (s > 32) s = 32;
@@ -404,7 +405,7 @@ size_t skinny_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     const int nt = skinny_tile_n(M);
     if (nt == 0 || splits <= 1) return 0;
     const int64_t PT = (N / 128) * skinny_chunks(M);
-    return (((size_t)PT * 4 + 255) & ~size_t(255)) + (size_t)splits * PT * nt * 128 * sizeof(float);
+    return kTicketBytes + (size_t)splits * PT * nt * 128 * sizeof(float);
 }
 
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
@@ -470,7 +471,7 @@ cudaError_t launch_gemm_skinny_noalloc(GemmArgs a, cudaStream_t st) {
     if (need > 0) {
         // ticket words of the split-K reduction (layout of the kernel's workspace)
         const size_t tickets = ((size_t)(a.N / 128) * skinny_chunks(a.M) * 4 + 255) & ~size_t(255);
-        e = cudaMemsetAsync(scratch, 0, tickets, st);
+        e = cudaMemsetAsync(scratch, 0, tickets, st);   // the part of the ticket region this call uses
         if (e != cudaSuccess) return e;
     }
     a.workspace = scratch;

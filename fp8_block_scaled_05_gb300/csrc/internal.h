@@ -8,6 +8,13 @@
 
 namespace fp8bs {
 
+// Every GEMM workspace starts with this many bytes of split-K / last-wave
+// tickets (int32, zero between calls: each call leaves the ones it used at
+// zero); the fp32 partials of every path start after it, so one call's
+// partials never land on the tickets another call relies on.
+constexpr size_t kTicketBytes = size_t(64) << 10;
+constexpr int64_t kMaxTickets = (int64_t)(kTicketBytes / sizeof(int32_t));
+
 // Upper bound on any single wait inside a kernel before it records a timeout
 // and returns (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
@@ -63,12 +70,13 @@ struct TailPlan {
     size_t bytes;         // workspace needed for the split (0 when none)
 };
 constexpr int kPromoteMaxParts = 4, kMxMaxParts = 2;
+constexpr int kMxTileN = 256;   // MX kernel output tile width
 TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts);
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
 
 // Dense / grouped kernel for power-of-two scales: the tensor core applies the
 // scales as UE8M0 block scale factors (tcgen05.mma kind::mxf8f6f4); output
-// tile 128 x 256, a.tm_b with box {128, 256}, a.tm_c as noted above.  Every scale must be a power of
+// tile 128 x 256 (kMxTileN), a.tm_b with box {128, 256}, a.tm_c as noted above.  Every scale must be a power of
 // two in [2^-127, 2^127]; others are reported in the status word.
 cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st);
 

@@ -146,10 +146,10 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  * M >= 0 (0 is a no-op), N, K > 0 and multiples of 128.  All pointers 16-byte aligned.
  * flags: FP8_GEMM_SCALES_POW2 | one FP8_GEMM_PATH_* value.
  * workspace: device scratch of fp8_gemm_workspace_size(M, N, K, 1) bytes (may be
- *     NULL when that size is 0).  Its first bytes hold split-K semaphores that
- *     must be zero before the first use; every completed call leaves them zero
- *     again (allocate it zero-filled once and reuse it).  Calls that share a
- *     workspace must not run concurrently.
+ *     NULL when that size is 0).  Its first 64 KiB hold split-K semaphores
+ *     that must be zero before the first use; every completed call leaves them
+ *     zero again (allocate it zero-filled once and reuse it, for any shapes).
+ *     Calls that share a workspace must not run concurrently.
  *     - Skinny path (M <= 256): required; smaller or NULL returns
  *       FP8_ERR_WORKSPACE.
  *     - Promote and MX paths: optional.  With it, when the output tiles do
@@ -212,7 +212,7 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
  * - All calls share the array, and it keeps what the last call left in it.
  *   The call clears the ticket words on `stream` before its launch.  Calls
  *   that overlap on the GPU (unordered streams) race on the array: order them.
- * - The scratch needed is 256-byte-rounded 4*T bytes of tickets plus
+ * - The scratch needed is 65536 bytes of tickets plus
  *   splits * T * NT * 128 * 4 bytes of partials, where NT = M rounded up to
  *   16, 32, 64 or 128 (128 for M > 64), T = (N/128) * ceil(M / NT) (tokens
  *   beyond 128 run as further 128-token chunks), and splits is as reported by

@@ -113,9 +113,9 @@ def test_workspace_size_and_plan(L):
     from fp8_block_scaled_05_gb300 import ops
     # Large M (no device here, so 152 SMs are assumed): 32 x 24 = 768 tiles of
     # 128 x 256 are 5 full waves + 8 tiles; those 8 are split into
-    # min(152 // 8, 32 // 8, 4) = 4 parts: 256 bytes of tickets (8 tiles x 8
-    # warps x 4, rounded to 256) + 8 x 4 fp32 128 x 256 parts.
-    assert ops.fp8_gemm_workspace_size(4096, 6144, 4096) == 256 + 8 * 4 * 128 * 256 * 4
+    # min(152 // 8, 32 // 8, 4) = 4 parts: the fixed 64 KiB ticket region +
+    # 8 x 4 fp32 128 x 256 parts.
+    assert ops.fp8_gemm_workspace_size(4096, 6144, 4096) == 65536 + 8 * 4 * 128 * 256 * 4
     assert ops.fp8_gemm_workspace_size(4096, 4864, 4096) == 0          # 32 x 19 = 608 tiles: 4 full waves
     assert ops.fp8_gemm_workspace_size(4096, 6144, 1920) == 0          # 15 K-blocks: no 2 parts of 8
     assert ops.fp8_gemm_workspace_size(1, 6144, 4096) > 0              # decode: split-K partials

@@ -94,6 +94,33 @@ def test_last_wave_split(ops, M, path):
     assert_gemm_close(bf16_to_np(c0), ref, f"{path} unsplit M={M}")
 
 
+def test_workspace_shared_across_shapes(ops):
+    """One zero-initialised workspace reused, in sequence, by calls of several
+    shapes and paths whose tickets and partials differ in size (split-K decode,
+    last-wave splits of both large-M kernels): each call's partials must never
+    land on the tickets a later call relies on.  Every result is checked
+    against the oracle."""
+    seq = [("promote", 1280, 4096, 2048), ("promote", 1536, 4096, 2048), ("skinny", 8, 640, 2048),
+           ("mx", 1536, 4096, 2048), ("skinny", 64, 4096, 4096), ("promote", 1280, 4096, 2048),
+           ("skinny", 8, 640, 2048), ("mx", 1536, 4096, 2048)]
+    cache = {}
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    for path, M, N, K in seq:
+        pow2 = path == "mx"
+        key = (M, N, K, pow2)
+        if key not in cache:
+            qa, sa, qw, sw = _case(M, N, K, seed=M + N, pow2=pow2)
+            cache[key] = (_to_dev(qa, sa, qw, sw), O.gemm_ref(qa, sa, qw, sw))
+        (dqa, dsa, dqw, dsw), ref = cache[key]
+        assert ops.fp8_gemm_workspace_size(M, N, K, 1) <= ws.numel()
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ops.fp8_blockscaled_gemm(dqa, dsa, dqw, dsw, c, ops.PATHS[path] | (ops.FP8_GEMM_SCALES_POW2 if pow2 else 0), ws)
+        torch.cuda.synchronize()
+        assert ops.fp8_last_device_status() == 0
+        assert_gemm_close(bf16_to_np(c), ref, f"shared workspace {path} {M}x{N}x{K}")
+    assert int(ws[:65536].view(torch.int32).abs().sum()) == 0   # tickets left at zero
+
+
 @pytest.mark.parametrize("M", [1, 2, 8, 16, 17, 33, 64, 100, 128, 200, 256])
 def test_skinny_ragged(ops, M):
     N, K = 640, 2048
