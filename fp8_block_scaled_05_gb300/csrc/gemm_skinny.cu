@@ -145,6 +145,11 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile int32_t* abort_flag = &ctl->abort_flag;
+    // The prologue above overlaps the previous kernel (programmatic dependent
+    // launch); its outputs (the activation codes and scales, usually) are read
+    // only from here on.  The next kernel may start its own prologue now.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -369,6 +374,10 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t st) {
         attr_done_mask |= 1 << (dev & 31);
     }
     dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits, (unsigned)((a.M + NT - 1) / NT));
+    if (pdl_for_tokens(a.M))   // programmatic dependent launch: measured faster up to 32 tokens only
+        return launch_pdl(k_gemm_skinny<NT>, grid, dim3(C::THREADS), smem_bytes<NT>(), st, a.tm_b, a.tm_a, a.sa,
+                          a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
+                          a.splits, static_cast<uint8_t*>(a.workspace), a.status);
     k_gemm_skinny<NT><<<grid, C::THREADS, smem_bytes<NT>(), st>>>(
         a.tm_b, a.tm_a, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N, (int)a.K,
         a.splits, static_cast<uint8_t*>(a.workspace), a.status);

@@ -19,6 +19,30 @@ constexpr int64_t kMaxTickets = (int64_t)(kTicketBytes / sizeof(int32_t));
 // and returns (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
+// Launches `kern` with programmatic stream serialization: it may start while
+// the previous kernel in the stream finishes, and waits for it in
+// griddep_wait() (the kernel must call that before touching its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Decode-sized steps (activation quantiser + skinny GEMM) launch with
+// programmatic stream serialization: measured 7-12% faster per layer at
+// 1..8 tokens, but 1.5-6% slower at 64..256 tokens with K = 14336.
+inline bool pdl_for_tokens(int64_t M) { return M <= 32; }
+
 // Codes written to the per-device status word (same values as fp8_status).
 constexpr int kStatusTimeout = 8;
 

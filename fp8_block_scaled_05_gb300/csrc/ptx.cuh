@@ -397,6 +397,19 @@ __device__ __forceinline__ void regs_alloc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// In a kernel launched with programmatic stream serialization: blocks until
+// the grids this one depends on have completed and their memory is visible
+// (a no-op otherwise).  Must precede every global access to data they wrote.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream, if launched with programmatic stream
+// serialization, start its CTAs (up to their griddep_wait) before this grid
+// has finished.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }

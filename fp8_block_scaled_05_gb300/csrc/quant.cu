@@ -16,6 +16,7 @@
 
 #include "codec.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8bs {
 
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const int64_t m0 = (int64_t)blockIdx.x * kActRows;
     const int64_t kb0 = (int64_t)blockIdx.y * kActKB;
+    griddep_wait();                  // x may come from the previous kernel in the stream
+    griddep_launch_dependents();     // the GEMM that follows may start its prologue
 
     uint4 v[kActItems];
 #pragma unroll
@@ -110,6 +113,9 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
     if (M == 0) return cudaSuccess;
     const int64_t KB = K / 128;
     dim3 grid((unsigned)((M + kActRows - 1) / kActRows), (unsigned)((KB + kActKB - 1) / kActKB));
+    if (pdl_for_tokens(M))   // a decode step: overlap with the kernels around it
+        return launch_pdl(k_quant_act_1x128, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x), M, KB, ldx, q,
+                          ldq, s, lds, pow2 ? 1 : 0);
     k_quant_act_1x128<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds,
                                             pow2 ? 1 : 0);
     return cudaGetLastError();

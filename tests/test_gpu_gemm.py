@@ -253,6 +253,35 @@ def test_qwen_prefill_full_size_sampled_rows(ops, layer, pow2):
     assert_gemm_close(bf16_to_np(y[rows]), ref, f"qwen prefill {layer} pow2={pow2}")
 
 
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_decode_layer_chain(ops, M):
+    """Decode steps as a model runs them: for each of three layers the
+    activation quantiser and then the skinny GEMM, back to back on one stream
+    with no synchronisation (up to 32 tokens both launch as programmatic
+    dependents, so each kernel's prologue overlaps the previous kernel), the
+    next layer's input being written by the host copy in between.  Every
+    layer's codes and output are checked against the oracle."""
+    K, N = 4096, 2048
+    layers = []
+    for i in range(3):
+        x = I.normal_bf16(I.stream(90 + i, M), (M, K))
+        w = I.normal_bf16(I.stream(95 + i, M), (N, K), std=0.02)
+        qw, sw = ops.quant_weight(w.cuda())
+        layers.append((x, qw, sw))
+    torch.cuda.synchronize()
+    outs = []
+    for x, qw, sw in layers:
+        qa, sa = ops.quant_act(x.cuda())
+        outs.append((ops.gemm(qa, sa, qw, sw), qa, sa))
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    for (x, qw, sw), (y, qa, sa) in zip(layers, outs):
+        qa_o, sa_o = O.quant_act_1x128(bf16_to_np(x))
+        assert np.array_equal(qa.cpu().numpy(), qa_o)
+        ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
+        assert_gemm_close(bf16_to_np(y), ref, f"decode chain M={M}")
+
+
 @pytest.mark.parametrize("K,N", [(14336, 4096), (4096, 6144)])
 @pytest.mark.parametrize("M", [1, 8, 64, 256])
 def test_decode_full_size(ops, M, K, N):
