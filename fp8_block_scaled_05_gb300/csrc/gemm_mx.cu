@@ -464,14 +464,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <bool GROUPED>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
-    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    static DeviceOnce attr_done;     // kernel attributes set on this device
     auto kern = k_gemm_mx<GROUPED>;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!(attr_done_mask & (1 << (dev & 31)))) {
+    if (!attr_done.test(dev)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done_mask |= 1 << (dev & 31);
+        attr_done.set(dev);
     }
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;

@@ -472,11 +472,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
 template <int BN, bool GROUPED>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<BN>;
-    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    static DeviceOnce attr_done;     // kernel attributes set on this device
     auto kern = k_gemm_promote<BN, GROUPED>;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!(attr_done_mask & (1 << (dev & 31)))) {
+    if (!attr_done.test(dev)) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
@@ -485,7 +485,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         if (C::SPLIT_REGS && fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<BN>());
         if (e != cudaSuccess) return e;
-        attr_done_mask |= 1 << (dev & 31);
+        attr_done.set(dev);
     }
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;

@@ -364,14 +364,14 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
 template <int NT>
 cudaError_t launch_nt(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<NT>;
-    static int attr_done_mask = 0;   // bit per device ordinal (< 32)
+    static DeviceOnce attr_done;     // kernel attributes set on this device
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!(attr_done_mask & (1 << (dev & 31)))) {
+    if (!attr_done.test(dev)) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_skinny<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem_bytes<NT>());
         if (e != cudaSuccess) return e;
-        attr_done_mask |= 1 << (dev & 31);
+        attr_done.set(dev);
     }
     dim3 grid((unsigned)(a.N / BMW), (unsigned)a.splits, (unsigned)((a.M + NT - 1) / NT));
     if (pdl_for_tokens(a.M))   // programmatic dependent launch: measured faster up to 32 tokens only

@@ -1,6 +1,7 @@
 // Host-side interface between the C-ABI layer (api.cu) and the kernel
 // translation units.  Not part of the public ABI.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -42,6 +43,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // programmatic stream serialization: measured 7-12% faster per layer at
 // 1..8 tokens, but 1.5-6% slower at 64..256 tokens with K = 14336.
 inline bool pdl_for_tokens(int64_t M) { return M <= 32; }
+
+// Per-device "done once" flags for a kernel's attribute set-up, safe to query
+// from several host threads (devices past 63 redo the set-up on every call,
+// which is harmless).
+struct DeviceOnce {
+    std::atomic<bool> done[64];
+    bool test(int dev) const { return dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire); }
+    void set(int dev) {
+        if (dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+    }
+};
 
 // Codes written to the per-device status word (same values as fp8_status).
 constexpr int kStatusTimeout = 8;
