@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "codec.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -120,10 +121,10 @@ __device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[
 template <int BN, bool GROUPED>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_c,
+                   const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
-                   const int32_t* __restrict__ offsets, int G, int* status, SplitTail split) {
+                   const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -405,6 +406,49 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     for (int j = 0; j < 32; ++j) acc[cc][j] = sum[j];
                 }
             }
+            if constexpr (BN == 256 && !GROUPED) {
+                if (qo.q != nullptr) {
+                    // Fused quantisation for the next layer: this warp holds, per row,
+                    // the whole 128-column block col0 .. col0 + 127, so the row's
+                    // amax needs no exchange.  Codes and scale are those the 1x128
+                    // activation quantiser gives for the bf16-rounded outputs.
+                    uint32_t pk[64];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+                                : "=r"(pk[16 * cc + e])
+                                : "f"(acc[cc][2 * e + 1]), "f"(acc[cc][2 * e]));
+                    uint32_t m2 = 0;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) m2 = absmax_bf16x2(m2, pk[e]);
+                    const BlockScale bs = make_scale(absmax_pair_to_f32(m2), qo.pow2 != 0);
+                    if (vrow) qo.s[(size_t)(col0 / 128) * qo.lds + m] = bs.s;
+                    // two 32 x 64-byte halves through the warp's buffer (64-byte swizzle)
+                    uint8_t* qbuf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int j0 = 32 * hf + 8 * k;   // first packed pair of this 16-byte piece
+                            const uint2 c0 = quant8(make_uint4(pk[j0], pk[j0 + 1], pk[j0 + 2], pk[j0 + 3]), bs);
+                            const uint2 c1 = quant8(make_uint4(pk[j0 + 4], pk[j0 + 5], pk[j0 + 6], pk[j0 + 7]), bs);
+                            *reinterpret_cast<uint4*>(qbuf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(c0.x, c0.y, c1.x, c1.y);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_q, qbuf, col0 + 64 * hf, tl.m0 + q * 32);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (!qo.write_c) continue;
+                }
+            }
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
                 // 32 x 32 blocks through this warp's 2 KB buffer and TMA stores:
@@ -500,8 +544,9 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
-    kern<<<grid, C::THREADS, smem_bytes<BN>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c),
-                                               a.ldc, (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split);
+    kern<<<grid, C::THREADS, smem_bytes<BN>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
+                                                     static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
+                                                     (int)a.K, a.offsets, a.G, a.status, split, a.qout);
     return cudaGetLastError();
 }
 

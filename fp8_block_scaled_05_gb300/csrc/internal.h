@@ -72,10 +72,23 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int
                                         int64_t ldq, float* s, bool pow2, cudaStream_t st);
 
 // ------------------------------------------------------------- GEMMs
+// Fused quantisation of the GEMM's output for the next layer: the E4M3 codes
+// and 1x128 scales fp8_quant_act_1x128 would produce from the bf16 C.
+struct QuantOut {
+    uint8_t* q;         // codes [M][ldq]; nullptr: no fused quantisation
+    int64_t ldq;
+    float* s;           // scales, K-block-major: s[(column / 128) * lds + row]
+    int64_t lds;
+    int pow2;           // scale rule of the codes (FP8_SCALE_POW2)
+    int write_c;        // also write the bf16 C
+};
+
 struct GemmArgs {
     CUtensorMap tm_a;               // qa [rows, K] uint8, box {128, 128}, 128B swizzle
     CUtensorMap tm_b;               // qb [rows, K] uint8, box {128, BN}, 128B swizzle
     CUtensorMap tm_c;               // promote / MX: c [rows, N] bf16, box {32, 32}, 64B swizzle
+    CUtensorMap tm_q;               // promote with QuantOut: codes [rows, N] u8, box {64, 32}, 64B swizzle
+    QuantOut qout;                  // promote: fused output quantisation (qout.q == nullptr: none)
     const float* sa;
     int64_t ldsa;
     const float* sb;

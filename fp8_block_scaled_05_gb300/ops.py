@@ -47,6 +47,8 @@ SIGNATURES = {
                                                     _i64, _i64, _u32, _vp, _sz, _vp]),
     "fp8_blockscaled_gemm_skinny_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64,
                                                            _i64, _i64, _u32, _vp]),
+    "fp8_blockscaled_gemm_quant": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _i64, _vp,
+                                                  _i64, _i64, _i64, _i64, _u32, ctypes.c_int, _vp, _sz, _vp]),
     "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
@@ -154,6 +156,29 @@ def fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Ten
     _check(lib().fp8_blockscaled_gemm(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0),
                                       _ptr(sb), _ptr(c), c.stride(0), M, N, K, int(flags), _ptr(workspace),
                                       ws_bytes, _stream(stream)), "fp8_blockscaled_gemm")
+
+
+def fp8_blockscaled_gemm_quant(qa, sa, qb, sb, c, qc, sc, flags: int = 0, out_mode: int = FP8_SCALE_FP32_AMAX,
+                               workspace: torch.Tensor | None = None, stream=None) -> None:
+    """C = block-scaled GEMM, and the 1x128 E4M3 quantisation of bf16(C) for
+    the next layer: qc uint8 [M, N], sc fp32 [N/128, >= M]; c (bf16 [M, N])
+    may be None."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(qc, torch.uint8, "qc")
+    _need(sc, torch.float32, "sc")
+    if c is not None:
+        _need(c, torch.bfloat16, "c")
+    M, K = qa.shape
+    N = qb.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_blockscaled_gemm_quant(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0),
+                                            _ptr(sb), _ptr(c), c.stride(0) if c is not None else 0, _ptr(qc),
+                                            qc.stride(0), _ptr(sc), sc.stride(0), M, N, K, int(flags),
+                                            int(out_mode), _ptr(workspace), ws_bytes, _stream(stream)),
+           "fp8_blockscaled_gemm_quant")
 
 
 def fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags: int = 0,
@@ -268,6 +293,21 @@ def grouped_gemm(qa, sa, offsets, qb, sb, pow2: bool = False, path: str = "auto"
     flags = PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0)
     fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags, None, stream)
     return c
+
+
+def gemm_quant(qa, sa, qb, sb, pow2: bool = False, out_pow2: bool = False, with_c: bool = True, stream=None):
+    """Block-scaled GEMM with the next layer's 1x128 quantisation fused in.
+    Returns (c or None, qc, sc) with sc in the [N/128, round_up(M, 4)] layout
+    of quant_act's scales."""
+    M, K = qa.shape
+    N = qb.shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device) if with_c else None
+    qc = torch.empty((M, N), dtype=torch.uint8, device=qa.device)
+    sc = torch.empty((N // 128, round_up(M, 4)), dtype=torch.float32, device=qa.device)
+    ws = workspace_for(M, N, K, 1, qa.device)
+    fp8_blockscaled_gemm_quant(qa, sa, qb, sb, c, qc, sc, FP8_GEMM_SCALES_POW2 if pow2 else 0,
+                               FP8_SCALE_POW2 if out_pow2 else FP8_SCALE_FP32_AMAX, ws, stream)
+    return c, qc, sc
 
 
 def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):

@@ -164,6 +164,33 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
                                 fp8_stream_t stream);
 
 /*
+ * Block-scaled FP8 GEMM with the next layer's activation quantisation fused
+ * into its epilogue.  The pages project a gain from fusing the quantisation
+ * kernels (upppp.jp NeMo RL FP8 article, §重要度サンプリングで精度を保つ).
+ *
+ * Computes C exactly as fp8_blockscaled_gemm (promote kernel), rounds it to
+ * bf16, and writes the E4M3 codes and 1x128 scales that
+ * fp8_quant_act_1x128(C_bf16, ..., out_mode) would produce from it: qc and sc
+ * are bit-identical to running the GEMM and then the activation quantiser on
+ * its output, without the bf16 round trip through memory.
+ *
+ * qa, sa, qb, sb, M, N, K, workspace: as fp8_blockscaled_gemm.
+ * c   optional (NULL: not written); bf16 [M, N], row pitch ldc (>= N, % 8 == 0).
+ * qc  device, uint8 [M, N], row pitch ldqc (>= N, % 16 == 0), 16-byte aligned.
+ * sc  device, fp32 [N/128][ldsc]: scale of row m, column block j at sc[j * ldsc + m]
+ *     (ldsc >= M, % 4 == 0, 16-byte aligned) -- the layout the next GEMM's sa takes.
+ * flags: FP8_GEMM_SCALES_POW2 (about sa, sb) | FP8_GEMM_PATH_AUTO or _PROMOTE;
+ *     the MX and skinny paths return FP8_ERR_NOT_IMPLEMENTED.
+ * out_mode: the scale rule of qc/sc (FP8_SCALE_FP32_AMAX or FP8_SCALE_POW2).
+ */
+FP8BS_API fp8_status fp8_blockscaled_gemm_quant(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                                const uint8_t *qb, int64_t ldb, const float *sb,
+                                                void *c, int64_t ldc, uint8_t *qc, int64_t ldqc,
+                                                float *sc, int64_t ldsc, int64_t M, int64_t N, int64_t K,
+                                                uint32_t flags, fp8_scale_mode out_mode,
+                                                void *workspace, size_t ws_bytes, fp8_stream_t stream);
+
+/*
  * Grouped (mixture-of-experts) block-scaled GEMM: for each expert g < G,
  * rows offsets[g] .. offsets[g+1]-1 of A (tokens sorted by expert) times
  * expert g's weights:

@@ -102,6 +102,32 @@ def test_gemm_validation(L):
         assert call() == 6
 
 
+def test_gemm_quant_validation(L):
+    f = L.fp8_blockscaled_gemm_quant
+    ok = dict(qa=A16, lda=256, sa=A16b, ldsa=8, qb=A16c, ldb=256, sb=A16, c=A16b, ldc=128, qc=A16c, ldqc=128,
+              sc=A16, ldsc=8, M=8, N=128, K=256, flags=0, mode=0, ws=NULL, wsb=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["qa"], a["lda"], a["sa"], a["ldsa"], a["qb"], a["ldb"], a["sb"], a["c"], a["ldc"], a["qc"],
+                 a["ldqc"], a["sc"], a["ldsc"], a["M"], a["N"], a["K"], a["flags"], a["mode"], a["ws"], a["wsb"],
+                 NULL)
+
+    assert call(qc=NULL) == 1
+    assert call(sc=NULL) == 1
+    assert call(mode=7) == 4
+    assert call(ldqc=120) == 2
+    assert call(ldsc=4) == 2
+    assert call(ldqc=136) == 3
+    assert call(sc=MIS) == 3
+    assert call(flags=0x21) == 9                  # the MX path has no fused quantisation
+    assert call(flags=0x30) == 9                  # nor the skinny path
+    assert call(M=0, qc=NULL) == 0
+    if not _has_gpu():
+        assert call() == 6                        # valid arguments; no sm_103 device here
+        assert call(c=NULL, ldc=0) == 6           # C is optional
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0
