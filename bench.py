@@ -54,6 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-pow2", action="store_true", help="skip the power-of-two scale-mode measurement")
+    p.add_argument("--no-fused", action="store_true", help="skip the fused GEMM + quantisation measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -443,6 +444,58 @@ def run_ours(args, world, rank, local):
                 "gemm_frac_fp8": flops_step / (p_gemm_ms / 1e3) / 1e12 / fp8_peak,
                 "kernels_ms": p_kern, "gpu_launches": launches_per_step * args.steps}
 
+    # ---------------- the GEMM with the next layer's quantisation fused into its
+    # epilogue, against the GEMM followed by the activation quantiser of its
+    # output (same inputs; each variant timed per layer over flushed steps).
+    fused = None
+    if not args.no_fused:
+        fl = {}
+        for L, pw in [(L, pw) for pw in (False, True) for L in layers]:
+            M, N = L["M"], L["N"]
+            qc = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            sc = torch.empty((N // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev)
+            mode = ops.FP8_SCALE_POW2 if pw else ops.FP8_SCALE_FP32_AMAX
+            flags = ops.FP8_GEMM_SCALES_POW2 if pw else 0
+            # operands in the matching scale mode
+            with torch.cuda.stream(stream):
+                ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], mode, stream)
+                ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream)
+
+            def unfused():
+                ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, L["ws"], stream)
+                ops.fp8_quant_act_1x128(L["c"], qc, sc, mode, stream)
+
+            def fused_c():
+                ops.fp8_blockscaled_gemm_quant(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], qc, sc, flags, mode,
+                                               L["ws"], stream)
+
+            def fused_noc():
+                ops.fp8_blockscaled_gemm_quant(L["qa"], L["sa"], L["qw"], L["sw"], None, qc, sc, flags, mode,
+                                               L["ws"], stream)
+
+            res = {"gemm_kernel": "mx" if pw else "promote"}
+            for name, fn in (("unfused_ms", unfused), ("fused_ms", fused_c), ("fused_no_c_ms", fused_noc)):
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup):
+                        flush.zero_()
+                        fn()
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.steps)]
+                with torch.cuda.stream(stream):
+                    for e0, e1 in evs:
+                        flush.zero_()
+                        e0.record(stream)
+                        fn()
+                        e1.record(stream)
+                torch.cuda.synchronize(dev)
+                res[name] = sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+            res["speedup"] = res["unfused_ms"] / res["fused_ms"]
+            res["speedup_no_c"] = res["unfused_ms"] / res["fused_no_c_ms"]
+            fl[L["name"] + (".pow2" if pw else ".fp32")] = res
+        fused = {"what": "GEMM then 1x128 quantisation of its bf16 output (unfused) vs the quantisation fused "
+                         "into the GEMM epilogue, with and without writing the bf16 output",
+                 "layers": fl}
+
     st = ops.fp8_last_device_status(stream)
     if st != 0:
         raise SystemExit(f"device status after the timed region: {ops.status_string(st)}")
@@ -473,6 +526,7 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "pow2": pow2,
+            "fused_quant": fused,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }

@@ -332,8 +332,11 @@ fp8_status fp8_blockscaled_gemm_quant(const uint8_t* qa, int64_t lda, const floa
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c ? c : static_cast<const void*>(qc),
                                          c ? ldc : N, M, N, K, flags))
         return e;
-    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
-    if (path != FP8_GEMM_PATH_AUTO && path != FP8_GEMM_PATH_PROMOTE) return FP8_ERR_NOT_IMPLEMENTED;
+    // large-M kernels only: MX for power-of-two scales (its epilogue warps have
+    // the time), promote otherwise
+    const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
+    if (forced == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    const bool mx = forced == FP8_GEMM_PATH_MX || (forced == FP8_GEMM_PATH_AUTO && (flags & FP8_GEMM_SCALES_POW2));
     if (M == 0) return FP8_OK;
     if (!qc || !sc) return FP8_ERR_NULL;
     if (ldb < K || ldqc < N || ldsc < M) return FP8_ERR_SHAPE;
@@ -379,7 +382,8 @@ fp8_status fp8_blockscaled_gemm_quant(const uint8_t* qa, int64_t lda, const floa
     if (fp8_status e = tensor_map(qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, N, M, ldqc, 64, 32, CU_TENSOR_MAP_SWIZZLE_64B,
                                   &a.tm_q))
         return e;
-    return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
 fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,

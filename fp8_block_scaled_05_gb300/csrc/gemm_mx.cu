@@ -60,6 +60,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "codec.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -135,9 +136,10 @@ __device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
 template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const __grid_constant__ CUtensorMap tm_c, const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
+              const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
+              const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
               int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status,
-              SplitTail split) {
+              SplitTail split, QuantOut qo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
@@ -439,6 +441,37 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tempty);
             if (col0 >= N) continue;   // the half of a 256-wide tile past N
+            if (!GROUPED && qo.q != nullptr) {
+                // Fused quantisation for the next layer: this warp holds, per row,
+                // the whole 128-column block col0 .. col0 + 127 as bf16 pairs, so
+                // the row's amax needs no exchange; codes and scale are those the
+                // 1x128 activation quantiser gives for these bf16 values.
+                uint32_t m2 = 0;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) m2 = absmax_bf16x2(m2, p[e]);
+                const BlockScale bs = make_scale(absmax_pair_to_f32(m2), qo.pow2 != 0);
+                if (m < tl.row_end) qo.s[(size_t)(col0 / 128) * qo.lds + m] = bs.s;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j0 = 32 * hf + 8 * k;
+                        const uint2 c0 = quant8(make_uint4(p[j0], p[j0 + 1], p[j0 + 2], p[j0 + 3]), bs);
+                        const uint2 c1 = quant8(make_uint4(p[j0 + 4], p[j0 + 5], p[j0 + 6], p[j0 + 7]), bs);
+                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(c0.x, c0.y, c1.x, c1.y);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_q, buf, col0 + 64 * hf, tl.m0 + q * 32);
+                        bulk_commit_group();
+                    }
+                }
+                if (!qo.write_c) continue;
+            }
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
 #pragma unroll
@@ -477,7 +510,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
-    if (!GROUPED) {
+    if (!GROUPED && a.qout.q == nullptr) {   // the fused quantisation needs whole tiles
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kMxMaxParts);
         if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
             split.n_full = (int)tp.n_full;
@@ -486,8 +519,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
-                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split);
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
+                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout);
     return cudaGetLastError();
 }
 

@@ -168,8 +168,9 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
  * into its epilogue.  The pages project a gain from fusing the quantisation
  * kernels (upppp.jp NeMo RL FP8 article, §重要度サンプリングで精度を保つ).
  *
- * Computes C exactly as fp8_blockscaled_gemm (promote kernel), rounds it to
- * bf16, and writes the E4M3 codes and 1x128 scales that
+ * Computes C as fp8_blockscaled_gemm does (the promote kernel, or the MX
+ * kernel for power-of-two scales), rounds it to bf16, and writes the E4M3
+ * codes and 1x128 scales that
  * fp8_quant_act_1x128(C_bf16, ..., out_mode) would produce from it: qc and sc
  * are bit-identical to running the GEMM and then the activation quantiser on
  * its output, without the bf16 round trip through memory.
@@ -179,8 +180,11 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
  * qc  device, uint8 [M, N], row pitch ldqc (>= N, % 16 == 0), 16-byte aligned.
  * sc  device, fp32 [N/128][ldsc]: scale of row m, column block j at sc[j * ldsc + m]
  *     (ldsc >= M, % 4 == 0, 16-byte aligned) -- the layout the next GEMM's sa takes.
- * flags: FP8_GEMM_SCALES_POW2 (about sa, sb) | FP8_GEMM_PATH_AUTO or _PROMOTE;
- *     the MX and skinny paths return FP8_ERR_NOT_IMPLEMENTED.
+ * flags: FP8_GEMM_SCALES_POW2 (about sa, sb) | FP8_GEMM_PATH_AUTO, _PROMOTE or
+ *     _MX (AUTO: MX with FP8_GEMM_SCALES_POW2, else promote); the skinny path
+ *     returns FP8_ERR_NOT_IMPLEMENTED.  On the promote kernel the cast runs
+ *     on the warps that bound its speed and measured slower than the separate
+ *     quantiser; on the MX kernel it runs on otherwise idle epilogue warps.
  * out_mode: the scale rule of qc/sc (FP8_SCALE_FP32_AMAX or FP8_SCALE_POW2).
  */
 FP8BS_API fp8_status fp8_blockscaled_gemm_quant(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,

@@ -120,12 +120,13 @@ def test_gemm_quant_validation(L):
     assert call(ldsc=4) == 2
     assert call(ldqc=136) == 3
     assert call(sc=MIS) == 3
-    assert call(flags=0x21) == 9                  # the MX path has no fused quantisation
-    assert call(flags=0x30) == 9                  # nor the skinny path
+    assert call(flags=0x20) == 4                  # MX without the pow2 promise
+    assert call(flags=0x30) == 9                  # the skinny path has no fused quantisation
     assert call(M=0, qc=NULL) == 0
     if not _has_gpu():
         assert call() == 6                        # valid arguments; no sm_103 device here
         assert call(c=NULL, ldc=0) == 6           # C is optional
+        assert call(flags=0x21) == 6              # MX with pow2 scales
 
 
 def test_grouped_validation(L):

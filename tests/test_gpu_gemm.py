@@ -123,14 +123,15 @@ def test_workspace_shared_across_shapes(ops):
 
 @pytest.mark.parametrize("M,N,K", [(200, 384, 512), (300, 1024, 1152), (129, 256, 128), (1, 512, 256),
                                    (1280, 4096, 2048)])
-@pytest.mark.parametrize("pow2,out_pow2", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("pow2,out_pow2", [(False, False), (True, True), (False, True), (True, False)])
 def test_gemm_quant_fused(ops, M, N, K, pow2, out_pow2):
     """GEMM with the next layer's 1x128 quantisation fused into the epilogue:
     the codes and scales must be exactly those of fp8_quant_act_1x128 (and of
     the oracle's quantiser) applied to the bf16 C the same call writes; C is
     within tolerance of the oracle; without C the codes and scales are the
     same.  Covers a half-empty last tile (N = 384), ragged M, K = 128, M = 1
-    and the last-wave K split (M = 1280, N = 4096)."""
+    and the last-wave K split (M = 1280, N = 4096).  Power-of-two input scales
+    take the MX kernel, the others the promote kernel."""
     qa, sa, qw, sw = _case(M, N, K, seed=M + K, pow2=pow2)
     ref = O.gemm_ref(qa, sa, qw, sw)
     dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
@@ -147,22 +148,24 @@ def test_gemm_quant_fused(ops, M, N, K, pow2, out_pow2):
     assert np.array_equal(sc[:, :M].cpu().numpy(), s_o.T)
 
 
-def test_gemm_quant_fused_llama_gate_up_sampled_rows(ops):
+@pytest.mark.parametrize("pow2", [False, True])
+def test_gemm_quant_fused_llama_gate_up_sampled_rows(ops, pow2):
     """Full-size Llama-3.1-8B gate+up GEMM with its output quantised in the
-    epilogue: sampled rows' C against the oracle, codes and scales against the
+    epilogue (promote kernel with fp32 scales, MX kernel with power-of-two
+    scales): sampled rows' C against the oracle, codes and scales against the
     oracle's quantiser of the same bf16 rows."""
     case = I.llama8b_layers(layers=["gate_up"])[0]
-    qa, sa = ops.quant_act(case.a.cuda())
-    qw, sw = ops.quant_weight(case.w.cuda())
-    c, qc, sc = ops.gemm_quant(qa, sa, qw, sw)
+    qa, sa = ops.quant_act(case.a.cuda(), pow2)
+    qw, sw = ops.quant_weight(case.w.cuda(), pow2)
+    c, qc, sc = ops.gemm_quant(qa, sa, qw, sw, pow2=pow2, out_pow2=pow2)
     torch.cuda.synchronize()
     assert ops.fp8_last_device_status() == 0
     rows = np.sort(np.random.Generator(np.random.PCG64(23)).choice(case.a.shape[0], 16, replace=False))
-    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]))
+    qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
     ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
     c_rows = bf16_to_np(c[rows])
     assert_gemm_close(c_rows, ref, "gemm_quant llama gate_up")
-    q_o, s_o = O.quant_act_1x128(c_rows)
+    q_o, s_o = O.quant_act_1x128(c_rows, pow2)
     assert np.array_equal(qc[rows].cpu().numpy(), q_o)
     assert np.array_equal(sc[:, rows].cpu().numpy(), s_o.T)
 
