@@ -33,8 +33,10 @@ round-to-nearest-even and saturation at +-448; the power-of-two scale is
 reference is dequantise-then-multiply in fp64.
 
 Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
-against facts that do not come from this file (the OCP code table, library
-casts, exact rational arithmetic, brute force and closed forms).
+and (training-side functions) tests/test_oracle_pins_training.py against
+facts that do not come from this file (the OCP code table, library
+casts, exact rational arithmetic, brute force, PyTorch autograd and closed
+forms).
 """
 from __future__ import annotations
 
@@ -51,6 +53,8 @@ __all__ = [
     "quant_act_1x128", "quant_weight_128x128",
     "dequant_act", "dequant_weight",
     "gemm_ref", "gemm_ref_rows", "grouped_gemm_ref",
+    "block_amax_col", "quant_act_128x1", "quant_weight_128x128_t",
+    "dgrad_ref", "wgrad_ref", "wgrad_ref_rows",
 ]
 
 
@@ -255,3 +259,81 @@ def grouped_gemm_ref(qa, sa, offsets, qw_groups, sw_groups, rows=None) -> np.nda
         r = want[sel]
         out[sel] = dequant_act(qa[r], sa[r]) @ dequant_weight(qw_groups[g], sw_groups[g]).T
     return out
+
+
+# --------------------------------------------------------------------------
+# Training-side operands and GEMMs
+#
+# The pages apply FP8 to training as well as generation ("end-to-end FP8":
+# page "NVIDIA NeMo RL достигает ускорения на 48% благодаря сквозному обучению
+# с точностью FP8", §Технический прорыв; page "エンドツーエンドFP8精度で実現
+# する高スループット強化学習トレーニング", the opening section: parameters,
+# activations, gradients and optimizer updates).  For a linear layer
+# y = x W^T the backward pass computes dX = dY W and dW = dY^T X.  The pages
+# name only the 1x128 (activations) and 128x128 (weights) blocks; the reading
+# taken here is that every operand is quantised in blocks of 128 along the
+# dimension its GEMM reduces over:
+#   dgrad  dX = dY W   : dY in 1x128 blocks along its rows (reduction over
+#                        output features), W in its 128x128 blocks;
+#   wgrad  dW = dY^T X : dY and X in 128x1 blocks (128 consecutive tokens of
+#                        one column), the reduction being over tokens.
+# --------------------------------------------------------------------------
+def block_amax_col(x: np.ndarray) -> np.ndarray:
+    """max |x| over each 128x1 block (128 consecutive rows of one column) of a
+    [M, K] float32 matrix -> [M/128, K]."""
+    M, K = x.shape
+    _check_mult(M, "M")
+    return np.abs(x).reshape(M // QBLOCK, QBLOCK, K).max(axis=1).astype(np.float32)
+
+
+def quant_act_128x1(x: np.ndarray, pow2: bool = False):
+    """128x1 (column-wise) activation quantisation, the wgrad operand.
+
+    x: float32 [M, K] (bf16 values), M tokens.  The block of column k, tokens
+    mb*128 .. mb*128+127 gets scale s[mb, k] from its own amax, and
+    q[m, k] = e4m3(x[m, k] / s[m/128, k]).  Returned transposed, the way the
+    wgrad GEMM reads them (token-contiguous rows): (qt uint8 [K, M] with
+    qt[k, m] = q[m, k], st float32 [K, M/128] with st[k, mb] = s[mb, k]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    s = scale_from_amax(block_amax_col(x), pow2)
+    q = _cast(x, np.repeat(s, QBLOCK, axis=0))
+    return np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
+def quant_weight_128x128_t(w: np.ndarray, pow2: bool = False):
+    """The 128x128 quantisation of W seen from W^T, the dgrad operand.
+
+    A 128x128 block of W^T is the transpose of a block of W and has the same
+    amax, so its codes and scale are those of W's block, transposed:
+    (qt uint8 [K, N] = q^T, st float32 [K/128, N/128] = s^T).
+    """
+    q, s = quant_weight_128x128(w, pow2)
+    return np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
+def dgrad_ref(q_dy, s_dy, q_w, s_w) -> np.ndarray:
+    """Input gradient of y = x W^T: dX[m, k] = sum_n deq(dY)[m, n] deq(W)[n, k]
+    in float64.
+
+    q_dy uint8 [M, N] with 1x128 scales s_dy [M, N/128] (blocks along n, the
+    reduction); q_w uint8 [N, K] with 128x128 scales s_w [N/128, K/128].
+    """
+    return dequant_act(q_dy, s_dy) @ dequant_weight(q_w, s_w)
+
+
+def wgrad_ref(qt_dy, st_dy, qt_x, st_x) -> np.ndarray:
+    """Weight gradient of y = x W^T: dW[n, k] = sum_m deq(dY)[m, n] deq(X)[m, k]
+    in float64.
+
+    Both operands come as quant_act_128x1 returns them: qt_dy uint8 [N, M]
+    (row n = column n of dY, token-contiguous) with st_dy [N, M/128], and
+    qt_x uint8 [K, M] with st_x [K, M/128].
+    """
+    return dequant_act(qt_dy, st_dy) @ dequant_act(qt_x, st_x).T
+
+
+def wgrad_ref_rows(qt_dy, st_dy, qt_x, st_x, rows) -> np.ndarray:
+    """wgrad_ref restricted to the given output rows n (for sampled checks)."""
+    rows = np.asarray(rows)
+    return dequant_act(qt_dy[rows], st_dy[rows]) @ dequant_act(qt_x, st_x).T
