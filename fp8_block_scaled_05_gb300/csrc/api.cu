@@ -236,6 +236,46 @@ fp8_status fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t
                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt, int64_t ldqt,
+                               float* st, int64_t ldst, uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                               fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (M < 0 || K <= 0 || (M % 128) || (K % 128) || M / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x || !qt || !st) return FP8_ERR_NULL;
+    if ((q == nullptr) != (s == nullptr)) return FP8_ERR_NULL;   // the 1x128 outputs come as a pair
+    if (ldx < K || ldqt < M || ldst < K) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldqt % 16) || (ldst % 4) || !aligned16(x) || !aligned16(qt) || !aligned16(st))
+        return FP8_ERR_ALIGN;
+    if (q != nullptr) {
+        if (ldq < K || lds < M) return FP8_ERR_SHAPE;
+        if ((ldq % 16) || (lds % 4) || !aligned16(q) || !aligned16(s)) return FP8_ERR_ALIGN;
+    }
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_act_128x1(x, M, K, ldx, qt, ldqt, st, ldst, q, ldq, s, lds,
+                                              mode == FP8_SCALE_POW2, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                                      float* s, uint8_t* qt, int64_t ldqt, float* st, fp8_scale_mode mode,
+                                      fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (N <= 0 || K <= 0 || (N % 128) || (K % 128) || N / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (!w || !qt || !st) return FP8_ERR_NULL;
+    if ((q == nullptr) != (s == nullptr)) return FP8_ERR_NULL;   // W's own codes come as a pair
+    if (ldw < K || ldqt < N) return FP8_ERR_SHAPE;
+    if ((ldw % 8) || (ldqt % 16) || !aligned16(w) || !aligned16(qt) || !aligned16(st)) return FP8_ERR_ALIGN;
+    if (q != nullptr) {
+        if (ldq < K) return FP8_ERR_SHAPE;
+        if ((ldq % 16) || !aligned16(q) || !aligned16(s)) return FP8_ERR_ALIGN;
+    }
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_weight_128x128_t(w, N, K, ldw, q, ldq, s, qt, ldqt, st, mode == FP8_SCALE_POW2,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t* splits) {
     const uint32_t path = plan_path(M, K, flags);
     int32_t sp = 1;
@@ -319,6 +359,53 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
+    return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
+}
+
+fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                      const uint8_t* qb, int64_t ldb, const float* sb, int64_t ldsb, void* c,
+                                      int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags, void* workspace,
+                                      size_t ws_bytes, fp8_stream_t stream) {
+    if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M, N, K, flags)) return e;
+    const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
+    if (forced == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    const bool mx = forced == FP8_GEMM_PATH_MX || (forced == FP8_GEMM_PATH_AUTO && (flags & FP8_GEMM_SCALES_POW2));
+    if (M == 0) return FP8_OK;
+    if (ldb < K || ldsb < N) return FP8_ERR_SHAPE;
+    if ((ldb % 16) || (ldsb % 4)) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+
+    GemmArgs a{};
+    a.sa = sa;
+    a.ldsa = ldsa;
+    a.sb = sb;
+    a.ldsb = ldsb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.offsets = nullptr;
+    a.G = 1;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = 1;
+    a.bn = mx ? kMxTileN : promote_tile_n(M, N, K, 1);
+    if (workspace && aligned16(workspace)) {
+        a.workspace = workspace;
+        a.ws_bytes = ws_bytes;
+    }
+    if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+        return e;
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+        return e;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 

@@ -137,9 +137,9 @@ template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
-              const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, uint16_t* __restrict__ c,
-              int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G, int* status,
-              SplitTail split, QuantOut qo) {
+              const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
+              uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G,
+              int* status, SplitTail split, QuantOut qo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int j = 0; j < KB_PER_SF; ++j) {
                     const int kb = kb0 + j;
                     fa[j] = (kb < w.kb1 && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
-                    fb0[j] = kb < w.kb1 ? sb0[kb] : 1.0f;
-                    fb1[j] = (kb < w.kb1 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
+                    fb0[j] = (kb < w.kb1 && ldsb == 0) ? sb0[kb] : 1.0f;
+                    fb1[j] = (kb < w.kb1 && ldsb == 0 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
                 }
                 uint32_t wa = 0, wb0 = 0, wb1 = 0;
 #pragma unroll
@@ -302,6 +302,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     wa |= ue8m0(fa[j], bad) << (8 * j);
                     wb0 |= ue8m0(fb0[j], bad) << (8 * j);
                     wb1 |= ue8m0(fb1[j], bad) << (8 * j);
+                }
+                // B scale-factor column j holds rows n0 + 32 j + lane: the weight
+                // block's scale, or with ldsb > 0 each row's own (sb[kb * ldsb + n])
+                uint32_t vb[8] = {wb0, wb0, wb0, wb0, wb1, wb1, wb1, wb1};
+                if (ldsb > 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = tl.n0 + 32 * j + lane;
+                        uint32_t wj = 0;
+#pragma unroll
+                        for (int i = 0; i < KB_PER_SF; ++i) {
+                            const int kb = kb0 + i;
+                            const float f = (kb < w.kb1 && n < N) ? sb[(size_t)kb * ldsb + n] : 1.0f;
+                            wj |= ue8m0(f, bad) << (8 * i);
+                        }
+                        vb[j] = wj;
+                    }
                 }
                 const uint32_t slot = gi % SF_SLOTS;
                 bool got = mbar_wait_sleep(&ctl->sempty[slot], ((gi / SF_SLOTS) & 1) ^ 1, kWaitLimitNs);
@@ -312,7 +329,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t col = tmem_base + lane_base + SF_COL0 + slot * SF_SLOT_COLS;
-                const uint32_t vb[8] = {wb0, wb0, wb0, wb0, wb1, wb1, wb1, wb1};
                 tmem_st_x1(col + (uint32_t)q, wa);
                 tmem_st_x8(col + 8, vb);
                 tmem_st_wait();
@@ -519,7 +535,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, static_cast<uint16_t*>(a.c), a.ldc,
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, a.ldsb, static_cast<uint16_t*>(a.c), a.ldc,
                                             (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout);
     return cudaGetLastError();
 }

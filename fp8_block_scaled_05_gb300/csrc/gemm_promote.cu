@@ -103,26 +103,26 @@ struct __align__(16) Ctrl {
     ScaleSlot ring[SRING];
 };
 
-template <int BN>
+// ROWB (a scale per B row): a ring of SRING x BN column scales follows the
+// group table.
+template <int BN, bool ROWB = false>
 constexpr size_t smem_bytes() {
     return 1024 /*align slack*/ + (size_t)Cfg<BN>::RING_BYTES + (size_t)Cfg<BN>::EPI_WARPS * EPI_BUF_BYTES +
-           sizeof(Ctrl) + (size_t)(MAX_GROUPS + 1) * sizeof(int32_t);
+           sizeof(Ctrl) + (size_t)(MAX_GROUPS + 4) * sizeof(int32_t) + (ROWB ? (size_t)SRING * BN * sizeof(float) : 0);
 }
-static_assert(smem_bytes<256>() <= 232448 && smem_bytes<128>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<256, true>() <= 232448 && smem_bytes<128, true>() <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record_timeout(int* status) {
     if (status) atomicCAS(status, 0, kStatusTimeout);
 }
 
-__device__ __forceinline__ void fma_chunk(float (&acc)[32], const uint32_t (&v)[32], float sc) {
-    fma32_packed(acc, v, sc);
-}
-
-template <int BN, bool GROUPED>
+// ROWB: sb holds a scale per B row (sb[kb * ldsb + n]), so the promotion
+// multiplies by a per-column scale product (dense only).
+template <int BN, bool GROUPED, bool ROWB>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
-                   const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb,
+                   const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo) {
     using C = Cfg<BN>;
@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     uint8_t* epi_buf = smem + (size_t)C::RING_BYTES;   // 1024-byte aligned
     Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)C::EPI_WARPS * EPI_BUF_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
+    float* sb_ring = reinterpret_cast<float*>(cum + MAX_GROUPS + 4);   // ROWB: [SRING][BN], 16-byte aligned
+    static_assert(!(ROWB && GROUPED), "per-row B scales are dense only");
 
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK;
@@ -281,7 +283,16 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     const bool v = m < tl.row_end;
                     cp_async_4(&S.sa[r], v ? sak + m : sa, v);
                 }
-                if (lane < 2) {
+                if constexpr (ROWB) {
+                    // the tile's BN column scales, 16 bytes per copy (zero past N)
+                    const float* sbk = sb + (size_t)kb * ldsb + tl.n0;
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int c4 = 4 * (lane + 32 * j);
+                        const bool v = tl.n0 + c4 < N;
+                        cp_async_16(sb_ring + slot * BN + c4, v ? sbk + c4 : sb, v);
+                    }
+                } else if (lane < 2) {
                     // BN = 256 spans weight blocks nb0 and nb0 + 1; BN = 128 uses only nb0
                     const int nb = nb0 + (BN == 256 ? lane : 0);
                     const bool v = nb < NB;
@@ -328,9 +339,21 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                const float sc = ctl->ring[slot].sa[row_in_tile] * ctl->ring[slot].sb[sbi];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+                // ROWB: sA here, the column scales inside the FMAs (the slot is
+                // handed back after them)
+                const float sc = ROWB ? ctl->ring[slot].sa[row_in_tile]
+                                      : ctl->ring[slot].sa[row_in_tile] * ctl->ring[slot].sb[sbi];
+                const float* sbv = sb_ring + slot * BN + sl * C::EPI_COLS;
+                auto fma_chunk = [&](float (&a)[32], const uint32_t (&v)[32], int cc) {
+                    if constexpr (ROWB)
+                        fma32_packed_cols(a, v, sc, sbv + cc * 32);
+                    else
+                        fma32_packed(a, v, sc);
+                };
+                if constexpr (!ROWB) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+                }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + sl * C::EPI_COLS;
                 uint32_t v0[32], v1[32];
@@ -345,14 +368,14 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->tempty[b]);
                     ready = mbar_test_wait(&ctl->tfull[kn % C::NBUF], (kn / C::NBUF) & 1);
-                    fma_chunk(acc[0], v0, sc);
+                    fma_chunk(acc[0], v0, 0);
                 } else {
                     // two round trips of two 32-column loads each
                     tmem_ld_x32(taddr, v0);
                     tmem_ld_x32(taddr + 32, v1);
                     tmem_ld_wait();
-                    fma_chunk(acc[0], v0, sc);
-                    fma_chunk(acc[1], v1, sc);
+                    fma_chunk(acc[0], v0, 0);
+                    fma_chunk(acc[1], v1, 1);
                     tmem_ld_x32(taddr + 64, v0);
                     tmem_ld_x32(taddr + 96, v1);
                     tmem_ld_wait();
@@ -361,8 +384,12 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->tempty[b]);
                     ready = mbar_test_wait(&ctl->tfull[kn % C::NBUF], (kn / C::NBUF) & 1);
-                    fma_chunk(acc[2], v0, sc);
-                    fma_chunk(acc[3], v1, sc);
+                    fma_chunk(acc[2], v0, 2);
+                    fma_chunk(acc[3], v1, 3);
+                }
+                if constexpr (ROWB) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
                 }
             }
             if (!ok) break;
@@ -513,11 +540,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     }
 }
 
-template <int BN, bool GROUPED>
+template <int BN, bool GROUPED, bool ROWB = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<BN>;
     static DeviceOnce attr_done;     // kernel attributes set on this device
-    auto kern = k_gemm_promote<BN, GROUPED>;
+    auto kern = k_gemm_promote<BN, GROUPED, ROWB>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done.test(dev)) {
@@ -527,7 +554,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         // The setmaxnreg split is only safe if the CTA really starts with
         // LAUNCH_REGS registers per thread; refuse to launch otherwise.
         if (C::SPLIT_REGS && fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<BN>());
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<BN, ROWB>());
         if (e != cudaSuccess) return e;
         attr_done.set(dev);
     }
@@ -544,8 +571,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
-    kern<<<grid, C::THREADS, smem_bytes<BN>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
-                                                     static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
+    kern<<<grid, C::THREADS, smem_bytes<BN, ROWB>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
+                                                           a.ldsb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
                                                      (int)a.K, a.offsets, a.G, a.status, split, a.qout);
     return cudaGetLastError();
 }
@@ -575,9 +602,9 @@ TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int ma
     if (parts > max_parts) parts = max_parts;
     if (parts < 2) return tp;
     const int epi_warps = bn == 128 ? 16 : 8;
+    if (left * epi_warps > kMaxTickets) return tp;   // more tickets than the region holds: no split
     tp.n_full = full;
     tp.parts = (int)parts;
-    if (left * epi_warps > kMaxTickets) return tp;
     tp.ticket_bytes = kTicketBytes;
     tp.bytes = tp.ticket_bytes + (size_t)left * parts * 128 * bn * sizeof(float);
     return tp;
@@ -594,6 +621,12 @@ size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;
     const bool grouped = a.offsets != nullptr;
+    if (a.ldsb > 0) {   // a scale per B row (dense only)
+        if (grouped) return cudaErrorInvalidValue;
+        if (a.bn == 128) return promote::launch<128, false, true>(a, st);
+        if (a.bn == 256) return promote::launch<256, false, true>(a, st);
+        return cudaErrorInvalidValue;
+    }
     if (a.bn == 128) return grouped ? promote::launch<128, true>(a, st) : promote::launch<128, false>(a, st);
     if (a.bn == 256) return grouped ? promote::launch<256, true>(a, st) : promote::launch<256, false>(a, st);
     return cudaErrorInvalidValue;

@@ -71,6 +71,15 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                         int64_t ldq, float* s, bool pow2, cudaStream_t st);
 
+// Transposing quantisers (training-side GEMM operands).  q == nullptr: the
+// non-transposed codes and scales are not written.
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt, int64_t ldqt,
+                                   float* st, int64_t ldst, uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                                   bool pow2, cudaStream_t stream);
+cudaError_t launch_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                                          float* s, uint8_t* qt, int64_t ldqt, float* st, bool pow2,
+                                          cudaStream_t stream);
+
 // ------------------------------------------------------------- GEMMs
 // Fused quantisation of the GEMM's output for the next layer: the E4M3 codes
 // and 1x128 scales fp8_quant_act_1x128 would produce from the bf16 C.
@@ -92,6 +101,8 @@ struct GemmArgs {
     const float* sa;
     int64_t ldsa;
     const float* sb;
+    int64_t ldsb;                   // 0: sb holds 128x128 block scales [G][N/128][K/128];
+                                    // > 0: a scale per B row, sb[kb * ldsb + n] (dense promote / MX)
     void* c;
     int64_t ldc;
     int64_t M, N, K;

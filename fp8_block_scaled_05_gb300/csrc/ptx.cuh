@@ -138,6 +138,15 @@ __device__ __forceinline__ void cp_async_4(void *dst, const void *src, bool vali
                  : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte
+// aligned); with valid == false nothing is read and the destination is
+// zero-filled.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
 // Arrives on `bar` once all of this thread's earlier cp.async copies have
 // landed (the barrier's expected count must include this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
@@ -382,6 +391,33 @@ __device__ __forceinline__ void fma32_packed(float (&acc)[32], const uint32_t (&
         asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(v[2 * j]), "r"(v[2 * j + 1]));
         asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(s));
         asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * j]), "=f"(acc[2 * j + 1]) : "l"(a));
+    }
+}
+
+// acc[j] = fma(v[j], RN(sa * sbv[j]), acc[j]) for 32 fp32 values: a scale
+// per column (sbv: 32 floats in shared memory, 16-byte aligned, the same
+// address in every lane).  Each scale product is rounded once, as the
+// single-scale form rounds sa * sb.
+__device__ __forceinline__ void fma32_packed_cols(float (&acc)[32], const uint32_t (&v)[32], float sa,
+                                                  const float *sbv) {
+    uint64_t s;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s) : "f"(sa));
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const float4 b = *reinterpret_cast<const float4 *>(sbv + 4 * g);
+        uint64_t p[2];
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p[0]) : "f"(b.x), "f"(b.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p[1]) : "f"(b.z), "f"(b.w));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = 4 * g + 2 * h;
+            uint64_t a, x;
+            asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(p[h]) : "l"(s));
+            asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc[j]), "f"(acc[j + 1]));
+            asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(v[j]), "r"(v[j + 1]));
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(p[h]));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[j]), "=f"(acc[j + 1]) : "l"(a));
+        }
     }
 }
 

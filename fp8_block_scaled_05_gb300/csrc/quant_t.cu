@@ -1,0 +1,235 @@
+// Transposing block quantisers: the operands of the training-side GEMMs of a
+// linear layer y = x W^T.
+//
+// The pages run FP8 through training as well as generation (page "NVIDIA
+// NeMo RL достигает ускорения на 48% благодаря сквозному обучению с
+// точностью FP8", greentreeone.com, §Технический прорыв; ai.warp-studio.com
+// end-to-end FP8 RL article, opening section: activations and gradients
+// too).  With every operand blocked along the dimension its GEMM reduces:
+//   dgrad  dX = dY W     needs W^T with W's own 128x128 blocks
+//                        (k_quant_w_128x128_t: W^T codes, optionally W's too);
+//   wgrad  dW = dY^T X   needs dY and X in 128x1 blocks (128 tokens of one
+//                        column), stored transposed so that the tokens are
+//                        contiguous (k_quant_act_128x1; optionally also the
+//                        1x128 codes that the forward GEMM or dgrad takes).
+// One pass over the bf16 input writes both layouts, so an operand that two
+// GEMMs need is read from HBM once.
+//
+// A CTA takes a 128 x 128 tile with 256 threads.  Thread t holds tile rows
+// 8 rg .. 8 rg + 7 (rg = t / 16) and columns 8 cg .. 8 cg + 7 (cg = t % 16),
+// one 16-byte load per row (a half-warp reads 256 contiguous bytes of one
+// row).  Codes of a tile column are formed from the thread's 8 rows and
+// written as one 8-byte piece into a 16 KB shared-memory tile: row 8 cg + j
+// (the tile column), 16-byte chunk (rg / 2) ^ (cg % 8) -- the XOR keeps the
+// 16 threads of a half-warp on 8 distinct chunks -- then each warp stores 16
+// of its rows with 16-byte stores, 128 contiguous bytes per output row.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "codec.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+constexpr int kTT = 128;   // tile edge (one block edge)
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Element (row i, column j) of the thread's 8 x 8 sub-tile as fp32.
+__device__ __forceinline__ float elem(const uint4 (&v)[8], int i, int j) {
+    const uint32_t w = word_of(v[i], j >> 1);
+    return (j & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
+}
+
+// Codes of the thread's 8 columns (8 rows each) into the shared tile;
+// scale_of(j) gives column j's BlockScale.
+template <typename ScaleOf>
+__device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
+                                                  ScaleOf scale_of) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const BlockScale bs = scale_of(j);
+        uint32_t part[2] = {0u, 0u};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {   // rows 2p (low byte) and 2p + 1
+            const uint32_t pair = quant_pair(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs);
+            part[p >> 1] |= pair << (16 * (p & 1));
+        }
+        const int R = 8 * cg + j;
+        *reinterpret_cast<uint2 *>(tcodes + R * kTT + ((((rg >> 1) ^ (cg & 7))) << 4) + ((rg & 1) << 3)) =
+            make_uint2(part[0], part[1]);
+    }
+}
+
+// The shared tile (after a barrier) to out[(row0 + R) * ldo + col0 + ...]:
+// warp w stores tile rows 16 w .. 16 w + 15, four rows per instruction.
+__device__ __forceinline__ void store_transposed(const uint8_t *tcodes, uint8_t *out, int64_t ldo, int64_t row0,
+                                                 int64_t col0, int warp, int lane) {
+    const int lc = lane & 7;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int R = 16 * warp + 4 * u + (lane >> 3);
+        const uint4 val = *reinterpret_cast<const uint4 *>(tcodes + R * kTT + ((lc ^ ((R >> 3) & 7)) << 4));
+        __stcs(reinterpret_cast<uint4 *>(out + (row0 + R) * ldo + col0 + 16 * lc), val);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128x1 activation blocks (tile (kb, mb) = blockIdx (x, y)), transposed
+// codes qt[k][m] and scales st[mb * ldst + k]; with ROWWISE also the 1x128
+// codes q[m][k] and scales s[kb * lds + m] of the same tile.
+// ---------------------------------------------------------------------------
+template <bool ROWWISE>
+__global__ void __launch_bounds__(256) k_quant_act_128x1(const uint16_t *__restrict__ x, int64_t ldx,
+                                                         uint8_t *__restrict__ qt, int64_t ldqt,
+                                                         float *__restrict__ st, int64_t ldst,
+                                                         uint8_t *__restrict__ q, int64_t ldq,
+                                                         float *__restrict__ s, int64_t lds, int pow2) {
+    __shared__ __align__(16) uint8_t tcodes[kTT * kTT];
+    __shared__ __align__(16) uint32_t colpart[8][16][4];   // per warp: packed |bf16| maxima of column pairs
+    __shared__ float2 colscale[kTT];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cg = lane & 15, rg = 2 * warp + (lane >> 4);
+    const int64_t k0 = (int64_t)blockIdx.x * kTT, m0 = (int64_t)blockIdx.y * kTT;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __ldcs(reinterpret_cast<const uint4 *>(x + (m0 + 8 * rg + i) * ldx + k0 + 8 * cg));
+
+    // column maxima over the thread's rows, then over the warp's two halves
+    uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        cm[0] = absmax_bf16x2(cm[0], v[i].x);
+        cm[1] = absmax_bf16x2(cm[1], v[i].y);
+        cm[2] = absmax_bf16x2(cm[2], v[i].z);
+        cm[3] = absmax_bf16x2(cm[3], v[i].w);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cm[j] = max_u16x2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+    if (lane < 16) *reinterpret_cast<uint4 *>(&colpart[warp][cg][0]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+
+    if constexpr (ROWWISE) {
+        // 1x128 blocks: row 8 rg + i spans the 16 lanes of this half-warp.  A
+        // plain exchange over lane bit 3, then a butterfly reduce-scatter over
+        // bits 2..0 leaves the amax of row item (lane % 8) in a[0].
+        uint32_t a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = absmax8(0u, v[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = max_u16x2(a[j], __shfl_xor_sync(0xFFFFFFFFu, a[j], 8));
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < o; ++j) {
+                const uint32_t send = upper ? a[j] : a[j + o];
+                const uint32_t keep = upper ? a[j + o] : a[j];
+                a[j] = max_u16x2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+            }
+        }
+        const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), pow2 != 0);
+        if (cg < 8) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int src = (lane & 16) | i;
+            const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
+            const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
+            __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
+                   quant8(v[i], scale_from_sr(si, ri, pow2 != 0)));
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < kTT) {
+        const int c = threadIdx.x;
+        uint32_t m2 = 0u;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m2 = max_u16x2(m2, colpart[w][c >> 3][(c & 7) >> 1]);
+        const uint32_t bits = (c & 1) ? (m2 >> 16) : (m2 & 0xFFFFu);
+        const BlockScale bs = make_scale(__uint_as_float(bits << 16), pow2 != 0);
+        colscale[c] = make_float2(bs.s, bs.r);
+        st[(size_t)blockIdx.y * ldst + k0 + c] = bs.s;
+    }
+    __syncthreads();
+    col_codes_to_smem(v, rg, cg, tcodes, [&](int j) {
+        const float2 sr = colscale[8 * cg + j];
+        return scale_from_sr(sr.x, sr.y, pow2 != 0);
+    });
+    __syncthreads();
+    store_transposed(tcodes, qt, ldqt, k0, m0, warp, lane);
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 weight blocks (tile (kb, nb) = blockIdx (x, y)): W^T codes
+// qt[k][n] and scales st[kb * NB + nb]; with q != nullptr also W's codes
+// q[n][k] and scales s[nb * KB + kb].
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_w_128x128_t(const uint16_t *__restrict__ w, int64_t ldw, int64_t KB,
+                                                           int64_t NB, uint8_t *__restrict__ q, int64_t ldq,
+                                                           float *__restrict__ s, uint8_t *__restrict__ qt,
+                                                           int64_t ldqt, float *__restrict__ st, int pow2) {
+    __shared__ __align__(16) uint8_t tcodes[kTT * kTT];
+    __shared__ float red[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cg = lane & 15, rg = 2 * warp + (lane >> 4);
+    const int64_t k0 = (int64_t)blockIdx.x * kTT, n0 = (int64_t)blockIdx.y * kTT;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __ldcs(reinterpret_cast<const uint4 *>(w + (n0 + 8 * rg + i) * ldw + k0 + 8 * cg));
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m2 = absmax8(m2, v[i]);
+    float amax = absmax_pair_to_f32(m2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const BlockScale bs = make_scale(amax, pow2 != 0);
+
+    if (q != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            __stcs(reinterpret_cast<uint2 *>(q + (n0 + 8 * rg + i) * ldq + k0 + 8 * cg), quant8(v[i], bs));
+    }
+    col_codes_to_smem(v, rg, cg, tcodes, [&](int) { return bs; });
+    __syncthreads();
+    store_transposed(tcodes, qt, ldqt, k0, n0, warp, lane);
+    if (threadIdx.x == 0) {
+        st[(size_t)blockIdx.x * NB + blockIdx.y] = bs.s;
+        if (q != nullptr) s[(size_t)blockIdx.y * KB + blockIdx.x] = bs.s;
+    }
+}
+
+cudaError_t launch_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *qt, int64_t ldqt,
+                                   float *st, int64_t ldst, uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                   bool pow2, cudaStream_t stream) {
+    if (M == 0) return cudaSuccess;
+    const dim3 grid((unsigned)(K / kTT), (unsigned)(M / kTT));
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    if (q != nullptr)
+        k_quant_act_128x1<true><<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds, pow2 ? 1 : 0);
+    else
+        k_quant_act_128x1<false><<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, nullptr, 0, nullptr, 0,
+                                                           pow2 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq,
+                                          float *s, uint8_t *qt, int64_t ldqt, float *st, bool pow2,
+                                          cudaStream_t stream) {
+    const int64_t KB = K / kTT, NB = N / kTT;
+    const dim3 grid((unsigned)KB, (unsigned)NB);
+    k_quant_w_128x128_t<<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(w), ldw, KB, NB, q, ldq, s, qt, ldqt,
+                                                  st, pow2 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -49,6 +49,12 @@ SIGNATURES = {
                                                            _i64, _i64, _u32, _vp]),
     "fp8_blockscaled_gemm_quant": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _i64, _vp,
                                                   _i64, _i64, _i64, _i64, _u32, ctypes.c_int, _vp, _sz, _vp]),
+    "fp8_quant_act_128x1": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                           ctypes.c_int, _vp]),
+    "fp8_quant_weight_128x128_t": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp,
+                                                  ctypes.c_int, _vp]),
+    "fp8_blockscaled_gemm_wgrad": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64,
+                                                  _i64, _i64, _u32, _vp, _sz, _vp]),
     "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
@@ -140,6 +146,63 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor,
     N, K = w.shape
     _check(lib().fp8_quant_weight_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(s), int(mode),
                                           _stream(stream)), "fp8_quant_weight_128x128")
+
+
+def fp8_quant_act_128x1(x: torch.Tensor, qt: torch.Tensor, st: torch.Tensor, q: torch.Tensor | None = None,
+                        s: torch.Tensor | None = None, mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
+    """x bf16 [M, K] (M % 128 == 0); qt uint8 [K, M] (128x1 codes, transposed);
+    st fp32 [M/128, ldst >= K]; optionally q uint8 [M, K] and s fp32
+    [K/128, lds >= M] (the 1x128 codes of x from the same pass)."""
+    _need(x, torch.bfloat16, "x")
+    _need(qt, torch.uint8, "qt")
+    _need(st, torch.float32, "st")
+    if q is not None:
+        _need(q, torch.uint8, "q")
+    if s is not None:
+        _need(s, torch.float32, "s")
+    M, K = x.shape
+    _check(lib().fp8_quant_act_128x1(_ptr(x), M, K, x.stride(0), _ptr(qt), qt.stride(0), _ptr(st), st.stride(0),
+                                     _ptr(q), q.stride(0) if q is not None else 0, _ptr(s),
+                                     s.stride(0) if s is not None else 0, int(mode), _stream(stream)),
+           "fp8_quant_act_128x1")
+
+
+def fp8_quant_weight_128x128_t(w: torch.Tensor, qt: torch.Tensor, st: torch.Tensor, q: torch.Tensor | None = None,
+                               s: torch.Tensor | None = None, mode: int = FP8_SCALE_FP32_AMAX,
+                               stream=None) -> None:
+    """w bf16 [N, K]; qt uint8 [K, N] (W^T codes); st fp32 [K/128, N/128]
+    contiguous; optionally q uint8 [N, K] and s fp32 [N/128, K/128] (W's own)."""
+    _need(w, torch.bfloat16, "w")
+    _need(qt, torch.uint8, "qt")
+    _need(st, torch.float32, "st")
+    if not st.is_contiguous() or (s is not None and not s.is_contiguous()):
+        raise ValueError("st and s must be contiguous")
+    if q is not None:
+        _need(q, torch.uint8, "q")
+    if s is not None:
+        _need(s, torch.float32, "s")
+    N, K = w.shape
+    _check(lib().fp8_quant_weight_128x128_t(_ptr(w), N, K, w.stride(0), _ptr(q),
+                                            q.stride(0) if q is not None else 0, _ptr(s), _ptr(qt), qt.stride(0),
+                                            _ptr(st), int(mode), _stream(stream)), "fp8_quant_weight_128x128_t")
+
+
+def fp8_blockscaled_gemm_wgrad(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """C[M, N] (bf16) = qa[M, K] * qb[N, K]^T with 1x128 scales on both
+    operands: sa fp32 [K/128, >= M], sb fp32 [K/128, >= N]."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(c, torch.bfloat16, "c")
+    M, K = qa.shape
+    N = qb.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_blockscaled_gemm_wgrad(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0),
+                                            _ptr(sb), sb.stride(0), _ptr(c), c.stride(0), M, N, K, int(flags),
+                                            _ptr(workspace), ws_bytes, _stream(stream)),
+           "fp8_blockscaled_gemm_wgrad")
 
 
 def fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
@@ -254,6 +317,35 @@ def quant_weight(w: torch.Tensor, pow2: bool = False, stream=None):
     return q, s
 
 
+def quant_act_t(x: torch.Tensor, pow2: bool = False, rowwise: bool = False, stream=None):
+    """128x1 quantisation of x [M, K] (M % 128 == 0), transposed: returns
+    (qt uint8 [K, M], st fp32 [M/128, round_up(K, 4)]), and with rowwise=True
+    also (q, s) as quant_act(x) returns them, from the same pass."""
+    M, K = x.shape
+    qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    st = torch.empty((M // 128, max(round_up(K, 4), 4)), dtype=torch.float32, device=x.device)
+    q = s = None
+    if rowwise:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        s = torch.empty((K // 128, max(round_up(M, 4), 4)), dtype=torch.float32, device=x.device)
+    fp8_quant_act_128x1(x, qt, st, q, s, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return (qt, st, q, s) if rowwise else (qt, st)
+
+
+def quant_weight_t(w: torch.Tensor, pow2: bool = False, with_w: bool = False, stream=None):
+    """W^T operand of the dgrad GEMM: returns (qt uint8 [K, N], st fp32
+    [K/128, N/128]), and with with_w=True also (q, s) as quant_weight(w)."""
+    N, K = w.shape
+    qt = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+    st = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
+    q = s = None
+    if with_w:
+        q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+        s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8_quant_weight_128x128_t(w, qt, st, q, s, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return (qt, st, q, s) if with_w else (qt, st)
+
+
 _ws: dict[int, torch.Tensor] = {}
 
 
@@ -308,6 +400,18 @@ def gemm_quant(qa, sa, qb, sb, pow2: bool = False, out_pow2: bool = False, with_
     fp8_blockscaled_gemm_quant(qa, sa, qb, sb, c, qc, sc, FP8_GEMM_SCALES_POW2 if pow2 else 0,
                                FP8_SCALE_POW2 if out_pow2 else FP8_SCALE_FP32_AMAX, ws, stream)
     return c, qc, sc
+
+
+def wgrad(qt_dy, st_dy, qt_x, st_x, pow2: bool = False, path: str = "auto", out=None, stream=None):
+    """dW [N, K] (bf16) = dY^T X from the transposed 128x1 operands
+    (quant_act_t of dY [T, N] and of X [T, K])."""
+    N, T = qt_dy.shape
+    K = qt_x.shape[0]
+    c = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=qt_dy.device)
+    ws = workspace_for(N, K, T, 1, qt_dy.device)
+    fp8_blockscaled_gemm_wgrad(qt_dy, st_dy, qt_x, st_x, c, PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0),
+                               ws, stream)
+    return c
 
 
 def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):

@@ -119,6 +119,68 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
                                     fp8_scale_mode mode, fp8_stream_t stream);
 
 /*
+ * Training-side operands.  The pages run FP8 through training as well as
+ * generation (greentreeone.com NeMo RL FP8 page, §Технический прорыв;
+ * ai.warp-studio.com end-to-end FP8 RL article, opening section: activations,
+ * gradients and updates).  For a linear layer y = x W^T the backward GEMMs
+ * are dX = dY W (dgrad) and dW = dY^T X (wgrad); every operand is blocked by
+ * 128 along the dimension its GEMM reduces over:
+ *   dgrad: A = dY codes from fp8_quant_act_1x128 (blocks along the output
+ *          features), B = W^T codes from fp8_quant_weight_128x128_t, run
+ *          through fp8_blockscaled_gemm with M = tokens, N = in-features,
+ *          K = out-features;
+ *   wgrad: A = dY^T and B = X^T codes from fp8_quant_act_128x1 (128x1 blocks:
+ *          128 tokens of one column), run through fp8_blockscaled_gemm_wgrad
+ *          with M = out-features, N = in-features, K = tokens.
+ */
+
+/*
+ * 128x1 activation quantisation, written transposed (the wgrad operand):
+ *
+ *   for every column k < K and token block mb < M/128:
+ *     amax          = max_{m in mb} |x[m, k]|
+ *     st[mb, k]     = scale(amax)
+ *     qt[k, m]      = e4m3( RN_fp32(x[m, k] / st[m/128, k]) )
+ *
+ * i.e. exactly what fp8_quant_act_1x128 writes for x^T.  Optionally (q and s
+ * both non-NULL) the same pass also writes the 1x128 codes and scales of x
+ * itself, as fp8_quant_act_1x128(x) would: one read of x for both layouts.
+ *
+ * x   device, bf16 [M, K] row-major, row pitch ldx (>= K, % 8 == 0)
+ * qt  device, uint8 [K, M] row-major (token-contiguous), row pitch ldqt (>= M, % 16 == 0)
+ * st  device, fp32 [M/128][ldst]: the scale of column k, token block mb is
+ *     st[mb * ldst + k] (ldst >= K, % 4 == 0) -- the layout a GEMM's sA/sB takes
+ * q, s  optional (both NULL, or both set): as fp8_quant_act_1x128 (ldq, lds)
+ * M >= 0 and M % 128 == 0 (pad ragged token counts with zero rows: they add
+ * nothing to dW), M/128 <= 65535; K > 0, K % 128 == 0.  Pointers 16-byte aligned.
+ */
+FP8BS_API fp8_status fp8_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                         uint8_t *qt, int64_t ldqt, float *st, int64_t ldst,
+                                         uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                                         fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
+ * 128x128 weight quantisation written for W^T (the dgrad operand): the
+ * blocks of W^T are W's blocks transposed, with the same scales, so
+ *
+ *   qt[k, n]       = q[n, k]        (q as fp8_quant_weight_128x128 defines it)
+ *   st[kb, nb]     = s[nb, kb]
+ *
+ * Optionally (q and s both non-NULL) W's own codes and scales come from the
+ * same pass, exactly as fp8_quant_weight_128x128 writes them.
+ *
+ * w   device, bf16 [N, K] row-major, row pitch ldw (>= K, % 8 == 0)
+ * qt  device, uint8 [K, N] row-major, row pitch ldqt (>= N, % 16 == 0)
+ * st  device, fp32 [K/128][N/128] row-major, contiguous
+ * q, s  optional: uint8 [N, K] (ldq >= K, % 16 == 0) and fp32 [N/128][K/128]
+ * N, K > 0, both multiples of 128, N/128 <= 65535.  Pointers 16-byte aligned.
+ */
+FP8BS_API fp8_status fp8_quant_weight_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                                uint8_t *q, int64_t ldq, float *s,
+                                                uint8_t *qt, int64_t ldqt, float *st,
+                                                fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM, C = A * B^T ("TN": both operands K-major):
  *
  *   C[m, n] = bf16_RN( sum_kb  sA[kb, m] * sB[n/128, kb] * P[m, n, kb] ),
@@ -162,6 +224,30 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
                                 void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                 uint32_t flags, void *workspace, size_t ws_bytes,
                                 fp8_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with a scale per row of B as well (the wgrad form,
+ * dW = dY^T X with both operands from fp8_quant_act_128x1):
+ *
+ *   C[m, n] = bf16_RN( sum_kb  sA[kb, m] * sB[kb, n] * P[m, n, kb] )
+ *
+ * qa, sa, lda, ldsa, c, ldc, M, N, K, workspace: as fp8_blockscaled_gemm
+ *     (K is the token count here, a multiple of 128).
+ * qb  device, uint8 [N, K], row pitch ldb (>= K, % 16 == 0)
+ * sb  device, fp32 [K/128][ldsb]: the scale of row n of B, K-block kb is
+ *     sb[kb * ldsb + n] (ldsb >= N, % 4 == 0, 16-byte aligned)
+ * flags: FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_AUTO, _PROMOTE or _MX (AUTO:
+ *     MX with FP8_GEMM_SCALES_POW2, else promote); FP8_GEMM_PATH_SKINNY
+ *     returns FP8_ERR_NOT_IMPLEMENTED.  On the promote kernel each K-block's
+ *     partial is multiplied by RN(sA * sB) per element (one more multiply per
+ *     element than the 128x128 form); the MX kernel takes the per-row scales
+ *     as its B scale factors at no extra cost.
+ */
+FP8BS_API fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                                const uint8_t *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                                void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                                uint32_t flags, void *workspace, size_t ws_bytes,
+                                                fp8_stream_t stream);
 
 /*
  * Block-scaled FP8 GEMM with the next layer's activation quantisation fused

@@ -92,3 +92,33 @@ def planted_rows(amaxes: np.ndarray, block: int, per_row_blocks: int, seed: int 
     allb = np.resize(allb, (((allb.shape[0] + per_row_blocks - 1) // per_row_blocks) * per_row_blocks,
                             allb.shape[1]))
     return allb.reshape(-1, per_row_blocks * block).astype(np.float32)
+
+
+def weight_block_rows(w: torch.Tensor, nbs, pow2: bool = False):
+    """Oracle 128x128 quantisation of the 128-row blocks `nbs` of a bf16
+    weight [N, K] (a block row's tiles depend on nothing outside it).
+    Returns (rows, q, s): the weight rows covered, their codes [len(rows), K]
+    and scales [len(nbs), K/128]."""
+    nbs = np.asarray(sorted(set(int(n) for n in nbs)))
+    rows = np.concatenate([np.arange(nb * 128, (nb + 1) * 128) for nb in nbs])
+    q, s = O.quant_weight_128x128(bf16_to_np(w[torch.from_numpy(rows)]), pow2)
+    return rows, q, s
+
+
+def sample_block_rows(N: int, count: int, seed: int):
+    """`count` distinct 128-row blocks of an N-row weight, always including
+    the first and the last."""
+    nb = N // 128
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pick = rng.choice(nb, min(count, nb), replace=False)
+    return np.unique(np.concatenate([pick, [0, nb - 1]]))
+
+
+def weight_block_cols(w: torch.Tensor, kbs, pow2: bool = False):
+    """Oracle 128x128 quantisation of the 128-column blocks `kbs` of a bf16
+    weight [N, K] (a block column's tiles depend on nothing outside it).
+    Returns (cols, q [N, len(cols)], s [N/128, len(kbs)])."""
+    kbs = np.asarray(sorted(set(int(k) for k in kbs)))
+    cols = np.concatenate([np.arange(kb * 128, (kb + 1) * 128) for kb in kbs])
+    q, s = O.quant_weight_128x128(bf16_to_np(w[:, torch.from_numpy(cols)]), pow2)
+    return cols, q, s

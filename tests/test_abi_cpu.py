@@ -129,6 +129,83 @@ def test_gemm_quant_validation(L):
         assert call(flags=0x21) == 6              # MX with pow2 scales
 
 
+def test_quant_act_128x1_validation(L):
+    f = L.fp8_quant_act_128x1
+    ok = dict(x=A16, M=256, K=128, ldx=128, qt=A16b, ldqt=256, st=A16c, ldst=128, q=NULL, ldq=0, s=NULL, lds=0,
+              mode=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["M"], a["K"], a["ldx"], a["qt"], a["ldqt"], a["st"], a["ldst"], a["q"], a["ldq"],
+                 a["s"], a["lds"], a["mode"], NULL)
+
+    assert call(x=NULL) == 1
+    assert call(qt=NULL) == 1
+    assert call(st=NULL) == 1
+    assert call(q=A16) == 1                       # q without s
+    assert call(M=200, ldqt=256) == 2             # M % 128: token blocks are whole
+    assert call(K=200) == 2
+    assert call(ldqt=128) == 2                    # ldqt < M
+    assert call(ldst=64) == 2                     # ldst < K
+    assert call(ldqt=264) == 3
+    assert call(ldst=130) == 3
+    assert call(st=MIS) == 3
+    assert call(q=A16, s=A16, ldq=64, lds=256) == 2   # ldq < K
+    assert call(q=A16, s=A16, ldq=128, lds=200) == 2  # lds < M
+    assert call(q=A16, s=MIS, ldq=128, lds=256) == 3
+    assert call(mode=5) == 4
+    assert call(M=0) == 0
+    if not _has_gpu():
+        assert call() == 6
+        assert call(q=A16, s=A16, ldq=128, lds=256) == 6
+
+
+def test_quant_weight_t_validation(L):
+    f = L.fp8_quant_weight_128x128_t
+    ok = dict(w=A16, N=256, K=128, ldw=128, q=NULL, ldq=0, s=NULL, qt=A16b, ldqt=256, st=A16c, mode=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["w"], a["N"], a["K"], a["ldw"], a["q"], a["ldq"], a["s"], a["qt"], a["ldqt"], a["st"],
+                 a["mode"], NULL)
+
+    assert call(w=NULL) == 1
+    assert call(qt=NULL) == 1
+    assert call(s=A16) == 1                       # s without q
+    assert call(N=0) == 2
+    assert call(N=200) == 2
+    assert call(ldqt=128) == 2                    # ldqt < N
+    assert call(ldqt=272 + 8) == 3
+    assert call(q=A16, s=A16, ldq=64) == 2        # ldq < K
+    assert call(q=A16, s=A16, ldq=136) == 3
+    assert call(mode=9) == 4
+    if not _has_gpu():
+        assert call() == 6
+        assert call(q=A16, s=A16, ldq=128) == 6
+
+
+def test_wgrad_validation(L):
+    f = L.fp8_blockscaled_gemm_wgrad
+    ok = dict(qa=A16, lda=256, sa=A16b, ldsa=256, qb=A16c, ldb=256, sb=A16, ldsb=128, c=A16b, ldc=128, M=256,
+              N=128, K=256, flags=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["qa"], a["lda"], a["sa"], a["ldsa"], a["qb"], a["ldb"], a["sb"], a["ldsb"], a["c"], a["ldc"],
+                 a["M"], a["N"], a["K"], a["flags"], NULL, 0, NULL)
+
+    assert call(sb=NULL) == 1
+    assert call(ldsb=64) == 2                     # ldsb < N
+    assert call(ldsb=130) == 3
+    assert call(K=200) == 2
+    assert call(flags=0x20) == 4                  # MX without the pow2 promise
+    assert call(flags=0x30) == 9                  # no skinny wgrad
+    assert call(M=0) == 0
+    if not _has_gpu():
+        assert call() == 6
+        assert call(flags=0x21) == 6
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0

@@ -10,7 +10,7 @@ import torch
 
 import oracle.fp8_oracle as O
 from fp8_block_scaled_05_gb300 import inputs as I
-from tests.helpers import assert_gemm_close, bf16_to_np
+from tests.helpers import assert_gemm_close, bf16_to_np, sample_block_rows, weight_block_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -148,6 +148,42 @@ def test_gemm_quant_fused(ops, M, N, K, pow2, out_pow2):
     assert np.array_equal(sc[:, :M].cpu().numpy(), s_o.T)
 
 
+@pytest.mark.parametrize("path,out_pow2", [("promote", False), ("promote", True), ("mx", False), ("mx", True)])
+def test_gemm_quant_fused_exact_output(ops, path, out_pow2):
+    """Operands whose product is exact in bf16 (codes decoding to {-1, 0, 1},
+    power-of-two scales shared by both K-blocks): C equals the oracle's C, so
+    the fused codes and scales must equal the oracle quantiser applied to the
+    oracle's C -- no value of the device path enters the expected result."""
+    rng = np.random.Generator(np.random.PCG64(33))
+    M, N, K = 300, 512, 256
+    lut = np.array([0x00, 0x38, 0xB8], np.uint8)
+    qa = lut[rng.integers(0, 3, (M, K))]
+    qw = lut[rng.integers(0, 3, (N, K))]
+    sa = np.repeat(2.0 ** rng.integers(-3, 3, (M, 1)), K // 128, axis=1).astype(np.float32)
+    sw = np.repeat(2.0 ** rng.integers(-2, 2, (N // 128, 1)), K // 128, axis=1).astype(np.float32)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
+    c, qc, sc = ops.gemm_quant(dqa, dsa, dqw, dsw, pow2=True, out_pow2=out_pow2) if path == "mx" else \
+        _gemm_quant_path(ops, dqa, dsa, dqw, dsw, ops.FP8_GEMM_PATH_PROMOTE | ops.FP8_GEMM_SCALES_POW2, out_pow2)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    assert np.array_equal(bf16_to_np(c), ref)
+    q_o, s_o = O.quant_act_1x128(ref.astype(np.float32), out_pow2)
+    assert np.array_equal(qc.cpu().numpy(), q_o)
+    assert np.array_equal(sc[:, :M].cpu().numpy(), s_o.T)
+
+
+def _gemm_quant_path(ops, qa, sa, qw, sw, flags, out_pow2):
+    M, N = qa.shape[0], qw.shape[0]
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    qc = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((N // 128, ops.round_up(M, 4)), dtype=torch.float32, device="cuda")
+    ops.fp8_blockscaled_gemm_quant(qa, sa, qw, sw, c, qc, sc, flags,
+                                   ops.FP8_SCALE_POW2 if out_pow2 else ops.FP8_SCALE_FP32_AMAX,
+                                   ops.workspace_for(M, N, qa.shape[1], 1, qa.device))
+    return c, qc, sc
+
+
 @pytest.mark.parametrize("pow2", [False, True])
 def test_gemm_quant_fused_llama_gate_up_sampled_rows(ops, pow2):
     """Full-size Llama-3.1-8B gate+up GEMM with its output quantised in the
@@ -162,9 +198,10 @@ def test_gemm_quant_fused_llama_gate_up_sampled_rows(ops, pow2):
     assert ops.fp8_last_device_status() == 0
     rows = np.sort(np.random.Generator(np.random.PCG64(23)).choice(case.a.shape[0], 16, replace=False))
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
-    ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
+    wrows, qw_o, sw_o = weight_block_rows(case.w, sample_block_rows(case.w.shape[0], 6, 24), pow2)
+    ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
     c_rows = bf16_to_np(c[rows])
-    assert_gemm_close(c_rows, ref, "gemm_quant llama gate_up")
+    assert_gemm_close(c_rows[:, wrows], ref, "gemm_quant llama gate_up")
     q_o, s_o = O.quant_act_1x128(c_rows, pow2)
     assert np.array_equal(qc[rows].cpu().numpy(), q_o)
     assert np.array_equal(sc[:, rows].cpu().numpy(), s_o.T)
@@ -278,9 +315,12 @@ def test_llama_full_size_sampled_rows(ops, layer, pow2):
     rows = np.sort(np.random.Generator(np.random.PCG64(8)).choice(case.a.shape[0], 24, replace=False))
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
-    qw_o, sw_o = qw.cpu().numpy(), sw.cpu().numpy()
+    nbs = sample_block_rows(case.w.shape[0], 6, 9)
+    wrows, qw_o, sw_o = weight_block_rows(case.w, nbs, pow2)
+    assert np.array_equal(qw[torch.from_numpy(wrows)].cpu().numpy(), qw_o)
+    assert np.array_equal(sw[torch.from_numpy(nbs)].cpu().numpy(), sw_o)
     ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
-    assert_gemm_close(bf16_to_np(y[rows]), ref, f"llama {layer}")
+    assert_gemm_close(bf16_to_np(y[rows])[:, wrows], ref, f"llama {layer}")
 
 
 @pytest.mark.parametrize("layer", ["gate_up", "down", "o_proj"])
@@ -298,8 +338,11 @@ def test_qwen_prefill_full_size_sampled_rows(ops, layer, pow2):
                                      [0, 127, 128, M - 1]]))
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
-    ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
-    assert_gemm_close(bf16_to_np(y[rows]), ref, f"qwen prefill {layer} pow2={pow2}")
+    nbs = sample_block_rows(case.w.shape[0], 6, 12)
+    wrows, qw_o, sw_o = weight_block_rows(case.w, nbs, pow2)
+    assert np.array_equal(qw[torch.from_numpy(wrows)].cpu().numpy(), qw_o)
+    ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
+    assert_gemm_close(bf16_to_np(y[rows])[:, wrows], ref, f"qwen prefill {layer} pow2={pow2}")
 
 
 @pytest.mark.parametrize("M", [1, 8, 32])
@@ -316,18 +359,20 @@ def test_decode_layer_chain(ops, M):
         x = I.normal_bf16(I.stream(90 + i, M), (M, K))
         w = I.normal_bf16(I.stream(95 + i, M), (N, K), std=0.02)
         qw, sw = ops.quant_weight(w.cuda())
-        layers.append((x, qw, sw))
+        layers.append((x, w, qw, sw))
     torch.cuda.synchronize()
     outs = []
-    for x, qw, sw in layers:
+    for x, _, qw, sw in layers:
         qa, sa = ops.quant_act(x.cuda())
         outs.append((ops.gemm(qa, sa, qw, sw), qa, sa))
     torch.cuda.synchronize()
     assert ops.fp8_last_device_status() == 0
-    for (x, qw, sw), (y, qa, sa) in zip(layers, outs):
+    for (x, w, qw, sw), (y, qa, sa) in zip(layers, outs):
         qa_o, sa_o = O.quant_act_1x128(bf16_to_np(x))
         assert np.array_equal(qa.cpu().numpy(), qa_o)
-        ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
+        qw_o, sw_o = O.quant_weight_128x128(bf16_to_np(w), False)
+        assert np.array_equal(qw.cpu().numpy(), qw_o)
+        ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
         assert_gemm_close(bf16_to_np(y), ref, f"decode chain M={M}")
 
 
@@ -339,11 +384,28 @@ def test_decode_full_size(ops, M, K, N):
     torch.cuda.synchronize()
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(case.a))
     assert np.array_equal(qa.cpu().numpy(), qa_o)
-    ref = O.gemm_ref(qa_o, sa_o, qw.cpu().numpy(), sw.cpu().numpy())
-    assert_gemm_close(bf16_to_np(y), ref, f"decode M={M}")
+    wrows, qw_o, sw_o = weight_block_rows(case.w, sample_block_rows(N, 6, M + K), False)
+    assert np.array_equal(qw[torch.from_numpy(wrows)].cpu().numpy(), qw_o)
+    ref = O.gemm_ref(qa_o, sa_o, qw_o, sw_o)
+    assert_gemm_close(bf16_to_np(y)[:, wrows], ref, f"decode M={M}")
 
 
 # ------------------------------------------------------------ grouped
+def _grouped_ref_blocks(qw_dev, w, grp, qa_o, sa_o, N, pow2, seed):
+    """Oracle reference of sampled grouped-GEMM rows (row i in expert grp[i])
+    on a few 128-row blocks of each expert's weight, quantised by the oracle
+    (and checked against the device's codes for those blocks).  Returns the
+    output columns covered and the reference [rows, columns]."""
+    nbs = sample_block_rows(N, 2, seed)
+    ref = []
+    for i, g in enumerate(grp):
+        wrows, q, s = weight_block_rows(w[int(g)], nbs, pow2)
+        if i == 0 or g != grp[i - 1]:
+            assert np.array_equal(qw_dev[int(g)][torch.from_numpy(wrows)].cpu().numpy(), q)
+        ref.append(O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], q, s)[0])
+    return wrows, np.stack(ref)
+
+
 def _grouped_inputs(offsets, N, K, seed, pow2=False):
     G = len(offsets) - 1
     M = int(offsets[-1])
@@ -405,9 +467,8 @@ def test_grouped_moe_full_size_sampled_rows(ops, pow2):
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_gate_up[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
     grp = np.searchsorted(m.offsets, rows, side="right") - 1
-    qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
-    ref = np.stack([O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], qw_n[g], sw_n[g])[0] for i, g in enumerate(grp)])
-    assert_gemm_close(bf16_to_np(c[rows]), ref, "moe gate_up")
+    wrows, ref = _grouped_ref_blocks(qw, w, grp, qa_o, sa_o, N, pow2, seed=10)
+    assert_gemm_close(bf16_to_np(c[rows])[:, wrows], ref, "moe gate_up")
 
 
 @pytest.mark.parametrize("pow2", [False, True])
@@ -436,6 +497,5 @@ def test_grouped_moe_down_full_size_sampled_rows(ops, pow2):
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(m.a_down[rows]), pow2)
     assert np.array_equal(qa[rows].cpu().numpy(), qa_o)
     grp = np.searchsorted(m.offsets, rows, side="right") - 1
-    qw_n, sw_n = qw.cpu().numpy(), sw.cpu().numpy()
-    ref = np.stack([O.gemm_ref(qa_o[i:i + 1], sa_o[i:i + 1], qw_n[g], sw_n[g])[0] for i, g in enumerate(grp)])
-    assert_gemm_close(bf16_to_np(c[rows]), ref, "moe down")
+    wrows, ref = _grouped_ref_blocks(qw, w, grp, qa_o, sa_o, N, pow2, seed=20)
+    assert_gemm_close(bf16_to_np(c[rows])[:, wrows], ref, "moe down")
