@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-pow2", action="store_true", help="skip the power-of-two scale-mode measurement")
     p.add_argument("--no-fused", action="store_true", help="skip the fused GEMM + quantisation measurement")
+    p.add_argument("--no-training", action="store_true", help="skip the training-step (forward + backward) "
+                                                                "measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -496,6 +498,13 @@ def run_ours(args, world, rank, local):
                          "into the GEMM epilogue, with and without writing the bf16 output",
                  "layers": fl}
 
+    # ---------------- a training step of each layer: forward y = x W^T and the
+    # backward GEMMs dX = dY W, dW = dY^T X, every operand from the dual-layout
+    # quantisers (x, W and dY are each read once for both of their layouts).
+    training = None
+    if not args.no_training:
+        training = train_measure(args, layers, ops, stream, dev, flush, fp8_peak, peaks["hbm_gbs"])
+
     st = ops.fp8_last_device_status(stream)
     if st != 0:
         raise SystemExit(f"device status after the timed region: {ops.status_string(st)}")
@@ -527,11 +536,101 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "pow2": pow2,
             "fused_quant": fused,
+            "training": training,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+TRAIN_KERNELS = ("quant_x", "quant_w", "fprop", "quant_dy", "dgrad", "wgrad")
+
+
+def train_measure(args, layers, ops, stream, dev, flush, fp8_peak, hbm_peak):
+    """Times one training step per layer (forward + backward of y = x W^T) in
+    both scale modes, per kernel with CUDA events over flushed steps.
+    Gradients dY: Student-t (nu = 4) x 1e-4, seeded."""
+    import torch
+
+    from fp8_block_scaled_05_gb300 import inputs as I
+    out = {"what": "per layer: dual quantisers of x (1x128 + 128x1), W (W + W^T) and dY (1x128 + 128x1); "
+                   "fprop y = x W^T, dgrad dX = dY W (W^T codes), wgrad dW = dY^T X (1x128 scales on both)",
+           "grad_recipe": "dY ~ Student-t(nu=4) x 1e-4, seeded PCG64", "modes": {}}
+    bufs = []
+    for L in layers:
+        M, N, K = L["M"], L["N"], L["K"]
+        dy = I.student_t_bf16(I.stream(args.seed + 500, N), (M, N), nu=4.0)
+        dy = (dy.float() * 1e-4).to(torch.bfloat16).to(dev)
+        B = dict(dy=dy,
+                 qt_x=torch.empty((K, M), dtype=torch.uint8, device=dev),
+                 st_x=torch.empty((M // 128, ops.round_up(K, 4)), dtype=torch.float32, device=dev),
+                 qt_w=torch.empty((K, N), dtype=torch.uint8, device=dev),
+                 st_w=torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev),
+                 q_dy=torch.empty((M, N), dtype=torch.uint8, device=dev),
+                 s_dy=torch.empty((N // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev),
+                 qt_dy=torch.empty((N, M), dtype=torch.uint8, device=dev),
+                 st_dy=torch.empty((M // 128, ops.round_up(N, 4)), dtype=torch.float32, device=dev),
+                 dx=torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                 dw=torch.empty((N, K), dtype=torch.bfloat16, device=dev),
+                 ws_d=ops.workspace_for(M, K, N, 1, dev), ws_w=ops.workspace_for(N, K, M, 1, dev))
+        bufs.append(B)
+    nk = len(TRAIN_KERNELS)
+
+    def tstep(evs, pow2):
+        mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+        flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
+        for i, (L, B) in enumerate(zip(layers, bufs)):
+            calls = (
+                lambda: ops.fp8_quant_act_128x1(L["a"], B["qt_x"], B["st_x"], L["qa"], L["sa"], mode, stream),
+                lambda: ops.fp8_quant_weight_128x128_t(L["w"], B["qt_w"], B["st_w"], L["qw"], L["sw"], mode, stream),
+                lambda: ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, L["ws"], stream),
+                lambda: ops.fp8_quant_act_128x1(B["dy"], B["qt_dy"], B["st_dy"], B["q_dy"], B["s_dy"], mode, stream),
+                lambda: ops.fp8_blockscaled_gemm(B["q_dy"], B["s_dy"], B["qt_w"], B["st_w"], B["dx"], flags,
+                                                 B["ws_d"], stream),
+                lambda: ops.fp8_blockscaled_gemm_wgrad(B["qt_dy"], B["st_dy"], B["qt_x"], B["st_x"], B["dw"], flags,
+                                                       B["ws_w"], stream),
+            )
+            for j, call in enumerate(calls):
+                if evs is not None:
+                    evs[nk * i + j].record(stream)
+                call()
+        if evs is not None:
+            evs[nk * len(layers)].record(stream)
+
+    flops = sum(6.0 * L["M"] * L["N"] * L["K"] for L in layers)
+    for pow2 in (False, True):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.zero_()
+                tstep(None, pow2)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk * len(layers) + 1)] for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.zero_()
+                tstep(evs[k], pow2)
+        torch.cuda.synchronize(dev)
+        step_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)) / args.steps
+        per = {}
+        for i, L in enumerate(layers):
+            M, N, K = L["M"], L["N"], L["K"]
+            ms = {kn: sum(evs[k][nk * i + j].elapsed_time(evs[k][nk * i + j + 1]) for k in range(args.steps))
+                  / args.steps for j, kn in enumerate(TRAIN_KERNELS)}
+            qbytes = {"quant_x": 4.0 * M * K + 8.0 * M * K / 128, "quant_w": 4.0 * N * K + 8.0 * N * K / 16384,
+                      "quant_dy": 4.0 * M * N + 8.0 * M * N / 128}
+            row = {"ms": ms}
+            for kn, b in qbytes.items():
+                row[kn + "_gbs"] = b / (ms[kn] / 1e3) / 1e9
+                row[kn + "_frac_hbm"] = row[kn + "_gbs"] / hbm_peak
+            for kn in ("fprop", "dgrad", "wgrad"):
+                row[kn + "_tflops"] = 2.0 * M * N * K / (ms[kn] / 1e3) / 1e12
+                row[kn + "_frac_fp8"] = row[kn + "_tflops"] / fp8_peak
+            per[L["name"]] = row
+        out["modes"]["pow2" if pow2 else "fp32"] = {
+            "gemm_kernel": "mx" if pow2 else "promote", "ms_per_step": step_ms,
+            "tflops": flops / (step_ms / 1e3) / 1e12, "layers": per,
+            "gpu_launches": nk * len(layers) * args.steps}
+    return out
 
 
 def main(argv=None):

@@ -63,6 +63,37 @@ __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, i
     }
 }
 
+// 4 x 4 byte transpose: words a, b, c, d are rows (byte 0 = column 0); word
+// j of the result holds column j (byte 0 from a).
+__device__ __forceinline__ void transpose4x4_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                   uint32_t (&o)[4]) {
+    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+    const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+    o[0] = __byte_perm(t0, t2, 0x5410);
+    o[1] = __byte_perm(t0, t2, 0x7632);
+    o[2] = __byte_perm(t1, t3, 0x5410);
+    o[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+// The thread's 8 x 8 codes, given as rows (rc[i]: row i, 8 columns), into
+// the shared tile column by column -- the same placement as
+// col_codes_to_smem, with the codes transposed in registers instead of
+// computed again.
+__device__ __forceinline__ void row_codes_to_smem_transposed(const uint2 (&rc)[8], int rg, int cg,
+                                                             uint8_t *tcodes) {
+    uint32_t lo03[4], hi03[4], lo47[4], hi47[4];
+    transpose4x4_bytes(rc[0].x, rc[1].x, rc[2].x, rc[3].x, lo03);   // columns 0..3, rows 0..3
+    transpose4x4_bytes(rc[4].x, rc[5].x, rc[6].x, rc[7].x, hi03);   // columns 0..3, rows 4..7
+    transpose4x4_bytes(rc[0].y, rc[1].y, rc[2].y, rc[3].y, lo47);   // columns 4..7, rows 0..3
+    transpose4x4_bytes(rc[4].y, rc[5].y, rc[6].y, rc[7].y, hi47);   // columns 4..7, rows 4..7
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int R = 8 * cg + j;
+        const uint2 val = j < 4 ? make_uint2(lo03[j], hi03[j]) : make_uint2(lo47[j - 4], hi47[j - 4]);
+        *reinterpret_cast<uint2 *>(tcodes + R * kTT + ((((rg >> 1) ^ (cg & 7))) << 4) + ((rg & 1) << 3)) = val;
+    }
+}
+
 // The shared tile (after a barrier) to out[(row0 + R) * ldo + col0 + ...]:
 // warp w stores tile rows 16 w .. 16 w + 15, four rows per instruction.
 __device__ __forceinline__ void store_transposed(const uint8_t *tcodes, uint8_t *out, int64_t ldo, int64_t row0,
@@ -82,7 +113,7 @@ __device__ __forceinline__ void store_transposed(const uint8_t *tcodes, uint8_t 
 // codes q[m][k] and scales s[kb * lds + m] of the same tile.
 // ---------------------------------------------------------------------------
 template <bool ROWWISE>
-__global__ void __launch_bounds__(256) k_quant_act_128x1(const uint16_t *__restrict__ x, int64_t ldx,
+__global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const uint16_t *__restrict__ x, int64_t ldx,
                                                          uint8_t *__restrict__ qt, int64_t ldqt,
                                                          float *__restrict__ st, int64_t ldst,
                                                          uint8_t *__restrict__ q, int64_t ldq,
@@ -194,12 +225,16 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128_t(const uint16_t *__res
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
     const BlockScale bs = make_scale(amax, pow2 != 0);
 
+    // One scale for the whole tile: W's codes and W^T's are the same bytes,
+    // computed once and transposed in registers.
+    uint2 rc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rc[i] = quant8(v[i], bs);
     if (q != nullptr) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            __stcs(reinterpret_cast<uint2 *>(q + (n0 + 8 * rg + i) * ldq + k0 + 8 * cg), quant8(v[i], bs));
+        for (int i = 0; i < 8; ++i) __stcs(reinterpret_cast<uint2 *>(q + (n0 + 8 * rg + i) * ldq + k0 + 8 * cg), rc[i]);
     }
-    col_codes_to_smem(v, rg, cg, tcodes, [&](int) { return bs; });
+    row_codes_to_smem_transposed(rc, rg, cg, tcodes);
     __syncthreads();
     store_transposed(tcodes, qt, ldqt, k0, n0, warp, lane);
     if (threadIdx.x == 0) {

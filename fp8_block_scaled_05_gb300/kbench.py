@@ -24,7 +24,9 @@ from . import ops
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("--kernel", required=True, choices=["quant_act", "quant_weight", "gemm", "grouped"])
+    p.add_argument("--kernel", required=True,
+                   choices=["quant_act", "quant_weight", "gemm", "grouped", "quant_act_t", "quant_weight_t", "wgrad"])
+    p.add_argument("--dual", action="store_true", help="quant_act_t / quant_weight_t: also the other layout")
     p.add_argument("--M", type=int, default=4096)
     p.add_argument("--N", type=int, default=4096)
     p.add_argument("--K", type=int, default=4096)
@@ -57,6 +59,30 @@ def main(argv=None):
         s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
         run = lambda: ops.fp8_quant_weight_128x128(w, q, s, mode)  # noqa: E731
         work, unit = 3.0 * N * K + 4.0 * (N // 128) * (K // 128), "GB/s"
+    elif a.kernel == "quant_act_t":
+        # x [M, K] -> 128x1 codes transposed (+ 1x128 codes with --dual)
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        qt = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        st = torch.empty((M // 128, ops.round_up(K, 4)), dtype=torch.float32, device=dev)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev) if a.dual else None
+        s = torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev) if a.dual else None
+        run = lambda: ops.fp8_quant_act_128x1(x, qt, st, q, s, mode)  # noqa: E731
+        work, unit = (4.0 if a.dual else 3.0) * M * K + (8.0 if a.dual else 4.0) * M * K / 128, "GB/s"
+    elif a.kernel == "quant_weight_t":
+        w = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        qt = torch.empty((K, N), dtype=torch.uint8, device=dev)
+        st = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev)
+        q = torch.empty((N, K), dtype=torch.uint8, device=dev) if a.dual else None
+        s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev) if a.dual else None
+        run = lambda: ops.fp8_quant_weight_128x128_t(w, qt, st, q, s, mode)  # noqa: E731
+        work, unit = (4.0 if a.dual else 3.0) * N * K, "GB/s"
+    elif a.kernel == "wgrad":
+        # C [M, N] = A [M, K] B [N, K]^T with 1x128 scales on both (K = tokens)
+        qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
+        qb, sb = ops.quant_act(torch.randn((N, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda: ops.wgrad(qa, sa, qb, sb, a.pow2, a.path, out=c)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
     elif a.kernel == "gemm":
         qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
         qw, sw = ops.quant_weight((torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16), a.pow2)
