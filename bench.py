@@ -10,7 +10,8 @@ block-scaled FP8 GEMM, all in libfp8bs.so's kernels, fp32 amax/448 scales.
 metric: quant+GEMM TFLOP/s = sum(2 M N K) / (t_quantA + t_quantW + t_gemm).
 
 Timing: W untimed warm-up steps, then exactly K steps, each preceded (outside
-its CUDA-event interval) by a 256 MB write that flushes the 129 MB L2;
+its CUDA-event interval) by a 256 MB write that flushes the 129 MB L2 and
+a 256 MB read that leaves it holding clean lines;
 barrier + synchronize around the timed region; max over ranks.  N > 1 runs
 independent replicas (the path has no exchange step): value is the work of
 all ranks divided by the slowest rank's time.
@@ -279,7 +280,8 @@ def run_ours(args, world, rank, local):
                  ws=ops.workspace_for(M, N, K, 1, dev))
         layers.append(L)
     flops_step = sum(2.0 * L["M"] * L["N"] * L["K"] for L in layers)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    from fp8_block_scaled_05_gb300.timing import L2Flush
+    flush = L2Flush(dev, L2_FLUSH_BYTES)
     launches_per_step = 3 * len(layers)
 
     def step(events=None, pow2=False):
@@ -303,7 +305,7 @@ def run_ours(args, world, rank, local):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * len(layers) + 1)] for _ in range(steps)]
         with torch.cuda.stream(stream):
             for k in range(steps):
-                flush.zero_()
+                flush()
                 step(evs[k], pow2)
         torch.cuda.synchronize(dev)
         step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps)]
@@ -316,7 +318,7 @@ def run_ours(args, world, rank, local):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             step()
     torch.cuda.synchronize(dev)
     st = ops.fp8_last_device_status(stream)
@@ -430,7 +432,7 @@ def run_ours(args, world, rank, local):
     if not args.no_pow2:
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
-                flush.zero_()
+                flush()
                 step(None, True)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -479,13 +481,13 @@ def run_ours(args, world, rank, local):
             for name, fn in (("unfused_ms", unfused), ("fused_ms", fused_c), ("fused_no_c_ms", fused_noc)):
                 with torch.cuda.stream(stream):
                     for _ in range(args.warmup):
-                        flush.zero_()
+                        flush()
                         fn()
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(args.steps)]
                 with torch.cuda.stream(stream):
                     for e0, e1 in evs:
-                        flush.zero_()
+                        flush()
                         e0.record(stream)
                         fn()
                         e1.record(stream)
@@ -524,7 +526,8 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded numpy PCG64: A ~ N(0,1) with 1% outlier channels x30, W ~ N(0,0.02))",
             "config": {"workload": WORKLOAD, "M": 4096, "scale": "fp32 amax/448",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed before every timed step (256 MB write outside the step's events)"},
+                       "l2": "flushed before every timed step (256 MB write, then a 256 MB read of a second buffer so the "
+                             "lines left are clean; outside the step's events)"},
             "roofline": {"bound": "tensor", "kernel": f"gemm.{dom}", "achieved": achieved, "peak": fp8_peak,
                          "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
                          "peak_source": f"{peaks['source']}: bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_OVER_BF16} "
@@ -602,12 +605,12 @@ def train_measure(args, layers, ops, stream, dev, flush, fp8_peak, hbm_peak):
     for pow2 in (False, True):
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
-                flush.zero_()
+                flush()
                 tstep(None, pow2)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk * len(layers) + 1)] for _ in range(args.steps)]
         with torch.cuda.stream(stream):
             for k in range(args.steps):
-                flush.zero_()
+                flush()
                 tstep(evs[k], pow2)
         torch.cuda.synchronize(dev)
         step_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)) / args.steps

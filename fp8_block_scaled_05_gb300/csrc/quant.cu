@@ -38,7 +38,7 @@ constexpr int kActPairs = kActKB / 2;
 constexpr int kActItems = kActRowsPerWarp * kActPairs;   // blocks per half-warp
 static_assert(kActItems <= 16 && (kActItems & (kActItems - 1)) == 0, "items per half-warp");
 
-__global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
+__global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
                                                          int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int64_t lds, int pow2) {
     __shared__ float s_tile[kActKB][kActRows];
@@ -126,7 +126,7 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 // 16w..16w+15, one warp-wide load covering two rows (half-warp each).  Each
 // lane keeps its 64 values in registers across the CTA-wide amax reduction.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
+__global__ void __launch_bounds__(256, 4) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
                                                          uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int pow2) {
     __shared__ float s_red[8];

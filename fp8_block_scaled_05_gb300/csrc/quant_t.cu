@@ -51,11 +51,15 @@ __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, i
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const BlockScale bs = scale_of(j);
-        uint32_t part[2] = {0u, 0u};
+        uint32_t part[2] = {0u, 0u}, miss = 0u;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {   // rows 2p (low byte) and 2p + 1
-            const uint32_t pair = quant_pair(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs);
-            part[p >> 1] |= pair << (16 * (p & 1));
+        for (int p = 0; p < 4; ++p)   // rows 2p (low byte) and 2p + 1
+            part[p >> 1] |= quant_pair_fast(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs, miss) << (16 * (p & 1));
+        if (miss != 0u) {             // rare: redo the column's pairs exactly
+            part[0] = part[1] = 0u;
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                part[p >> 1] |= quant_pair(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs) << (16 * (p & 1));
         }
         const int R = 8 * cg + j;
         *reinterpret_cast<uint2 *>(tcodes + R * kTT + ((((rg >> 1) ^ (cg & 7))) << 4) + ((rg & 1) << 3)) =
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
 // qt[k][n] and scales st[kb * NB + nb]; with q != nullptr also W's codes
 // q[n][k] and scales s[nb * KB + kb].
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_w_128x128_t(const uint16_t *__restrict__ w, int64_t ldw, int64_t KB,
+__global__ void __launch_bounds__(256, 4) k_quant_w_128x128_t(const uint16_t *__restrict__ w, int64_t ldw, int64_t KB,
                                                            int64_t NB, uint8_t *__restrict__ q, int64_t ldq,
                                                            float *__restrict__ s, uint8_t *__restrict__ qt,
                                                            int64_t ldqt, float *__restrict__ st, int pow2) {

@@ -20,6 +20,7 @@ import torch
 
 from . import build as _build
 from . import ops
+from .timing import L2Flush
 
 
 def main(argv=None):
@@ -45,7 +46,7 @@ def main(argv=None):
     g.manual_seed(0)
     M, N, K = a.M, a.N, a.K
     mode = ops.FP8_SCALE_POW2 if a.pow2 else ops.FP8_SCALE_FP32_AMAX
-    flush = None if a.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = None if a.no_flush else L2Flush(dev)
 
     if a.kernel == "quant_act":
         x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
@@ -124,7 +125,7 @@ def main(argv=None):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.iters)]
     for e0, e1 in evs:
         if flush is not None:
-            flush.zero_()
+            flush()
         e0.record()
         timed()
         e1.record()
