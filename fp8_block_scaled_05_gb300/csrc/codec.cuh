@@ -139,27 +139,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)r;
 }
 
-// Both elements of a pair times one factor, as one packed multiply (each
-// lane an IEEE mul.rn.f32, so the products equal two scalar multiplies).
-__device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float &pb) {
-    uint64_t x, k;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(k) : "f"(f));
-    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(k));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(x));
-}
-
-// The corrected quotients of a pair, out of line: taken for a few pairs in
-// a million, so the unrolled quantisation loops keep only the fast path and
-// stay small in the instruction cache.
-static __device__ __noinline__ uint32_t quant_pair_exact(float xa, float xb, float s, float r, int mode) {
-    BlockScale bs;
-    bs.s = s;
-    bs.r = r;
-    bs.mode = mode;
-    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
-}
-
 // Codes of two elements, e4m3(RN(x/s)) each.
 //
 // Fast path for mode 0: q0 = RN(x r) is within 1.5 ulp of x/s, so the
@@ -170,51 +149,46 @@ static __device__ __noinline__ uint32_t quant_pair_exact(float xa, float xb, flo
 // pairs whose interval contains an E4M3 rounding boundary (a few in a
 // million) take the two-step corrected quotient.
 __device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
-    float qa, qb;
-    if (bs.mode == 1) {
-        mul2(xa, xb, bs.r, qa, qb);
-        return e4m3x2(qa, qb);
-    }
+    if (bs.mode == 1) return e4m3x2(xa * bs.r, xb * bs.r);
     if (bs.mode == 0) {
+        const float qa = xa * bs.r, qb = xb * bs.r;
         constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
-        float la, lb, ha, hb;
-        mul2(xa, xb, bs.r, qa, qb);
-        mul2(qa, qb, kLo, la, lb);
-        mul2(qa, qb, kHi, ha, hb);
-        const uint32_t lo = e4m3x2(la, lb), hi = e4m3x2(ha, hb);
+        const uint32_t lo = e4m3x2(qa * kLo, qb * kLo), hi = e4m3x2(qa * kHi, qb * kHi);
         if (lo == hi) return lo;
     }
-    return quant_pair_exact(xa, xb, bs.s, bs.r, bs.mode);
+    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
 }
 
-// The fast path of quant_pair without its branch: returns the codes of the
-// lower interval end and ORs into `miss` the bits where the two ends differ
-// (mode 2 always misses), so a caller can check several pairs at once and
-// take the exact path only when some pair missed.
-__device__ __forceinline__ uint32_t quant_pair_fast(float xa, float xb, const BlockScale &bs, uint32_t &miss) {
-    float qa, qb;
-    mul2(xa, xb, bs.r, qa, qb);
-    if (bs.mode == 1) return e4m3x2(qa, qb);
-    constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
-    float la, lb, ha, hb;
-    mul2(qa, qb, kLo, la, lb);
-    mul2(qa, qb, kHi, ha, hb);
-    const uint32_t lo = e4m3x2(la, lb), hi = e4m3x2(ha, hb);
-    miss |= (lo ^ hi) | (bs.mode == 2 ? 1u : 0u);
-    return lo;
+// Both elements of a pair times one factor, as one packed multiply (each
+// lane an IEEE mul.rn.f32, so the products equal two scalar multiplies).
+__device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float &pb) {
+    uint64_t x, k;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(k) : "f"(f));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(k));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(x));
 }
 
-// Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes):
-// the four pairs take the fast path, and only if one of them missed are all
-// four redone exactly.
+// Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes).
 __device__ __forceinline__ uint2 quant8(const uint4 &v, const BlockScale &bs) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t p[4], miss = 0u;
+    uint32_t p[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) p[i] = quant_pair_fast(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), bs, miss);
-    if (miss != 0u) {
+    for (int i = 0; i < 4; ++i) p[i] = quant_pair(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), bs);
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// quant8 for a power-of-two scale (r = 2^-e exactly): x * r is x / s with no
+// rounding, so no check is needed; both elements of a pair in one packed
+// multiply.
+__device__ __forceinline__ uint2 quant8_pow2(const uint4 &v, float r) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t p[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = quant_pair(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), bs);
+    for (int i = 0; i < 4; ++i) {
+        float qa, qb;
+        mul2(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), r, qa, qb);
+        p[i] = e4m3x2(qa, qb);
     }
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }

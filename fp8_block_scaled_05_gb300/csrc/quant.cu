@@ -38,9 +38,11 @@ constexpr int kActPairs = kActKB / 2;
 constexpr int kActItems = kActRowsPerWarp * kActPairs;   // blocks per half-warp
 static_assert(kActItems <= 16 && (kActItems & (kActItems - 1)) == 0, "items per half-warp");
 
+// POW2: power-of-two scales, cast by an exact multiply (no division, no check).
+template <bool POW2>
 __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
-                                                         int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
-                                                         float* __restrict__ s, int64_t lds, int pow2) {
+                                                            int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
+                                                            float* __restrict__ s, int64_t lds) {
     __shared__ float s_tile[kActKB][kActRows];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const int64_t m0 = (int64_t)blockIdx.x * kActRows;
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __re
         }
     }
     // this lane's block: item (l16 mod kActItems) of half `half`
-    const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), pow2 != 0);
+    const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
     if (l16 < kActItems) {
         const int r = l16 / kActPairs, p = l16 % kActPairs;
         const int rl = warp * kActRowsPerWarp + r;
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __re
         const int64_t m = m0 + warp * kActRowsPerWarp + r;
         const int64_t kb = kb0 + 2 * p + half;
         if (m < M && kb < KB) {
-            const uint2 c = quant8(v[i], scale_from_sr(si, ri, pow2 != 0));
+            const uint2 c = POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false));
             __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8), c);
         }
     }
@@ -113,11 +115,10 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
     if (M == 0) return cudaSuccess;
     const int64_t KB = K / 128;
     dim3 grid((unsigned)((M + kActRows - 1) / kActRows), (unsigned)((KB + kActKB - 1) / kActKB));
+    auto kern = pow2 ? k_quant_act_1x128<true> : k_quant_act_1x128<false>;
     if (pdl_for_tokens(M))   // a decode step: overlap with the kernels around it
-        return launch_pdl(k_quant_act_1x128, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x), M, KB, ldx, q,
-                          ldq, s, lds, pow2 ? 1 : 0);
-    k_quant_act_1x128<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds,
-                                            pow2 ? 1 : 0);
+        return launch_pdl(kern, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds);
+    kern<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds);
     return cudaGetLastError();
 }
 
@@ -126,7 +127,7 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 // 16w..16w+15, one warp-wide load covering two rows (half-warp each).  Each
 // lane keeps its 64 values in registers across the CTA-wide amax reduction.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256, 4) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
+__global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
                                                          uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int pow2) {
     __shared__ float s_red[8];

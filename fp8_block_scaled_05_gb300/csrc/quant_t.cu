@@ -44,22 +44,26 @@ __device__ __forceinline__ float elem(const uint4 (&v)[8], int i, int j) {
 }
 
 // Codes of the thread's 8 columns (8 rows each) into the shared tile;
-// scale_of(j) gives column j's BlockScale.
-template <typename ScaleOf>
+// scale_of(j) gives column j's BlockScale (POW2: power-of-two scales, an
+// exact multiply).
+template <bool POW2, typename ScaleOf>
 __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
                                                   ScaleOf scale_of) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const BlockScale bs = scale_of(j);
-        uint32_t part[2] = {0u, 0u}, miss = 0u;
+        uint32_t part[2] = {0u, 0u};
 #pragma unroll
-        for (int p = 0; p < 4; ++p)   // rows 2p (low byte) and 2p + 1
-            part[p >> 1] |= quant_pair_fast(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs, miss) << (16 * (p & 1));
-        if (miss != 0u) {             // rare: redo the column's pairs exactly
-            part[0] = part[1] = 0u;
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                part[p >> 1] |= quant_pair(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs) << (16 * (p & 1));
+        for (int p = 0; p < 4; ++p) {   // rows 2p (low byte) and 2p + 1
+            uint32_t pair;
+            if constexpr (POW2) {
+                float qa, qb;
+                mul2(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs.r, qa, qb);
+                pair = e4m3x2(qa, qb);
+            } else {
+                pair = quant_pair(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs);
+            }
+            part[p >> 1] |= pair << (16 * (p & 1));
         }
         const int R = 8 * cg + j;
         *reinterpret_cast<uint2 *>(tcodes + R * kTT + ((((rg >> 1) ^ (cg & 7))) << 4) + ((rg & 1) << 3)) =
@@ -116,12 +120,12 @@ __device__ __forceinline__ void store_transposed(const uint8_t *tcodes, uint8_t 
 // codes qt[k][m] and scales st[mb * ldst + k]; with ROWWISE also the 1x128
 // codes q[m][k] and scales s[kb * lds + m] of the same tile.
 // ---------------------------------------------------------------------------
-template <bool ROWWISE>
+template <bool ROWWISE, bool POW2>
 __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const uint16_t *__restrict__ x, int64_t ldx,
                                                          uint8_t *__restrict__ qt, int64_t ldqt,
                                                          float *__restrict__ st, int64_t ldst,
                                                          uint8_t *__restrict__ q, int64_t ldq,
-                                                         float *__restrict__ s, int64_t lds, int pow2) {
+                                                         float *__restrict__ s, int64_t lds) {
     __shared__ __align__(16) uint8_t tcodes[kTT * kTT];
     __shared__ __align__(16) uint32_t colpart[8][16][4];   // per warp: packed |bf16| maxima of column pairs
     __shared__ float2 colscale[kTT];
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
                 a[j] = max_u16x2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
             }
         }
-        const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), pow2 != 0);
+        const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
         if (cg < 8) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
             const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
             const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
             __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
-                   quant8(v[i], scale_from_sr(si, ri, pow2 != 0)));
+                   POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
         }
     }
     __syncthreads();
@@ -184,14 +188,14 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
 #pragma unroll
         for (int w = 0; w < 8; ++w) m2 = max_u16x2(m2, colpart[w][c >> 3][(c & 7) >> 1]);
         const uint32_t bits = (c & 1) ? (m2 >> 16) : (m2 & 0xFFFFu);
-        const BlockScale bs = make_scale(__uint_as_float(bits << 16), pow2 != 0);
+        const BlockScale bs = make_scale(__uint_as_float(bits << 16), POW2);
         colscale[c] = make_float2(bs.s, bs.r);
         st[(size_t)blockIdx.y * ldst + k0 + c] = bs.s;
     }
     __syncthreads();
-    col_codes_to_smem(v, rg, cg, tcodes, [&](int j) {
+    col_codes_to_smem<POW2>(v, rg, cg, tcodes, [&](int j) {
         const float2 sr = colscale[8 * cg + j];
-        return scale_from_sr(sr.x, sr.y, pow2 != 0);
+        return scale_from_sr(sr.x, sr.y, POW2);
     });
     __syncthreads();
     store_transposed(tcodes, qt, ldqt, k0, m0, warp, lane);
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
 // qt[k][n] and scales st[kb * NB + nb]; with q != nullptr also W's codes
 // q[n][k] and scales s[nb * KB + kb].
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256, 4) k_quant_w_128x128_t(const uint16_t *__restrict__ w, int64_t ldw, int64_t KB,
+__global__ void __launch_bounds__(256) k_quant_w_128x128_t(const uint16_t *__restrict__ w, int64_t ldw, int64_t KB,
                                                            int64_t NB, uint8_t *__restrict__ q, int64_t ldq,
                                                            float *__restrict__ s, uint8_t *__restrict__ qt,
                                                            int64_t ldqt, float *__restrict__ st, int pow2) {
@@ -253,11 +257,9 @@ cudaError_t launch_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t 
     if (M == 0) return cudaSuccess;
     const dim3 grid((unsigned)(K / kTT), (unsigned)(M / kTT));
     const uint16_t *xp = static_cast<const uint16_t *>(x);
-    if (q != nullptr)
-        k_quant_act_128x1<true><<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds, pow2 ? 1 : 0);
-    else
-        k_quant_act_128x1<false><<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, nullptr, 0, nullptr, 0,
-                                                           pow2 ? 1 : 0);
+    auto kern = q != nullptr ? (pow2 ? k_quant_act_128x1<true, true> : k_quant_act_128x1<true, false>)
+                             : (pow2 ? k_quant_act_128x1<false, true> : k_quant_act_128x1<false, false>);
+    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds);
     return cudaGetLastError();
 }
 
