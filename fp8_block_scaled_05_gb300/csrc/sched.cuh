@@ -16,8 +16,12 @@ __device__ __forceinline__ void group_rows(const int32_t* __restrict__ offsets, 
     hi = min(max(offsets[g + 1], lo), M);
 }
 
-// Tile t -> coordinates.  Dense: m-tiles vary fastest so that CTAs running at
-// the same time share the weight tile.  Grouped: tiles of expert g follow
+// Tile t -> coordinates.  Dense: the operand that is re-read once per tile
+// column (or row) of the other is the smaller one, so that it stays in L2:
+// with M <= N m-tiles vary fastest (CTAs running at the same time share the
+// B tile, and A is re-read per column of tiles); with M > N (e.g. a weight
+// gradient, M = out-features, N = in-features) n-tiles vary fastest and B is
+// the one re-read.  Grouped: tiles of expert g follow
 // those of expert g-1; inside an expert, m-tiles vary fastest.  cum[g] is the
 // number of tiles of experts before g (shared memory, from
 // build_group_table).
@@ -26,8 +30,16 @@ __device__ __forceinline__ Tile decode_tile(int t, int M, int N, const int32_t* 
                                             const int32_t* __restrict__ offsets, int G) {
     Tile r;
     if (!GROUPED) {
-        const int MT = (M + BM - 1) / BM;
-        const int mt = t % MT, nt = t / MT;
+        int mt, nt;
+        if (M > N) {
+            const int NT = (N + BN - 1) / BN;
+            mt = t / NT;
+            nt = t % NT;
+        } else {
+            const int MT = (M + BM - 1) / BM;
+            mt = t % MT;
+            nt = t / MT;
+        }
         r.m0 = mt * BM;
         r.row_end = M;
         r.brow = nt * BN;
