@@ -33,7 +33,8 @@ round-to-nearest-even and saturation at +-448; the power-of-two scale is
 reference is dequantise-then-multiply in fp64.
 
 Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
-and (training-side functions) tests/test_oracle_pins_training.py against
+and (training-side functions) tests/test_oracle_pins_training.py, (per-tensor
+scaling) tests/test_oracle_pins_per_tensor.py against
 facts that do not come from this file (the OCP code table, library
 casts, exact rational arithmetic, brute force, PyTorch autograd and closed
 forms).
@@ -55,6 +56,7 @@ __all__ = [
     "gemm_ref", "gemm_ref_rows", "grouped_gemm_ref",
     "block_amax_col", "quant_act_128x1", "quant_weight_128x128_t",
     "dgrad_ref", "wgrad_ref", "wgrad_ref_rows",
+    "quant_per_tensor", "gemm_per_tensor_ref",
 ]
 
 
@@ -337,3 +339,30 @@ def wgrad_ref_rows(qt_dy, st_dy, qt_x, st_x, rows) -> np.ndarray:
     """wgrad_ref restricted to the given output rows n (for sampled checks)."""
     rows = np.asarray(rows)
     return dequant_act(qt_dy[rows], st_dy[rows]) @ dequant_act(qt_x, st_x).T
+
+
+# --------------------------------------------------------------------------
+# Per-tensor dynamic scaling
+#
+# One scale for the whole tensor, recomputed from the tensor's current amax
+# so that every value fits the FP8 range (page "エンドツーエンドFP8精度で実現
+# する高スループット強化学習トレーニング", ai.warp-studio.com,
+# §FP8強化学習における精度と安定性の確保: dynamic scaling factors per tensor).
+# The scale rule and the cast are the block quantisers' (amax/448 rounded to
+# fp32, or the power of two), applied to a single block that is the tensor.
+# --------------------------------------------------------------------------
+def quant_per_tensor(x: np.ndarray, pow2: bool = False):
+    """Per-tensor quantisation of a float32 matrix (bf16 values).
+
+    Returns (q uint8 of x's shape, s float32 scalar): s from max |x| over the
+    whole tensor, q = e4m3(x / s).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    s = scale_from_amax(np.array([amax], np.float32), pow2)[0]
+    return _cast(x, np.full(x.shape, s, np.float32)), np.float32(s)
+
+
+def gemm_per_tensor_ref(qa, sa, qb, sb) -> np.ndarray:
+    """C = sA * sB * (dec(qa) @ dec(qb)^T) in float64, one scale per operand."""
+    return (e4m3_decode(qa) @ e4m3_decode(qb).T) * (np.float64(np.float32(sa)) * np.float64(np.float32(sb)))
