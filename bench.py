@@ -58,6 +58,7 @@ def parse_args(argv=None):
     p.add_argument("--no-fused", action="store_true", help="skip the fused GEMM + quantisation measurement")
     p.add_argument("--no-training", action="store_true", help="skip the training-step (forward + backward) "
                                                                 "measurement")
+    p.add_argument("--no-per-tensor", action="store_true", help="skip the per-tensor scaling measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -500,6 +501,13 @@ def run_ours(args, world, rank, local):
                          "into the GEMM epilogue, with and without writing the bf16 output",
                  "layers": fl}
 
+    # ---------------- the same step with per-tensor dynamic scaling: one amax
+    # per tensor (two passes: reduction, then cast) and the GEMM with one scale
+    # per operand (MX kernel, unit scale factors, scale product in the epilogue).
+    per_tensor = None
+    if not args.no_per_tensor:
+        per_tensor = per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_peak)
+
     # ---------------- a training step of each layer: forward y = x W^T and the
     # backward GEMMs dX = dY W, dW = dY^T X, every operand from the dual-layout
     # quantisers (x, W and dY are each read once for both of their layouts).
@@ -540,11 +548,60 @@ def run_ours(args, world, rank, local):
             "pow2": pow2,
             "fused_quant": fused,
             "training": training,
+            "per_tensor": per_tensor,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_peak):
+    """The bench step with per-tensor scaling, timed per call with CUDA events
+    over flushed steps (same inputs and shapes as the block-scaled step)."""
+    import torch
+
+    bufs = [dict(sa=torch.empty(2, dtype=torch.float32, device=dev), sw=torch.empty(2, dtype=torch.float32, device=dev))
+            for _ in layers]
+    names = ("quant_act", "quant_weight", "gemm")
+
+    def pstep(evs):
+        for i, (L, B) in enumerate(zip(layers, bufs)):
+            calls = (lambda: ops.fp8_quant_per_tensor(L["a"], L["qa"], B["sa"], 0, stream),
+                     lambda: ops.fp8_quant_per_tensor(L["w"], L["qw"], B["sw"], 0, stream),
+                     lambda: ops.fp8_tensorscaled_gemm(L["qa"], B["sa"][:1], L["qw"], B["sw"][:1], L["c"], 0, L["ws"],
+                                                       stream))
+            for j, call in enumerate(calls):
+                if evs is not None:
+                    evs[3 * i + j].record(stream)
+                call()
+        if evs is not None:
+            evs[3 * len(layers)].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush()
+            pstep(None)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * len(layers) + 1)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush()
+            pstep(evs[k])
+    torch.cuda.synchronize(dev)
+    total = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps))
+    kern, gemm_ms = {}, 0.0
+    for i, L in enumerate(layers):
+        for j, kn in enumerate(names):
+            ms = sum(evs[k][3 * i + j].elapsed_time(evs[k][3 * i + j + 1]) for k in range(args.steps)) / args.steps
+            kern[f"{L['name']}.{kn}"] = ms
+            if kn == "gemm":
+                gemm_ms += ms
+    return {"scale": "one fp32 amax/448 per tensor (two passes: amax reduction, then cast)",
+            "gemm_path": "mx (unit scale factors, scale product in the epilogue)",
+            "value": flops_step * args.steps / (total / 1e3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": total / args.steps, "gemm_only_tflops": flops_step / (gemm_ms / 1e3) / 1e12,
+            "gemm_frac_fp8": flops_step / (gemm_ms / 1e3) / 1e12 / fp8_peak, "kernels_ms": kern,
+            "gpu_launches": 5 * len(layers) * args.steps}
 
 
 TRAIN_KERNELS = ("quant_x", "quant_w", "fprop", "quant_dy", "dgrad", "wgrad")

@@ -276,6 +276,21 @@ fp8_status fp8_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64
                                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_quant_per_tensor(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                float* scale_amax, fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (M < 0 || K <= 0 || (K % 8) || M > (1ll << 40) || K > (1ll << 40)) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x || !q || !scale_amax) return FP8_ERR_NULL;
+    if (ldx < K || ldq < K) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldq % 16) || !aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scale_amax) % 8))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_per_tensor(x, M, K, ldx, q, ldq, scale_amax, mode == FP8_SCALE_POW2, d->sm_count,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t* splits) {
     const uint32_t path = plan_path(M, K, flags);
     int32_t sp = 1;
@@ -407,6 +422,53 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
         return e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
+}
+
+fp8_status fp8_tensorscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, const uint8_t* qb, int64_t ldb,
+                                 const float* sb, void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 uint32_t flags, void* workspace, size_t ws_bytes, fp8_stream_t stream) {
+    // the block-scaled validation with the one-scale pointers standing in for
+    // the scale arrays (ldsa = M keeps its pitch rule satisfied)
+    if (fp8_status e = check_gemm_common(qa, lda, sa, M > 0 ? ((M + 3) / 4) * 4 : 0, qb, sb, c, ldc, M, N, K,
+                                         flags | FP8_GEMM_SCALES_POW2))
+        return e;
+    const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
+    if (forced == FP8_GEMM_PATH_PROMOTE || forced == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    if (M == 0) return FP8_OK;
+    if (ldb < K) return FP8_ERR_SHAPE;
+    if (ldb % 16) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+
+    GemmArgs a{};
+    a.per_tensor = 1;
+    a.sa = sa;
+    a.sb = sb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.offsets = nullptr;
+    a.G = 1;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = 1;
+    a.bn = kMxTileN;
+    if (workspace && aligned16(workspace)) {
+        a.workspace = workspace;
+        a.ws_bytes = ws_bytes;
+    }
+    if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+        return e;
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+        return e;
+    return cuda_status(launch_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fp8_status fp8_blockscaled_gemm_quant(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa, const uint8_t* qb,

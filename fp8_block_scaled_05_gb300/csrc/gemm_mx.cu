@@ -133,7 +133,11 @@ __device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
     return ok ? e : 127u;
 }
 
-template <bool GROUPED>
+// PER_TENSOR: sa and sb each point at one fp32 scale for the whole operand
+// (per-tensor scaling).  The scale factors are then 2^0 (the block-scaled MMA
+// is a plain FP8 MMA with fp32 accumulation over all of K) and the epilogue
+// multiplies by RN(sa * sb) once.
+template <bool GROUPED, bool PER_TENSOR = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
@@ -292,9 +296,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < KB_PER_SF; ++j) {
                     const int kb = kb0 + j;
-                    fa[j] = (kb < w.kb1 && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
-                    fb0[j] = (kb < w.kb1 && ldsb == 0) ? sb0[kb] : 1.0f;
-                    fb1[j] = (kb < w.kb1 && ldsb == 0 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
+                    fa[j] = (!PER_TENSOR && kb < w.kb1 && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
+                    fb0[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0) ? sb0[kb] : 1.0f;
+                    fb1[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
                 }
                 uint32_t wa = 0, wb0 = 0, wb1 = 0;
 #pragma unroll
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // B scale-factor column j holds rows n0 + 32 j + lane: the weight
                 // block's scale, or with ldsb > 0 each row's own (sb[kb * ldsb + n])
                 uint32_t vb[8] = {wb0, wb0, wb0, wb0, wb1, wb1, wb1, wb1};
-                if (ldsb > 0) {
+                if (!PER_TENSOR && ldsb > 0) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int n = tl.n0 + 32 * j + lane;
@@ -362,6 +366,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_store_2d(&tm_c, buf, col, row);
                 bulk_commit_group();
             }
+        };
+        // Per-tensor scaling: the whole product's scale, applied to each fp32
+        // accumulator before the bf16 rounding.
+        const float ts = PER_TENSOR ? sa[0] * sb[0] : 1.0f;
+        auto scaled = [&](uint32_t v) -> uint32_t {
+            return PER_TENSOR ? __float_as_uint(__uint_as_float(v) * ts) : v;
         };
         uint32_t tt = 0;
         bool ok = true;
@@ -425,7 +435,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        pk[jj] = pack_bf16x2(__float_as_uint(sum[2 * jj]), __float_as_uint(sum[2 * jj + 1]));
+                        pk[jj] = pack_bf16x2(scaled(__float_as_uint(sum[2 * jj])),
+                                             scaled(__float_as_uint(sum[2 * jj + 1])));
                     store_block(pk, col0 + 32 * cc, tl.m0 + q * 32);
                 }
                 continue;
@@ -441,8 +452,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    p[jj] = pack_bf16x2(v0[2 * jj], v0[2 * jj + 1]);
-                    p[16 + jj] = pack_bf16x2(v1[2 * jj], v1[2 * jj + 1]);
+                    p[jj] = pack_bf16x2(scaled(v0[2 * jj]), scaled(v0[2 * jj + 1]));
+                    p[16 + jj] = pack_bf16x2(scaled(v1[2 * jj]), scaled(v1[2 * jj + 1]));
                 }
             }
 #pragma unroll
@@ -451,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_x32(taddr + 32 * r, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) p[16 * r + jj] = pack_bf16x2(v[2 * jj], v[2 * jj + 1]);
+                for (int jj = 0; jj < 16; ++jj) p[16 * r + jj] = pack_bf16x2(scaled(v[2 * jj]), scaled(v[2 * jj + 1]));
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -511,10 +522,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <bool GROUPED>
+template <bool GROUPED, bool PER_TENSOR = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     static DeviceOnce attr_done;     // kernel attributes set on this device
-    auto kern = k_gemm_mx<GROUPED>;
+    auto kern = k_gemm_mx<GROUPED, PER_TENSOR>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done.test(dev)) {
@@ -544,6 +555,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;
+    if (a.per_tensor) return a.offsets != nullptr ? cudaErrorInvalidValue : mx::launch<false, true>(a, st);
     return a.offsets != nullptr ? mx::launch<true>(a, st) : mx::launch<false>(a, st);
 }
 

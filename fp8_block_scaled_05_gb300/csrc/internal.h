@@ -80,6 +80,11 @@ cudaError_t launch_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, i
                                           float* s, uint8_t* qt, int64_t ldqt, float* st, bool pow2,
                                           cudaStream_t stream);
 
+// Per-tensor quantiser: zeroes scale_amax[1], reduces max |x| into it, then
+// casts with the scale it derives (written to scale_amax[0]).
+cudaError_t launch_quant_per_tensor(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                    float* scale_amax, bool pow2, int sm_count, cudaStream_t st);
+
 // ------------------------------------------------------------- GEMMs
 // Fused quantisation of the GEMM's output for the next layer: the E4M3 codes
 // and 1x128 scales fp8_quant_act_1x128 would produce from the bf16 C.
@@ -101,6 +106,7 @@ struct GemmArgs {
     const float* sa;
     int64_t ldsa;
     const float* sb;
+    int per_tensor;                 // MX only: sa, sb point at one scale each (per-tensor scaling)
     int64_t ldsb;                   // 0: sb holds 128x128 block scales [G][N/128][K/128];
                                     // > 0: a scale per B row, sb[kb * ldsb + n] (dense promote / MX)
     void* c;

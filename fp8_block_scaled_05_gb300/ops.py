@@ -55,6 +55,9 @@ SIGNATURES = {
                                                   ctypes.c_int, _vp]),
     "fp8_blockscaled_gemm_wgrad": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64,
                                                   _i64, _i64, _u32, _vp, _sz, _vp]),
+    "fp8_quant_per_tensor": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, ctypes.c_int, _vp]),
+    "fp8_tensorscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _u32,
+                                             _vp, _sz, _vp]),
     "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
@@ -205,6 +208,35 @@ def fp8_blockscaled_gemm_wgrad(qa, sa, qb, sb, c, flags: int = 0, workspace: tor
            "fp8_blockscaled_gemm_wgrad")
 
 
+def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor, scale_amax: torch.Tensor,
+                         mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
+    """x bf16 [M, K]; q uint8 [M, K]; scale_amax fp32 [2] (scale, amax) on the device."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    _need(scale_amax, torch.float32, "scale_amax")
+    if scale_amax.numel() < 2 or not scale_amax.is_contiguous():
+        raise ValueError("scale_amax must be a contiguous fp32 tensor of 2 elements")
+    M, K = x.shape
+    _check(lib().fp8_quant_per_tensor(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(scale_amax), int(mode),
+                                      _stream(stream)), "fp8_quant_per_tensor")
+
+
+def fp8_tensorscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
+                          stream=None) -> None:
+    """C[M, N] (bf16) = sa * sb * qa[M, K] qb[N, K]^T; sa, sb one-element fp32 device tensors."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(c, torch.bfloat16, "c")
+    M, K = qa.shape
+    N = qb.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_tensorscaled_gemm(_ptr(qa), qa.stride(0), _ptr(sa), _ptr(qb), qb.stride(0), _ptr(sb), _ptr(c),
+                                       c.stride(0), M, N, K, int(flags), _ptr(workspace), ws_bytes, _stream(stream)),
+           "fp8_tensorscaled_gemm")
+
+
 def fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
                          stream=None) -> None:
     """C[M, N] (bf16) = block-scaled qa[M, K] * qb[N, K]^T."""
@@ -346,6 +378,15 @@ def quant_weight_t(w: torch.Tensor, pow2: bool = False, with_w: bool = False, st
     return (qt, st, q, s) if with_w else (qt, st)
 
 
+def quant_tensor(x: torch.Tensor, pow2: bool = False, stream=None):
+    """Per-tensor quantisation: returns (q uint8 [M, K], scale_amax fp32 [2])."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty(2, dtype=torch.float32, device=x.device)
+    fp8_quant_per_tensor(x, q, sa, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return q, sa
+
+
 _ws: dict[int, torch.Tensor] = {}
 
 
@@ -411,6 +452,16 @@ def wgrad(qt_dy, st_dy, qt_x, st_x, pow2: bool = False, path: str = "auto", out=
     ws = workspace_for(N, K, T, 1, qt_dy.device)
     fp8_blockscaled_gemm_wgrad(qt_dy, st_dy, qt_x, st_x, c, PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0),
                                ws, stream)
+    return c
+
+
+def gemm_tensor(qa, sa, qb, sb, out=None, stream=None):
+    """C = per-tensor-scaled GEMM; sa, sb the scale_amax tensors of quant_tensor
+    (their element 0 is the scale)."""
+    M, K = qa.shape
+    N = qb.shape[0]
+    c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    fp8_tensorscaled_gemm(qa, sa[:1], qb, sb[:1], c, 0, workspace_for(M, N, K, 1, qa.device), stream)
     return c
 
 

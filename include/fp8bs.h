@@ -226,6 +226,48 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
                                 fp8_stream_t stream);
 
 /*
+ * Per-tensor dynamic scaling: one scale for the whole tensor, recomputed from
+ * its current amax so that every value fits the FP8 range (ai.warp-studio.com
+ * end-to-end FP8 RL article, §FP8強化学習における精度と安定性の確保).
+ *
+ *   amax           = max over the whole tensor of |x[m, k]|
+ *   s              = scale(amax)        (see fp8_scale_mode; the block rule
+ *                                        applied to one block, the tensor)
+ *   q[m, k]        = e4m3( RN_fp32(x[m, k] / s) )
+ *
+ * Two kernels on `stream` (an amax reduction, then the cast); the call also
+ * clears the amax word first.
+ * x          device, bf16 [M, K] row-major, row pitch ldx (>= K, % 8 == 0)
+ * q          device, uint8 [M, K] row-major, row pitch ldq (>= K, % 16 == 0)
+ * scale_amax device, 2 floats, 8-byte aligned: [0] receives s, [1] the amax
+ *            (overwritten; both valid once the stream reaches the call's end)
+ * M >= 0 (0 is a no-op: nothing written), K > 0, K % 8 == 0.
+ */
+FP8BS_API fp8_status fp8_quant_per_tensor(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t *q, int64_t ldq, float *scale_amax,
+                                          fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
+ * FP8 GEMM with one scale per operand (per-tensor scaling):
+ *
+ *   C[m, n] = bf16_RN( RN_fp32(sa * sb) * sum_k dec(qa[m, k]) dec(qb[n, k]) )
+ *
+ * with the sum accumulated in fp32 by the tensor core over the whole K range
+ * (no per-K-block promotion is needed: the scales do not change along K).
+ * Runs the MX kernel with unit scale factors.
+ * qa, lda, qb, ldb, c, ldc, M, N, K, workspace: as fp8_blockscaled_gemm.
+ * sa, sb  device, one fp32 each (e.g. scale_amax[0] of fp8_quant_per_tensor).
+ * flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_MX (FP8_GEMM_SCALES_POW2 is
+ *     accepted and changes nothing); _PROMOTE and _SKINNY return
+ *     FP8_ERR_NOT_IMPLEMENTED.
+ */
+FP8BS_API fp8_status fp8_tensorscaled_gemm(const uint8_t *qa, int64_t lda, const float *sa,
+                                           const uint8_t *qb, int64_t ldb, const float *sb,
+                                           void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                           uint32_t flags, void *workspace, size_t ws_bytes,
+                                           fp8_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM with a scale per row of B as well (the wgrad form,
  * dW = dY^T X with both operands from fp8_quant_act_128x1):
  *

@@ -206,6 +206,49 @@ def test_wgrad_validation(L):
         assert call(flags=0x21) == 6
 
 
+def test_quant_per_tensor_validation(L):
+    f = L.fp8_quant_per_tensor
+    ok = dict(x=A16, M=4, K=256, ldx=256, q=A16b, ldq=256, sa=A16c, mode=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["M"], a["K"], a["ldx"], a["q"], a["ldq"], a["sa"], a["mode"], NULL)
+
+    assert call(x=NULL) == 1
+    assert call(sa=NULL) == 1
+    assert call(K=260) == 2                       # K % 8
+    assert call(ldq=128) == 2
+    assert call(ldq=264) == 3
+    assert call(sa=A16c + 4) == 3                 # scale_amax 8-byte aligned
+    assert call(mode=3) == 4
+    assert call(M=0) == 0
+    if not _has_gpu():
+        assert call() == 6
+        assert call(K=8, ldx=8, ldq=16) == 6      # any K % 8 == 0
+
+
+def test_tensorscaled_gemm_validation(L):
+    f = L.fp8_tensorscaled_gemm
+    ok = dict(qa=A16, lda=256, sa=A16b, qb=A16c, ldb=256, sb=A16, c=A16b, ldc=128, M=8, N=128, K=256, flags=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["qa"], a["lda"], a["sa"], a["qb"], a["ldb"], a["sb"], a["c"], a["ldc"], a["M"], a["N"], a["K"],
+                 a["flags"], NULL, 0, NULL)
+
+    assert call(sa=NULL) == 1
+    assert call(sb=NULL) == 1
+    assert call(K=200) == 2
+    assert call(ldb=128) == 2
+    assert call(flags=0x10) == 9                  # promote: not built for per-tensor scales
+    assert call(flags=0x30) == 9                  # nor skinny
+    assert call(M=0) == 0
+    if not _has_gpu():
+        assert call() == 6
+        assert call(flags=0x20) == 6              # MX without the pow2 flag is fine here
+        assert call(flags=0x21) == 6
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0
