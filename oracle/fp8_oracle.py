@@ -34,7 +34,8 @@ reference is dequantise-then-multiply in fp64.
 
 Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
 and (training-side functions) tests/test_oracle_pins_training.py, (per-tensor
-scaling) tests/test_oracle_pins_per_tensor.py against
+scaling) tests/test_oracle_pins_per_tensor.py, (KV-cache attention)
+tests/test_oracle_pins_attention.py against
 facts that do not come from this file (the OCP code table, library
 casts, exact rational arithmetic, brute force, PyTorch autograd and closed
 forms).
@@ -57,6 +58,7 @@ __all__ = [
     "block_amax_col", "quant_act_128x1", "quant_weight_128x128_t",
     "dgrad_ref", "wgrad_ref", "wgrad_ref_rows",
     "quant_per_tensor", "gemm_per_tensor_ref",
+    "quant_with_scale", "decode_attention_ref",
 ]
 
 
@@ -366,3 +368,50 @@ def quant_per_tensor(x: np.ndarray, pow2: bool = False):
 def gemm_per_tensor_ref(qa, sa, qb, sb) -> np.ndarray:
     """C = sA * sB * (dec(qa) @ dec(qb)^T) in float64, one scale per operand."""
     return (e4m3_decode(qa) @ e4m3_decode(qb).T) * (np.float64(np.float32(sa)) * np.float64(np.float32(sb)))
+
+
+# --------------------------------------------------------------------------
+# FP8 KV cache and attention (decode)
+#
+# Page "NVIDIA NeMo RL FP8" (upppp.jp), §KVキャッシュとAttentionにも拡張:
+# the KV cache and the attention run in FP8 too; because the policy's weights
+# change every step, the Q, K and V scales are recomputed at the end of each
+# training step (from training prompts and responses) and handed to the
+# rollout engine.  Readings: one fp32 scale per tensor for each of Q, K and V
+# (the per-tensor rule above applied to the calibration activations); the
+# cache holds E4M3 codes cast with those fixed scales (values beyond the
+# calibrated range saturate at +-448 codes); the attention dequantises and
+# computes softmax(q.K^T / sqrt(D)) V, here in float64.
+# --------------------------------------------------------------------------
+def quant_with_scale(x: np.ndarray, s) -> np.ndarray:
+    """Codes of x under a given fp32 scale: e4m3(RN_fp32(x / s))."""
+    x = np.asarray(x, dtype=np.float32)
+    return _cast(x, np.full(x.shape, np.float32(s), np.float32))
+
+
+def decode_attention_ref(q, sq, k_cache, sk, v_cache, sv, seq_lens) -> np.ndarray:
+    """One decode step of grouped-query attention over an FP8 KV cache.
+
+    q       uint8 [B, Hq, D] codes of the new tokens' queries (scale sq)
+    k_cache uint8 [B, Hkv, T, D] codes (scale sk); v_cache likewise (sv)
+    seq_lens int [B]: keys 0 .. seq_lens[b]-1 of sequence b are attended
+    Query head h reads KV head h // (Hq / Hkv).  Returns float64 [B, Hq, D];
+    a sequence with no keys gets zeros.
+    """
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D), np.float64)
+    qd = e4m3_decode(q) * np.float64(np.float32(sq))
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        for h in range(Hq):
+            g = h // G
+            kd = e4m3_decode(k_cache[b, g, :L]) * np.float64(np.float32(sk))
+            vd = e4m3_decode(v_cache[b, g, :L]) * np.float64(np.float32(sv))
+            scores = kd @ qd[b, h] / np.sqrt(np.float64(D))
+            p = np.exp(scores - scores.max())
+            out[b, h] = (p / p.sum()) @ vd
+    return out
