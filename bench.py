@@ -59,6 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--no-training", action="store_true", help="skip the training-step (forward + backward) "
                                                                 "measurement")
     p.add_argument("--no-per-tensor", action="store_true", help="skip the per-tensor scaling measurement")
+    p.add_argument("--no-attention", action="store_true", help="skip the FP8 KV-cache decode attention measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -508,6 +509,11 @@ def run_ours(args, world, rank, local):
     if not args.no_per_tensor:
         per_tensor = per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_peak)
 
+    # ---------------- one decode step of attention over an FP8 KV cache
+    attention = None
+    if not args.no_attention:
+        attention = attention_measure(args, ops, stream, dev, flush, peaks["hbm_gbs"])
+
     # ---------------- a training step of each layer: forward y = x W^T and the
     # backward GEMMs dX = dY W, dW = dY^T X, every operand from the dual-layout
     # quantisers (x, W and dY are each read once for both of their layouts).
@@ -549,6 +555,7 @@ def run_ours(args, world, rank, local):
             "fused_quant": fused,
             "training": training,
             "per_tensor": per_tensor,
+            "attention": attention,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
@@ -602,6 +609,61 @@ def per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_pe
             "ms_per_step": total / args.steps, "gemm_only_tflops": flops_step / (gemm_ms / 1e3) / 1e12,
             "gemm_frac_fp8": flops_step / (gemm_ms / 1e3) / 1e12 / fp8_peak, "kernels_ms": kern,
             "gpu_launches": 5 * len(layers) * args.steps}
+
+
+def attention_measure(args, ops, stream, dev, flush, hbm_peak):
+    """One decode step of grouped-query attention over an FP8 KV cache at the
+    Qwen3-8B attention shape (32 query heads, 8 KV heads, D 128): 64
+    sequences with 4096 cached tokens each.  The cache holds seeded random
+    codes of N(0, 1) activations under calibrated per-tensor scales (drawn on
+    the device: only the timing matters here; parity is tested separately)."""
+    import torch
+
+    B, Hq, Hkv, T, D = 64, 32, 8, 4096, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed + 77)
+    kv = torch.randn((B * Hkv * T, D), generator=g, device=dev).to(torch.bfloat16)
+    qx = torch.randn((B * Hq, D), generator=g, device=dev).to(torch.bfloat16)
+    sa = torch.empty(2, dtype=torch.float32, device=dev)
+    kc = torch.empty((B * Hkv * T, D), dtype=torch.uint8, device=dev)
+    vc = torch.empty_like(kc)
+    qc = torch.empty((B * Hq, D), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        ops.fp8_quant_per_tensor(kv, kc, sa, 0, stream)          # calibration + cast
+        vc.copy_(kc.flip(0))
+        ops.fp8_quant_per_tensor(qx, qc, sa, 0, stream)
+    torch.cuda.synchronize(dev)
+    del kv
+    sq = sa[:1].clone()
+    sk = sa[:1].clone()
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    need = ops.fp8_decode_attention_workspace_size(B, Hq, T)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    kc4, vc4, qc3 = kc.view(B, Hkv, T, D), vc.view(B, Hkv, T, D), qc.view(B, Hq, D)
+
+    def run():
+        ops.fp8_decode_attention(qc3, sq, kc4, sk, vc4, sk, lens, out, ws, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush()
+            run()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush()
+            e0.record(stream)
+            run()
+            e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+    kv_bytes = 2.0 * B * Hkv * T * D            # FP8 K and V read once
+    alg = kv_bytes + B * Hq * D + 2.0 * B * Hq * D
+    return {"workload": "decode attention, Qwen3-8B heads (Hq 32, Hkv 8, D 128), 64 sequences x 4096 cached tokens",
+            "kv_cache": "E4M3 codes, per-tensor calibrated K and V scales", "ms": ms,
+            "GB/s": alg / (ms / 1e3) / 1e9, "frac_hbm": alg / (ms / 1e3) / 1e9 / hbm_peak,
+            "bf16_cache_bytes_ratio": 2.0, "kernels_per_step": 2 if need else 1}
 
 
 TRAIN_KERNELS = ("quant_x", "quant_w", "fprop", "quant_dy", "dgrad", "wgrad")

@@ -291,6 +291,49 @@ fp8_status fp8_quant_per_tensor(const void* x, int64_t M, int64_t K, int64_t ldx
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_quant_with_scale(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                const float* scale, fp8_stream_t stream) {
+    if (M < 0 || K <= 0 || (K % 8) || M > (1ll << 40) || K > (1ll << 40)) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x || !q || !scale) return FP8_ERR_NULL;
+    if (ldx < K || ldq < K) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldq % 16) || !aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scale) % 4))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_cast_with_scale(x, M, K, ldx, q, ldq, scale, d->sm_count,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fp8_decode_attention_workspace_size(int64_t B, int64_t Hq, int64_t T) {
+    if (B <= 0 || Hq <= 0 || T <= 0 || B > 65535 || Hq > 4096 || T > (1 << 24)) return 0;
+    return attn_workspace_bytes((int)B, (int)Hq, (int)T);
+}
+
+fp8_status fp8_decode_attention(const uint8_t* q, const float* sq, const uint8_t* k_cache, const float* sk,
+                                const uint8_t* v_cache, const float* sv, const int32_t* seq_lens, int64_t B,
+                                int64_t Hq, int64_t Hkv, int64_t T, int64_t D, void* out, void* workspace,
+                                size_t ws_bytes, fp8_stream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || D != 128) return FP8_ERR_SHAPE;
+    if (Hq % Hkv) return FP8_ERR_SHAPE;
+    const int64_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return FP8_ERR_SHAPE;
+    if (B > 65535 || Hkv > 65535 || T > (1 << 24) || Hq > 4096) return FP8_ERR_SHAPE;
+    if (B == 0) return FP8_OK;
+    if (!q || !sq || !k_cache || !sk || !v_cache || !sv || !seq_lens || !out) return FP8_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) % 4) || (reinterpret_cast<uintptr_t>(sq) % 4) ||
+        (reinterpret_cast<uintptr_t>(sk) % 4) || (reinterpret_cast<uintptr_t>(sv) % 4))
+        return FP8_ERR_ALIGN;
+    const size_t need = attn_workspace_bytes((int)B, (int)Hq, (int)T);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace))) return FP8_ERR_WORKSPACE;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_decode_attention(q, sq, k_cache, sk, v_cache, sv, seq_lens, (int)B, (int)Hq, (int)Hkv,
+                                               (int)T, workspace, static_cast<uint16_t*>(out),
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t* splits) {
     const uint32_t path = plan_path(M, K, flags);
     int32_t sp = 1;

@@ -85,6 +85,16 @@ cudaError_t launch_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, i
 cudaError_t launch_quant_per_tensor(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                     float* scale_amax, bool pow2, int sm_count, cudaStream_t st);
 
+cudaError_t launch_cast_with_scale(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                   const float* scale, int sm_count, cudaStream_t st);
+
+// FP8 KV cache decode attention (attn.cu): D = 128, Hq / Hkv in {1, 2, 4, 8}.
+int attn_splits(int T);
+size_t attn_workspace_bytes(int B, int Hq, int T);
+cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uint8_t* kc, const float* sk,
+                                    const uint8_t* vc, const float* sv, const int32_t* seq_lens, int B, int Hq,
+                                    int Hkv, int T, void* workspace, uint16_t* out, cudaStream_t st);
+
 // ------------------------------------------------------------- GEMMs
 // Fused quantisation of the GEMM's output for the next layer: the E4M3 codes
 // and 1x128 scales fp8_quant_act_1x128 would produce from the bf16 C.

@@ -125,6 +125,61 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_quant_tensor(const uint16_t* 
     }
 }
 
+// Cast under a given scale (scale[0], a positive normal fp32 in device
+// memory: a calibrated KV-cache or query scale): q = e4m3(RN(x / s)), values
+// beyond +-448 s saturating.
+__global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __restrict__ x, ChunkWalk w,
+                                                             uint8_t* __restrict__ q, int64_t ldq,
+                                                             const float* __restrict__ scale) {
+    const float sc = __ldg(scale);
+    const BlockScale bs = scale_from_sr(sc, __frcp_rn(sc), false);
+    if (w.flat) {
+        const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
+        for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
+            uint4 v[kPtUnroll];
+#pragma unroll
+            for (int u = 0; u < kPtUnroll; ++u) {
+                const int64_t c = c0 + u * step;
+                v[u] = c < total ? __ldcs(reinterpret_cast<const uint4*>(x + c * 8)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kPtUnroll; ++u) {
+                const int64_t c = c0 + u * step;
+                if (c < total) __stcs(reinterpret_cast<uint2*>(q + c * 8), quant8(v[u], bs));
+            }
+        }
+    } else {
+        for (int64_t r = blockIdx.x; r < w.M; r += gridDim.x) {
+            for (int64_t c0 = threadIdx.x; c0 < w.cpr; c0 += kPtThreads * kPtUnroll) {
+                uint4 v[kPtUnroll];
+#pragma unroll
+                for (int u = 0; u < kPtUnroll; ++u) {
+                    const int64_t c = c0 + (int64_t)u * kPtThreads;
+                    v[u] = c < w.cpr ? __ldcs(reinterpret_cast<const uint4*>(x + chunk_offset(w, r, c)))
+                                     : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kPtUnroll; ++u) {
+                    const int64_t c = c0 + (int64_t)u * kPtThreads;
+                    if (c < w.cpr) __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8), quant8(v[u], bs));
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_cast_with_scale(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                   const float* scale, int sm_count, cudaStream_t st) {
+    if (M == 0) return cudaSuccess;
+    ChunkWalk w{M, K / 8, ldx, ldx == K && ldq == K};
+    const int64_t chunks = M * w.cpr;
+    int64_t grid = (int64_t)sm_count * 4;
+    const int64_t need = w.flat ? (chunks + (int64_t)kPtThreads * kPtUnroll - 1) / ((int64_t)kPtThreads * kPtUnroll) : M;
+    if (need < grid) grid = need < 1 ? 1 : need;
+    k_cast_scale<<<(unsigned)grid, kPtThreads, 0, st>>>(static_cast<const uint16_t*>(x), w, q, ldq, scale);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant_per_tensor(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                     float* scale_amax, bool pow2, int sm_count, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(scale_amax + 1, 0, sizeof(float), st);

@@ -58,6 +58,10 @@ SIGNATURES = {
     "fp8_quant_per_tensor": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, ctypes.c_int, _vp]),
     "fp8_tensorscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _u32,
                                              _vp, _sz, _vp]),
+    "fp8_quant_with_scale": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "fp8_decode_attention_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "fp8_decode_attention": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp,
+                                            _vp, _sz, _vp]),
     "fp8_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
@@ -219,6 +223,39 @@ def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor, scale_amax: torch.Ten
     M, K = x.shape
     _check(lib().fp8_quant_per_tensor(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(scale_amax), int(mode),
                                       _stream(stream)), "fp8_quant_per_tensor")
+
+
+def fp8_quant_with_scale(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None) -> None:
+    """q = e4m3(x / scale[0]); x bf16 [M, K] (or any 2-D view), q uint8 of the same shape."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    _need(scale, torch.float32, "scale")
+    M, K = x.shape
+    _check(lib().fp8_quant_with_scale(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(scale),
+                                      _stream(stream)), "fp8_quant_with_scale")
+
+
+def fp8_decode_attention_workspace_size(B: int, Hq: int, T: int) -> int:
+    return int(lib().fp8_decode_attention_workspace_size(B, Hq, T))
+
+
+def fp8_decode_attention(q, sq, k_cache, sk, v_cache, sv, seq_lens, out, workspace=None, stream=None) -> None:
+    """q uint8 [B, Hq, D]; k_cache / v_cache uint8 [B, Hkv, T, D]; sq, sk, sv
+    one-element fp32 device tensors; seq_lens int32 [B]; out bf16 [B, Hq, D]."""
+    for t, dt, n in ((q, torch.uint8, "q"), (k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
+                     (sq, torch.float32, "sq"), (sk, torch.float32, "sk"), (sv, torch.float32, "sv"),
+                     (seq_lens, torch.int32, "seq_lens"), (out, torch.bfloat16, "out")):
+        _need(t, dt, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, D = q.shape
+    Hkv, T = k_cache.shape[1], k_cache.shape[2]
+    if v_cache.shape != k_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("cache shapes do not match q")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_decode_attention(_ptr(q), _ptr(sq), _ptr(k_cache), _ptr(sk), _ptr(v_cache), _ptr(sv),
+                                      _ptr(seq_lens), B, Hq, Hkv, T, D, _ptr(out), _ptr(workspace), ws_bytes,
+                                      _stream(stream)), "fp8_decode_attention")
 
 
 def fp8_tensorscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
@@ -463,6 +500,18 @@ def gemm_tensor(qa, sa, qb, sb, out=None, stream=None):
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
     fp8_tensorscaled_gemm(qa, sa[:1], qb, sb[:1], c, 0, workspace_for(M, N, K, 1, qa.device), stream)
     return c
+
+
+def decode_attention(q, sq, k_cache, sk, v_cache, sv, seq_lens, stream=None):
+    """One FP8 decode-attention step; allocates the bf16 output and the
+    split workspace.  sq, sk, sv: fp32 device tensors whose element 0 is the scale."""
+    B, Hq, D = q.shape
+    T = k_cache.shape[2]
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    need = fp8_decode_attention_workspace_size(B, Hq, T)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    fp8_decode_attention(q, sq[:1], k_cache, sk[:1], v_cache, sv[:1], seq_lens, out, ws, stream)
+    return out
 
 
 def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):

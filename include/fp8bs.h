@@ -248,6 +248,56 @@ FP8BS_API fp8_status fp8_quant_per_tensor(const void *x, int64_t M, int64_t K, i
                                           fp8_scale_mode mode, fp8_stream_t stream);
 
 /*
+ * FP8 KV cache and decode attention (upppp.jp NeMo RL FP8 article,
+ * §KVキャッシュとAttentionにも拡張): during rollout the KV cache and the
+ * attention run in FP8; the Q, K and V scales are recomputed at the end of
+ * each training step (the policy changes) and used for the next rollout.
+ * Calibration is fp8_quant_per_tensor's amax (scale_amax[0] = amax/448 of
+ * the calibration Q, K or V activations); the cache and the queries are cast
+ * with fp8_quant_with_scale; fp8_decode_attention runs one decode step.
+ */
+
+/*
+ * Cast under a given scale:  q[m, k] = e4m3( RN_fp32(x[m, k] / s) ),  s = scale[0].
+ * Values beyond +-448 s saturate to the largest code (a calibrated scale can
+ * be exceeded by later activations).
+ * x      device, bf16 [M, K] row-major, row pitch ldx (>= K, % 8 == 0)
+ * q      device, uint8 [M, K], row pitch ldq (>= K, % 16 == 0)
+ * scale  device, one fp32; must be a positive normal number (it is read on
+ *        the device; nothing checks it)
+ * M >= 0 (0 is a no-op), K > 0, K % 8 == 0.  x, q 16-byte aligned.
+ */
+FP8BS_API fp8_status fp8_quant_with_scale(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t *q, int64_t ldq, const float *scale,
+                                          fp8_stream_t stream);
+
+/*
+ * One decode step of grouped-query attention over an FP8 KV cache:
+ *
+ *   o[b, h, :] = sum_t p_t * dec(v[b, g, t, :]) * sv,   g = h / (Hq / Hkv),
+ *   p = softmax_t( (dec(q[b, h, :]) sq) . (dec(k[b, g, t, :]) sk) / sqrt(D) ),
+ *   t = 0 .. seq_lens[b] - 1   (a sequence with no keys gets zeros)
+ *
+ * computed in fp32 (online softmax over key splits of 512, merged in a
+ * second kernel when T > 512), output rounded to bf16.
+ * q        device, uint8 [B, Hq, D] codes (scale sq[0])
+ * k_cache  device, uint8 [B, Hkv, T, D] codes (sk[0]); v_cache likewise (sv[0])
+ * seq_lens device, int32 [B]; values are clamped to [0, T]
+ * out      device, bf16 [B, Hq, D]
+ * workspace device scratch of fp8_decode_attention_workspace_size(B, Hq, T)
+ *          bytes (NULL when that is 0); no state is kept between calls.
+ * D == 128; Hq % Hkv == 0 with Hq / Hkv in {1, 2, 4, 8}; T > 0.
+ * B >= 0 (0 is a no-op).  q, caches, out and workspace 16-byte aligned.
+ */
+FP8BS_API size_t fp8_decode_attention_workspace_size(int64_t B, int64_t Hq, int64_t T);
+FP8BS_API fp8_status fp8_decode_attention(const uint8_t *q, const float *sq,
+                                          const uint8_t *k_cache, const float *sk,
+                                          const uint8_t *v_cache, const float *sv,
+                                          const int32_t *seq_lens, int64_t B, int64_t Hq,
+                                          int64_t Hkv, int64_t T, int64_t D, void *out,
+                                          void *workspace, size_t ws_bytes, fp8_stream_t stream);
+
+/*
  * FP8 GEMM with one scale per operand (per-tensor scaling):
  *
  *   C[m, n] = bf16_RN( RN_fp32(sa * sb) * sum_k dec(qa[m, k]) dec(qb[n, k]) )

@@ -249,6 +249,45 @@ def test_tensorscaled_gemm_validation(L):
         assert call(flags=0x21) == 6
 
 
+def test_quant_with_scale_validation(L):
+    f = L.fp8_quant_with_scale
+    assert f(NULL, 4, 128, 128, A16b, 128, A16c, NULL) == 1
+    assert f(A16, 4, 128, 128, A16b, 128, NULL, NULL) == 1
+    assert f(A16, 4, 130, 136, A16b, 144, A16c, NULL) == 2        # K % 8
+    assert f(A16, 4, 128, 128, A16b, 136, A16c, NULL) == 3        # ldq % 16
+    assert f(A16, 4, 128, 128, A16b, 128, A16c + 2, NULL) == 3    # scale 4-byte aligned
+    assert f(A16, 0, 128, 128, NULL, 128, NULL, NULL) == 0
+    if not _has_gpu():
+        assert f(A16, 4, 128, 128, A16b, 128, A16c, NULL) == 6
+
+
+def test_decode_attention_validation(L):
+    f = L.fp8_decode_attention
+    ok = dict(q=A16, sq=A16b, k=A16c, sk=A16b, v=A16, sv=A16b, lens=A16c, B=2, Hq=8, Hkv=2, T=1024, D=128,
+              out=A16b, ws=A16c, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["sq"], a["k"], a["sk"], a["v"], a["sv"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["T"],
+                 a["D"], a["out"], a["ws"], a["wsb"], NULL)
+
+    assert call(D=64) == 2
+    assert call(Hq=6, Hkv=4) == 2                 # Hq % Hkv
+    assert call(Hq=48, Hkv=3) == 2                # group of 16
+    assert call(T=0) == 2
+    assert call(q=NULL) == 1
+    assert call(lens=NULL) == 1
+    assert call(k=MIS) == 3
+    assert call(ws=NULL) == 5                     # two splits need the workspace
+    assert call(wsb=100) == 5
+    assert call(B=0) == 0
+    assert L.fp8_decode_attention_workspace_size(2, 8, 512) == 0       # one split: direct output
+    assert L.fp8_decode_attention_workspace_size(2, 8, 1024) == 2 * 8 * 2 * 130 * 4
+    if not _has_gpu():
+        assert call() == 6
+        assert call(T=512, ws=NULL, wsb=0) == 6
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0
