@@ -13,12 +13,23 @@
 //
 // k_decode_attn: one CTA per (key split, KV head, sequence), 4 warps.  The G
 // query heads of the group share every K/V byte the CTA reads.
-//   scores  lanes over keys (32 keys per warp block), each lane the full
-//           128-dim dot products of its key with the G dequantised queries
-//           (shared memory, the scale product and log2(e)/sqrt(D) folded in);
-//   softmax online per warp (max and sum by shuffles, exp2);
-//   P V     lanes over dims: lane l adds p_t v[t, 4l .. 4l+3] for the
-//           block's 32 keys (a 128-byte coalesced row per key);
+//   scores  Q K^T on the tensor cores straight from the E4M3 codes
+//           (mma.sync m16n8k32 e4m3, fp32 accumulation): the G <= 8 heads
+//           are the MMA's rows (the rest zero), 8 keys per MMA column tile,
+//           4 tiles = the warp's block of 32 keys, 4 k-steps = D.  The dot
+//           product sums over all dims, so the k positions can take the dims
+//           in any order that A and B share: lane (group r, j = lane % 4)
+//           loads the 32-byte segment j of its key's row, and k-step s uses
+//           bytes 8s .. 8s+7 of it (the query segment likewise);
+//   softmax online per warp, on the C fragments (head r's scores sit in
+//           lanes 4r .. 4r+3: two shuffles per reduction), exp2 with the
+//           scale product and log2(e)/sqrt(D) folded in;
+//   P V     on the CUDA cores, lanes over dims: lane l adds p_t v[t, 4l .. 4l+3]
+//           for the block's 32 keys, packed fma.rn.f32x2;
+//   loads   each warp streams its key blocks through two shared-memory
+//           stages with cp.async (16 bytes per lane, zero-filled past the
+//           sequence), the next block's K and V landing while the current one
+//           is computed;
 //   merge   the 4 warps' (m, l, o) in shared memory; with several splits the
 //           CTA writes (m, l, o) and k_attn_combine merges the splits.
 #include <cstdint>
@@ -65,6 +76,41 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// 16-byte global -> shared copy, zero-filled when !valid (nothing is read).
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Per warp, per stage: 32 key rows (16-byte chunk c of row r at chunk
+// c ^ (r % 8), so the fragment reads below spread over all banks) and 32
+// value rows, 4 KB each.
+constexpr int kAttnStages = 2;
+constexpr int kAttnStageBytes = 2 * 32 * kAttnD;
+constexpr int kAttnSmemBytes = kAttnWarps * kAttnStages * kAttnStageBytes;
+
+// D = A B + C for one m16n8k32 tile, A (16 x 32) and B (32 x 8) E4M3, fp32 C/D.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// acc[0..1] += p * (v0, v1) as one packed FMA.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float p, float v0, float v1) {
+    uint64_t a, v, pp;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(v0), "f"(v1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(pp) : "f"(p));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(v), "l"(pp));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
 // part: [B][Hq][n_split][2 + D] floats (m in log2 units, l, o unnormalised)
 // when n_split > 1; otherwise the output is written directly.
 template <int G>
@@ -74,113 +120,140 @@ __global__ void __launch_bounds__(32 * kAttnWarps) k_decode_attn(
     const int32_t* __restrict__ seq_lens, int Hkv, int T, int n_split, float* __restrict__ part,
     uint16_t* __restrict__ out) {
     constexpr int D = kAttnD;
-    __shared__ __align__(16) float qs[G][D];
+    static_assert(G >= 1 && G <= 8, "query heads per KV head");
     __shared__ float ps[kAttnWarps][G][32];
+    __shared__ float cs[kAttnWarps][G];
     __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
     __shared__ __align__(16) float wo[kAttnWarps][G][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 2, j = lane & 3;   // MMA row (head) and 32-byte segment
     const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int Hq = Hkv * G;
     const int L = min(max(seq_lens[b], 0), T);
     const int t0 = sp * kAttnSplit, t1 = min(t0 + kAttnSplit, L);
 
-    // queries of the group, dequantised, with sq * sk * log2(e) / sqrt(D)
-    const float c = sq[0] * sk[0] * (1.4426950408889634f * 0.08838834764831845f);
-    for (int i = threadIdx.x; i < G * D / 4; i += blockDim.x) {
-        const int h = i / (D / 4), d4 = i % (D / 4);
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(q + ((size_t)b * Hq + g * G + h) * D + 4 * d4);
-        float f[4];
-        e4m3x4_to_f32(w, f);
-        *reinterpret_cast<float4*>(&qs[h][4 * d4]) = make_float4(f[0] * c, f[1] * c, f[2] * c, f[3] * c);
+    // A fragments: head grp's query segment j (zero rows past the group)
+    uint32_t qa[8];
+    {
+        uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+        if (grp < G) {
+            const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + g * G + grp) * D + 32 * j);
+            q0 = __ldg(qrow);
+            q1 = __ldg(qrow + 1);
+        }
+        qa[0] = q0.x; qa[1] = q0.y; qa[2] = q0.z; qa[3] = q0.w;
+        qa[4] = q1.x; qa[5] = q1.y; qa[6] = q1.z; qa[7] = q1.w;
     }
-    __syncthreads();
-
+    // scores in log2 units: raw code products times sq sk log2(e) / sqrt(D)
+    const float c = sq[0] * sk[0] * (1.4426950408889634f * 0.08838834764831845f);
     const float vscale = sv[0];
     const size_t head_base = ((size_t)b * Hkv + g) * (size_t)T * D;
-    float m[G], l[G], o[G][4];
+    float m = -INFINITY, l = 0.0f;             // head grp's state (lanes 4 grp .. 4 grp + 3)
+    float o[G][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.0f;
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[h][j] = 0.0f;
-    }
-    for (int tb = t0 + 32 * warp; tb < t1; tb += 32 * kAttnWarps) {
-        const int t = tb + lane;
-        const bool valid = t < t1;
-        float s[G];
+        for (int e = 0; e < 4; ++e) o[h][e] = 0.0f;
+
+    // the warp's key blocks: tb = t0 + 32 warp + 128 i
+    extern __shared__ __align__(128) uint8_t attn_smem[];
+    uint8_t* wbuf = attn_smem + (size_t)warp * kAttnStages * kAttnStageBytes;
+    auto issue = [&](int tb, int stage) {   // cp.async of block tb into `stage`
+        uint8_t* ks = wbuf + stage * kAttnStageBytes;
+        uint8_t* vs = ks + 32 * D;
 #pragma unroll
-        for (int h = 0; h < G; ++h) s[h] = 0.0f;
-        if (valid) {
-            // the key's whole 128-byte row first, then the arithmetic
-            const uint4* krow = reinterpret_cast<const uint4*>(kc + head_base + (size_t)t * D);
-            uint4 kr[D / 16];
-#pragma unroll
-            for (int ch = 0; ch < D / 16; ++ch) kr[ch] = __ldg(krow + ch);
-#pragma unroll
-            for (int ch = 0; ch < D / 16; ++ch) {
-                const uint32_t w[4] = {kr[ch].x, kr[ch].y, kr[ch].z, kr[ch].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float kf[4];
-                    e4m3x4_to_f32(w[e], kf);
-                    const int d = 16 * ch + 4 * e;
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float4 qv = *reinterpret_cast<const float4*>(&qs[h][d]);
-                        s[h] = fmaf(qv.x, kf[0], s[h]);
-                        s[h] = fmaf(qv.y, kf[1], s[h]);
-                        s[h] = fmaf(qv.z, kf[2], s[h]);
-                        s[h] = fmaf(qv.w, kf[3], s[h]);
-                    }
-                }
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int qi = lane + 32 * u, r = qi >> 3, c = qi & 7;
+            const bool valid = tb + r < t1;
+            const size_t off = head_base + (size_t)(valid ? tb + r : 0) * D + 16 * c;
+            cp16(ks + r * D + 16 * (c ^ (r & 7)), kc + off, valid);
+            cp16(vs + r * D + 16 * c, vc + off, valid);
         }
+    };
+    int tb = t0 + 32 * warp;
+    if (tb < t1) issue(tb, 0);
+    cp_commit();
+    for (int it = 0; tb < t1; tb += 32 * kAttnWarps, ++it) {
+        const int stage = it & 1;
+        if (tb + 32 * kAttnWarps < t1) issue(tb + 32 * kAttnWarps, stage ^ 1);
+        cp_commit();
+        cp_wait<1>();   // this block's copies (all but the newest group) have landed
+        __syncwarp();
+        const uint8_t* ks = wbuf + stage * kAttnStageBytes;
+        const uint8_t* vs = ks + 32 * D;
+        const int nk = min(32, t1 - tb);   // warp-uniform
+        float sc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            // B fragments: key row 8 nt + grp, 32-byte segment j (chunks 2j, 2j+1)
+            const int r = 8 * nt + grp;
+            const uint4 k0 = *reinterpret_cast<const uint4*>(ks + r * D + 16 * ((2 * j) ^ (r & 7)));
+            const uint4 k1 = *reinterpret_cast<const uint4*>(ks + r * D + 16 * ((2 * j + 1) ^ (r & 7)));
+            const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] = 0.0f;
+#pragma unroll
+            for (int ksx = 0; ksx < 4; ++ksx) mma_e4m3_16832(sc[nt], qa[2 * ksx], qa[2 * ksx + 1], kw[2 * ksx], kw[2 * ksx + 1]);
+        }
+        // this lane: head grp, keys tb + 8 nt + 2 j + e (e = 0, 1)
+        float s8[8];
+        float bm = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const bool valid = 8 * nt + 2 * j + e < nk;
+                s8[2 * nt + e] = valid ? sc[nt][e] * c : -INFINITY;
+                bm = fmaxf(bm, s8[2 * nt + e]);
+            }
+        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 2));   // key tb is valid: bm is finite
+        const float mn = fmaxf(m, bm);
+        const float corr = exp2f(m - mn);                        // 0 while m is -inf
+        float psum = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float pv = exp2f(s8[2 * nt + e] - mn);     // 0 for the invalid keys
+                psum += pv;
+                if (grp < G) ps[warp][grp][8 * nt + 2 * j + e] = pv;
+            }
+        psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 1);
+        psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 2);
+        l = l * corr + psum;
+        m = mn;
+        if (grp < G && j == 0) cs[warp][grp] = corr;
+        __syncwarp();
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float bm = warp_max(valid ? s[h] : -INFINITY);   // lane 0's key is valid: bm is finite
-            const float mn = fmaxf(m[h], bm);
-            const float corr = exp2f(m[h] - mn);                  // 0 while m[h] is -inf
-            const float p = valid ? exp2f(s[h] - mn) : 0.0f;
-            l[h] = l[h] * corr + warp_sum(p);
-            m[h] = mn;
+            const float cf = cs[warp][h];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[h][j] *= corr;
-            ps[warp][h][lane] = p;
+            for (int e = 0; e < 4; ++e) o[h][e] *= cf;
         }
-        __syncwarp();
-        const int nk = min(32, t1 - tb);   // warp-uniform
-        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(vc + head_base + (size_t)tb * D) + lane;
-        for (int j0 = 0; j0 < nk; j0 += 8) {
-            uint32_t vw[8];   // 8 value rows in flight
+#pragma unroll 8
+        for (int u = 0; u < nk; ++u) {
+            float vf[4];
+            e4m3x4_to_f32(*reinterpret_cast<const uint32_t*>(vs + u * D + 4 * lane), vf);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) vw[u] = j0 + u < nk ? __ldg(vrow + (size_t)(j0 + u) * (D / 4)) : 0u;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (j0 + u < nk) {
-                    float vf[4];
-                    e4m3x4_to_f32(vw[u], vf);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float p = ps[warp][h][j0 + u];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) o[h][e] = fmaf(p, vf[e], o[h][e]);
-                    }
-                }
+            for (int h = 0; h < G; ++h) {
+                const float pw = ps[warp][h][u];
+                fma2(o[h][0], o[h][1], pw, vf[0], vf[1]);
+                fma2(o[h][2], o[h][3], pw, vf[2], vf[3]);
             }
         }
-        __syncwarp();
+        __syncwarp();   // the stage is read before the next issue overwrites it
     }
+    cp_wait<0>();
 
     // merge the warps
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        if (lane == 0) {
-            wm[warp][h] = m[h];
-            wl[warp][h] = l[h];
-        }
-        *reinterpret_cast<float4*>(&wo[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+    if (grp < G && j == 0) {
+        wm[warp][grp] = m;
+        wl[warp][grp] = l;
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+        *reinterpret_cast<float4*>(&wo[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
     __syncthreads();
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
         const int h = i / D, d = i % D;
@@ -247,11 +320,21 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
     const dim3 grid((unsigned)ns, (unsigned)Hkv, (unsigned)B);
     float* part = static_cast<float*>(workspace);
     const int G = Hq / Hkv;
+    static DeviceOnce attr_done;   // dynamic shared memory above 48 KB, per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_done.test(dev)) {
+        for (auto kern : {k_decode_attn<1>, k_decode_attn<2>, k_decode_attn<4>, k_decode_attn<8>}) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
+        attr_done.set(dev);
+    }
     switch (G) {
-        case 1: k_decode_attn<1><<<grid, 32 * kAttnWarps, 0, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
-        case 2: k_decode_attn<2><<<grid, 32 * kAttnWarps, 0, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
-        case 4: k_decode_attn<4><<<grid, 32 * kAttnWarps, 0, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
-        case 8: k_decode_attn<8><<<grid, 32 * kAttnWarps, 0, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
+        case 1: k_decode_attn<1><<<grid, 32 * kAttnWarps, kAttnSmemBytes, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
+        case 2: k_decode_attn<2><<<grid, 32 * kAttnWarps, kAttnSmemBytes, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
+        case 4: k_decode_attn<4><<<grid, 32 * kAttnWarps, kAttnSmemBytes, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
+        case 8: k_decode_attn<8><<<grid, 32 * kAttnWarps, kAttnSmemBytes, st>>>(q, sq, kc, sk, vc, sv, seq_lens, Hkv, T, ns, part, out); break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();
