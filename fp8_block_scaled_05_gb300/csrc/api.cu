@@ -305,6 +305,23 @@ fp8_status fp8_quant_with_scale(const void* x, int64_t M, int64_t K, int64_t ldx
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_kv_cache_append(const void* k_new, const void* v_new, const float* sk, const float* sv,
+                               const int32_t* seq_lens, uint8_t* k_cache, uint8_t* v_cache, int64_t B, int64_t Hkv,
+                               int64_t T, int64_t D, fp8_stream_t stream) {
+    if (B < 0 || Hkv <= 0 || T <= 0 || D != 128 || B > 65535 || Hkv > 65535 || T > (1 << 24)) return FP8_ERR_SHAPE;
+    if (B * Hkv > INT32_MAX) return FP8_ERR_SHAPE;
+    if (B == 0) return FP8_OK;
+    if (!k_new || !v_new || !sk || !sv || !seq_lens || !k_cache || !v_cache) return FP8_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) % 4) || (reinterpret_cast<uintptr_t>(sk) % 4) ||
+        (reinterpret_cast<uintptr_t>(sv) % 4))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_kv_append(k_new, v_new, sk, sv, seq_lens, k_cache, v_cache, (int)B, (int)Hkv, (int)T,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t fp8_decode_attention_workspace_size(int64_t B, int64_t Hq, int64_t T) {
     if (B <= 0 || Hq <= 0 || T <= 0 || B > 65535 || Hq > 4096 || T > (1 << 24)) return 0;
     return attn_workspace_bytes((int)B, (int)Hq, (int)T);

@@ -306,6 +306,37 @@ __global__ void __launch_bounds__(kAttnD) k_attn_combine(const float* __restrict
     out[bh * D + threadIdx.x] = f32_to_bf16(r);
 }
 
+// Cache append for one decode step: the new token's K and V rows of every
+// (sequence b, KV head g), cast with the calibrated scales, go to slot
+// seq_lens[b] of the cache (skipped when that is outside [0, T)).  One warp
+// per (b, g): lanes 0..15 cast K (8 values each), lanes 16..31 V.
+__global__ void __launch_bounds__(32) k_kv_append(const uint16_t* __restrict__ k_new,
+                                                  const uint16_t* __restrict__ v_new, const float* __restrict__ sk,
+                                                  const float* __restrict__ sv, const int32_t* __restrict__ seq_lens,
+                                                  uint8_t* __restrict__ kc, uint8_t* __restrict__ vc, int Hkv, int T) {
+    constexpr int D = kAttnD;
+    const int bg = blockIdx.x, b = bg / Hkv, lane = threadIdx.x;
+    const int pos = seq_lens[b];
+    if (pos < 0 || pos >= T) return;
+    const bool is_v = lane >= 16;
+    const int c = lane & 15;
+    const float s = __ldg(is_v ? sv : sk);
+    const BlockScale bs = scale_from_sr(s, __frcp_rn(s), false);
+    const uint16_t* src = (is_v ? v_new : k_new) + (size_t)bg * D + 8 * c;
+    uint8_t* dst = (is_v ? vc : kc) + ((size_t)bg * T + pos) * D + 8 * c;
+    *reinterpret_cast<uint2*>(dst) = quant8(*reinterpret_cast<const uint4*>(src), bs);
+}
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const float* sk, const float* sv,
+                             const int32_t* seq_lens, uint8_t* kc, uint8_t* vc, int B, int Hkv, int T,
+                             cudaStream_t st) {
+    if (B == 0) return cudaSuccess;
+    k_kv_append<<<(unsigned)(B * Hkv), 32, 0, st>>>(static_cast<const uint16_t*>(k_new),
+                                                      static_cast<const uint16_t*>(v_new), sk, sv, seq_lens, kc, vc,
+                                                      Hkv, T);
+    return cudaGetLastError();
+}
+
 int attn_splits(int T) { return (T + kAttnSplit - 1) / kAttnSplit; }
 
 size_t attn_workspace_bytes(int B, int Hq, int T) {

@@ -90,6 +90,9 @@ cudaError_t launch_cast_with_scale(const void* x, int64_t M, int64_t K, int64_t 
 
 // FP8 KV cache decode attention (attn.cu): D = 128, Hq / Hkv in {1, 2, 4, 8}.
 int attn_splits(int T);
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const float* sk, const float* sv,
+                             const int32_t* seq_lens, uint8_t* kc, uint8_t* vc, int B, int Hkv, int T,
+                             cudaStream_t st);
 size_t attn_workspace_bytes(int B, int Hq, int T);
 cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uint8_t* kc, const float* sk,
                                     const uint8_t* vc, const float* sv, const int32_t* seq_lens, int B, int Hq,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "fp8_tensorscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _u32,
                                              _vp, _sz, _vp]),
     "fp8_quant_with_scale": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "fp8_kv_cache_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "fp8_decode_attention_workspace_size": (_sz, [_i64, _i64, _i64]),
     "fp8_decode_attention": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp,
                                             _vp, _sz, _vp]),
@@ -233,6 +234,21 @@ def fp8_quant_with_scale(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, 
     M, K = x.shape
     _check(lib().fp8_quant_with_scale(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(scale),
                                       _stream(stream)), "fp8_quant_with_scale")
+
+
+def fp8_kv_cache_append(k_new, v_new, sk, sv, seq_lens, k_cache, v_cache, stream=None) -> None:
+    """k_new / v_new bf16 [B, Hkv, D]; caches uint8 [B, Hkv, T, D]; writes slot seq_lens[b]."""
+    for t, dt, n in ((k_new, torch.bfloat16, "k_new"), (v_new, torch.bfloat16, "v_new"),
+                     (sk, torch.float32, "sk"), (sv, torch.float32, "sv"), (seq_lens, torch.int32, "seq_lens"),
+                     (k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache")):
+        _need(t, dt, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hkv, T, D = k_cache.shape
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shapes do not match the cache")
+    _check(lib().fp8_kv_cache_append(_ptr(k_new), _ptr(v_new), _ptr(sk), _ptr(sv), _ptr(seq_lens), _ptr(k_cache),
+                                     _ptr(v_cache), B, Hkv, T, D, _stream(stream)), "fp8_kv_cache_append")
 
 
 def fp8_decode_attention_workspace_size(B: int, Hq: int, T: int) -> int:

@@ -272,6 +272,22 @@ FP8BS_API fp8_status fp8_quant_with_scale(const void *x, int64_t M, int64_t K, i
                                           fp8_stream_t stream);
 
 /*
+ * Cache append of one decode step: for every sequence b and KV head g,
+ *   k_cache[b, g, seq_lens[b], :] = e4m3( RN_fp32(k_new[b, g, :] / sk[0]) )
+ * and likewise v with sv[0] (values beyond +-448 s saturate).  Rows whose
+ * slot seq_lens[b] is outside [0, T) are skipped; seq_lens is not changed
+ * (the caller advances it after the step's attention).
+ * k_new, v_new  device, bf16 [B, Hkv, D], contiguous
+ * sk, sv        device, one fp32 each (positive normal numbers)
+ * k_cache, v_cache  device, uint8 [B, Hkv, T, D]
+ * D == 128; B >= 0 (0 is a no-op).  Tensors 16-byte aligned.
+ */
+FP8BS_API fp8_status fp8_kv_cache_append(const void *k_new, const void *v_new, const float *sk,
+                                         const float *sv, const int32_t *seq_lens, uint8_t *k_cache,
+                                         uint8_t *v_cache, int64_t B, int64_t Hkv, int64_t T, int64_t D,
+                                         fp8_stream_t stream);
+
+/*
  * One decode step of grouped-query attention over an FP8 KV cache:
  *
  *   o[b, h, :] = sum_t p_t * dec(v[b, g, t, :]) * sv,   g = h / (Hq / Hkv),

@@ -288,6 +288,16 @@ def test_decode_attention_validation(L):
         assert call(T=512, ws=NULL, wsb=0) == 6
 
 
+def test_kv_cache_append_validation(L):
+    f = L.fp8_kv_cache_append
+    assert f(A16, A16b, A16c, A16c, A16, A16b, A16c, 2, 8, 64, 64, NULL) == 2     # D != 128
+    assert f(NULL, A16b, A16c, A16c, A16, A16b, A16c, 2, 8, 64, 128, NULL) == 1
+    assert f(A16, A16b, A16c, A16c, A16, MIS, A16c, 2, 8, 64, 128, NULL) == 3
+    assert f(A16, A16b, A16c, A16c, A16, A16b, A16c, 0, 8, 64, 128, NULL) == 0
+    if not _has_gpu():
+        assert f(A16, A16b, A16c, A16c, A16, A16b, A16c, 2, 8, 64, 128, NULL) == 6
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0

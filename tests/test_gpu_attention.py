@@ -124,3 +124,31 @@ def test_decode_attention_qwen8b_full_size_sampled(ops):
     ref = O.decode_attention_ref(codes["q"][0][pick], scales["q"][0], codes["k"][0][pick], scales["k"][0],
                                  codes["v"][0][pick], scales["v"][0], lens[pick])
     assert_gemm_close(bf16_to_np(out)[pick].reshape(-1, 128), ref.reshape(-1, 128), "attention qwen8b")
+
+
+def test_kv_cache_append_then_attend(ops):
+    """Three decode steps: each appends the new token's K/V rows at every
+    sequence's current length (one sequence already full: skipped), then
+    attends; the cache rows and the outputs against the oracle, the other
+    cache slots untouched."""
+    B, Hq, Hkv, T, D = 3, 8, 2, 64, 128
+    scales, codes = _setup(ops, B, Hq, Hkv, T, seed=11)
+    lens = np.array([10, 0, T])
+    kc_o, vc_o = codes["k"][0].copy(), codes["v"][0].copy()
+    kc_d, vc_d = codes["k"][1].clone(), codes["v"][1].clone()
+    for step in range(3):
+        kn = I.normal_bf16(I.stream(20 + step, 1), (B, Hkv, D))
+        vn = I.normal_bf16(I.stream(20 + step, 2), (B, Hkv, D))
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        ops.fp8_kv_cache_append(kn.cuda(), vn.cuda(), scales["k"][1], scales["v"][1], lens_d, kc_d, vc_d)
+        for b in range(B):
+            if lens[b] < T:
+                kc_o[b, :, lens[b]] = O.quant_with_scale(bf16_to_np(kn[b]), scales["k"][0])
+                vc_o[b, :, lens[b]] = O.quant_with_scale(bf16_to_np(vn[b]), scales["v"][0])
+        lens = np.minimum(lens + 1, T)
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        out = ops.decode_attention(codes["q"][1], scales["q"][1], kc_d, scales["k"][1], vc_d, scales["v"][1], lens_d)
+        _sync_ok(ops)
+        assert np.array_equal(kc_d.cpu().numpy(), kc_o) and np.array_equal(vc_d.cpu().numpy(), vc_o)
+        ref = O.decode_attention_ref(codes["q"][0], scales["q"][0], kc_o, scales["k"][0], vc_o, scales["v"][0], lens)
+        assert_gemm_close(bf16_to_np(out).reshape(-1, D), ref.reshape(-1, D), f"append step {step}")
