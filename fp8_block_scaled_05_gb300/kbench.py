@@ -26,7 +26,8 @@ from .timing import L2Flush
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", required=True,
-                   choices=["quant_act", "quant_weight", "gemm", "grouped", "quant_act_t", "quant_weight_t", "wgrad"])
+                   choices=["quant_act", "quant_weight", "gemm", "grouped", "quant_act_t", "quant_weight_t", "wgrad",
+                            "pt_gemm", "attention"])
     p.add_argument("--dual", action="store_true", help="quant_act_t / quant_weight_t: also the other layout")
     p.add_argument("--M", type=int, default=4096)
     p.add_argument("--N", type=int, default=4096)
@@ -84,6 +85,27 @@ def main(argv=None):
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         run = lambda: ops.wgrad(qa, sa, qb, sb, a.pow2, a.path, out=c)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif a.kernel == "pt_gemm":
+        # per-tensor scaled GEMM (one scale per operand)
+        qa, sa = ops.quant_tensor(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16))
+        qw, sw = ops.quant_tensor((torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16))
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        run = lambda: ops.gemm_tensor(qa, sa, qw, sw, out=c)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif a.kernel == "attention":
+        # decode attention over an FP8 KV cache: M sequences, N query heads
+        # (N / 4 KV heads), K cached tokens each, D = 128
+        B, Hq, T, D = M, N, K, 128
+        Hkv = max(1, Hq // 4)
+        kv = torch.randn((B * Hkv * T, D), generator=g, device=dev).to(torch.bfloat16)
+        kc, ssk = ops.quant_tensor(kv)
+        del kv
+        vc = kc.flip(0).contiguous()
+        qc, ssq = ops.quant_tensor(torch.randn((B * Hq, D), generator=g, device=dev).to(torch.bfloat16))
+        lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+        kc4, vc4, qc3 = kc.view(B, Hkv, T, D), vc.view(B, Hkv, T, D), qc.view(B, Hq, D)
+        run = lambda: ops.decode_attention(qc3, ssq, kc4, ssk, vc4, ssk, lens)  # noqa: E731
+        work, unit = 2.0 * B * Hkv * T * D + 3.0 * B * Hq * D, "GB/s"
     elif a.kernel == "gemm":
         qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
         qw, sw = ops.quant_weight((torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16), a.pow2)
