@@ -34,7 +34,7 @@ reference is dequantise-then-multiply in fp64.
 
 Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
 and (training-side functions) tests/test_oracle_pins_training.py, (per-tensor
-scaling) tests/test_oracle_pins_per_tensor.py, (KV-cache attention)
+scaling and UE8M0 scale bytes) tests/test_oracle_pins_per_tensor.py, (KV-cache attention)
 tests/test_oracle_pins_attention.py against
 facts that do not come from this file (the OCP code table, library
 casts, exact rational arithmetic, brute force, PyTorch autograd and closed
@@ -59,6 +59,7 @@ __all__ = [
     "dgrad_ref", "wgrad_ref", "wgrad_ref_rows",
     "quant_per_tensor", "gemm_per_tensor_ref",
     "quant_with_scale", "decode_attention_ref",
+    "scale_to_ue8m0", "ue8m0_to_scale",
 ]
 
 
@@ -415,3 +416,26 @@ def decode_attention_ref(q, sq, k_cache, sk, v_cache, sv, seq_lens) -> np.ndarra
             p = np.exp(scores - scores.max())
             out[b, h] = (p / p.sum()) @ vd
     return out
+
+
+# --------------------------------------------------------------------------
+# Power-of-two scales stored as UE8M0 bytes
+#
+# A power-of-two scale 2^e (e in [-127, 127], the power-of-two rule above)
+# needs only its exponent.  The byte format is UE8M0 of the OCP Microscaling
+# (MX) specification v1.0: 8 exponent bits, bias 127, no sign or mantissa,
+# 0xFF reserved for NaN; byte b means 2^(b - 127).
+# --------------------------------------------------------------------------
+def scale_to_ue8m0(s) -> np.ndarray:
+    """Byte e + 127 of each power-of-two scale 2^e (ValueError otherwise)."""
+    s = np.asarray(s, dtype=np.float64)
+    e = np.log2(s)
+    if not np.all(np.isfinite(e)) or not np.array_equal(e, np.round(e)) or np.any(np.abs(e) > 127):
+        raise ValueError("not a power of two in [2^-127, 2^127]")
+    return (np.round(e).astype(np.int64) + 127).astype(np.uint8)
+
+
+def ue8m0_to_scale(b) -> np.ndarray:
+    """2^(b - 127) as float32 (b < 255)."""
+    b = np.asarray(b, dtype=np.int64)
+    return np.ldexp(np.float64(1.0), b - 127).astype(np.float32)

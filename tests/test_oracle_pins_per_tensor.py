@@ -157,3 +157,36 @@ def test_mutant_per_tensor_quantisers_are_caught(mutant):
 
 def test_mutant_per_tensor_gemm_is_caught():
     assert not check_per_tensor_gemm(_gemm_one_scale)
+
+
+# ---------------------------------------------------------------- UE8M0 scale bytes
+def test_ue8m0_landmarks():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "ue8m0_ocp_mx_landmarks.txt")
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        b, v = line.split()
+        assert float(O.ue8m0_to_scale(int(b, 16))) == float(v)
+        assert int(O.scale_to_ue8m0(np.float32(float(v)))) == int(b, 16)
+
+
+def test_ue8m0_roundtrip_of_every_pow2_scale():
+    # every exponent the power-of-two rule can produce, and the scales that
+    # rule gives for a sweep of amax values
+    e = np.arange(-127, 128)
+    s = np.ldexp(np.float64(1.0), e).astype(np.float32)
+    b = O.scale_to_ue8m0(s)
+    assert np.array_equal(b.astype(np.int64), e + 127)
+    assert np.array_equal(O.ue8m0_to_scale(b), s)
+    amax = np.exp2(np.arange(-140, 127, 0.37)).astype(np.float32)      # all finite in float32
+    sp = O.scale_from_amax_pow2(amax[amax > 0])
+    assert np.array_equal(O.ue8m0_to_scale(O.scale_to_ue8m0(sp)), sp)
+
+
+def test_ue8m0_rejects_non_powers_of_two():
+    with pytest.raises(ValueError):
+        O.scale_to_ue8m0(np.float32(0.75))
+    with pytest.raises(ValueError):
+        O.scale_to_ue8m0(np.float32(2.0 ** -130))
