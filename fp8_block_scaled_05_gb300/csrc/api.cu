@@ -130,7 +130,7 @@ fp8_status tensor_map(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, u
 
 fp8_status check_mode(int mode) { return (mode == FP8_SCALE_FP32_AMAX || mode == FP8_SCALE_POW2) ? FP8_OK : FP8_ERR_SCALE_MODE; }
 
-constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_MASK;
+constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_SCALES_E8 | FP8_GEMM_PATH_MASK;
 
 // Path of a dense GEMM: the one forced by the flags, else the skinny kernel
 // for M <= 256, else the MX kernel when the caller promises power-of-two
@@ -138,6 +138,7 @@ constexpr uint32_t kKnownFlags = FP8_GEMM_SCALES_POW2 | FP8_GEMM_PATH_MASK;
 uint32_t plan_path(int64_t M, int64_t K, uint32_t flags) {
     const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
     if (forced != FP8_GEMM_PATH_AUTO) return forced;
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_GEMM_PATH_MX;   // byte scales: the MX kernel reads them
     if (M <= 256 && K <= 128 * 1024) return FP8_GEMM_PATH_SKINNY;
     return (flags & FP8_GEMM_SCALES_POW2) ? FP8_GEMM_PATH_MX : FP8_GEMM_PATH_PROMOTE;
 }
@@ -146,6 +147,7 @@ uint32_t plan_path(int64_t M, int64_t K, uint32_t flags) {
 uint32_t grouped_path(uint32_t flags) {
     const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
     if (forced != FP8_GEMM_PATH_AUTO) return forced;
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_GEMM_PATH_MX;
     return (flags & FP8_GEMM_SCALES_POW2) ? FP8_GEMM_PATH_MX : FP8_GEMM_PATH_PROMOTE;
 }
 
@@ -158,7 +160,7 @@ fp8_status check_gemm_common(const void* qa, int64_t lda, const float* sa, int64
     if (flags & ~kKnownFlags) return FP8_ERR_SCALE_MODE;
     const uint32_t path = flags & FP8_GEMM_PATH_MASK;
     if (path > FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
-    if (path == FP8_GEMM_PATH_MX && !(flags & FP8_GEMM_SCALES_POW2)) return FP8_ERR_SCALE_MODE;
+    if (path == FP8_GEMM_PATH_MX && !(flags & (FP8_GEMM_SCALES_POW2 | FP8_GEMM_SCALES_E8))) return FP8_ERR_SCALE_MODE;
     if (M == 0) return FP8_OK;
     if (!qa || !sa || !qb || !sb || !c) return FP8_ERR_NULL;
     if (lda < K || ldc < N || ldsa < M) return FP8_ERR_SHAPE;
@@ -223,13 +225,39 @@ fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_quant_act_1x128_e8(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                  uint8_t* s, int64_t lds, fp8_stream_t stream) {
+    if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 31) - 1 || K > (1ll << 26)) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x || !q || !s) return FP8_ERR_NULL;
+    if (ldx < K || ldq < K || lds < M) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldq % 16) || (lds % 4) || !aligned16(x) || !aligned16(q)) return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_act_1x128(x, M, K, ldx, q, ldq, nullptr, lds, true,
+                                              reinterpret_cast<cudaStream_t>(stream), s));
+}
+
+fp8_status fp8_quant_weight_128x128_e8(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                                       uint8_t* s, fp8_stream_t stream) {
+    if (N <= 0 || K <= 0 || (N % 128) || (K % 128) || N / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (!w || !q || !s) return FP8_ERR_NULL;
+    if (ldw < K || ldq < K) return FP8_ERR_SHAPE;
+    if ((ldw % 8) || (ldq % 16) || !aligned16(w) || !aligned16(q)) return FP8_ERR_ALIGN;   // s: bytes, any address
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_weight_128x128(w, N, K, ldw, q, ldq, nullptr, true,
+                                                   reinterpret_cast<cudaStream_t>(stream), s));
+}
+
 fp8_status fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
                                     float* s, fp8_scale_mode mode, fp8_stream_t stream) {
     if (fp8_status e = check_mode(mode)) return e;
     if (N <= 0 || K <= 0 || (N % 128) || (K % 128) || N / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
     if (!w || !q || !s) return FP8_ERR_NULL;
     if (ldw < K || ldq < K) return FP8_ERR_SHAPE;
-    if ((ldw % 8) || (ldq % 16) || !aligned16(w) || !aligned16(q) || !aligned16(s)) return FP8_ERR_ALIGN;
+    if ((ldw % 8) || (ldq % 16) || !aligned16(w) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s) % 4))
+        return FP8_ERR_ALIGN;
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
     return cuda_status(launch_quant_weight_128x128(w, N, K, ldw, q, ldq, s, mode == FP8_SCALE_POW2,
@@ -383,6 +411,7 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     if (ldb < K) return FP8_ERR_SHAPE;
     if (ldb % 16) return FP8_ERR_ALIGN;
     const uint32_t path = plan_path(M, K, flags);
+    if ((flags & FP8_GEMM_SCALES_E8) && path != FP8_GEMM_PATH_MX) return FP8_ERR_NOT_IMPLEMENTED;
     if (path == FP8_GEMM_PATH_SKINNY && (M > 256 || K / 128 > 1024)) return FP8_ERR_SHAPE;
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
@@ -419,6 +448,7 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         return cuda_status(launch_gemm_skinny(a, st));
     }
     const bool mx = path == FP8_GEMM_PATH_MX;
+    a.scales_e8 = (flags & FP8_GEMM_SCALES_E8) ? 1 : 0;
     a.bn = mx ? kMxTileN : promote_tile_n(M, N, K, 1);
     if (workspace && aligned16(workspace)) {
         // optional: lets the kernel split its last wave of tiles
@@ -441,6 +471,7 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
                                       const uint8_t* qb, int64_t ldb, const float* sb, int64_t ldsb, void* c,
                                       int64_t ldc, int64_t M, int64_t N, int64_t K, uint32_t flags, void* workspace,
                                       size_t ws_bytes, fp8_stream_t stream) {
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_ERR_NOT_IMPLEMENTED;   // fp32 scales only
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M, N, K, flags)) return e;
     const uint32_t forced = flags & FP8_GEMM_PATH_MASK;
     if (forced == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
@@ -487,6 +518,7 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
 fp8_status fp8_tensorscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, const uint8_t* qb, int64_t ldb,
                                  const float* sb, void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                  uint32_t flags, void* workspace, size_t ws_bytes, fp8_stream_t stream) {
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_ERR_SCALE_MODE;   // one fp32 scale per operand
     // the block-scaled validation with the one-scale pointers standing in for
     // the scale arrays (ldsa = M keeps its pitch rule satisfied)
     if (fp8_status e = check_gemm_common(qa, lda, sa, M > 0 ? ((M + 3) / 4) * 4 : 0, qb, sb, c, ldc, M, N, K,
@@ -536,6 +568,7 @@ fp8_status fp8_blockscaled_gemm_quant(const uint8_t* qa, int64_t lda, const floa
                                       float* sc, int64_t ldsc, int64_t M, int64_t N, int64_t K, uint32_t flags,
                                       fp8_scale_mode out_mode, void* workspace, size_t ws_bytes,
                                       fp8_stream_t stream) {
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_ERR_NOT_IMPLEMENTED;   // fp32 scales only
     if (fp8_status e = check_mode(out_mode)) return e;
     // c is optional here: validate with the codes standing in for it
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c ? c : static_cast<const void*>(qc),
@@ -605,6 +638,7 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M_total, N, K, flags)) return e;
     const uint32_t path = grouped_path(flags);
     if (path == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    if ((flags & FP8_GEMM_SCALES_E8) && path != FP8_GEMM_PATH_MX) return FP8_ERR_NOT_IMPLEMENTED;
     if (M_total == 0) return FP8_OK;
     if (!offsets) return FP8_ERR_NULL;
     if ((int64_t)G * N > INT32_MAX) return FP8_ERR_SHAPE;
@@ -625,6 +659,7 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     a.sm_count = d->sm_count;
     a.splits = 1;
     const bool mx = path == FP8_GEMM_PATH_MX;
+    a.scales_e8 = (flags & FP8_GEMM_SCALES_E8) ? 1 : 0;
     a.bn = mx ? kMxTileN : promote_tile_n(M_total, N, K, G);
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M_total, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))

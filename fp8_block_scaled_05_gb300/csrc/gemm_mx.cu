@@ -137,13 +137,22 @@ __device__ __forceinline__ uint32_t ue8m0(float s, bool& bad) {
 // (per-tensor scaling).  The scale factors are then 2^0 (the block-scaled MMA
 // is a plain FP8 MMA with fp32 accumulation over all of K) and the epilogue
 // multiplies by RN(sa * sb) once.
+// Element i of a scale array: fp32, or (e8) a UE8M0 byte widened to the fp32
+// power of two it stands for (byte 0 is 2^-127, a subnormal; 255 becomes inf
+// and is reported by ue8m0 below).
+__device__ __forceinline__ float scale_at(const float* __restrict__ p, size_t i, int e8) {
+    if (!e8) return p[i];
+    const uint32_t b = reinterpret_cast<const uint8_t*>(p)[i];
+    return __uint_as_float(b == 0u ? 0x00400000u : b << 23);
+}
+
 template <bool GROUPED, bool PER_TENSOR = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
               const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
               uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G,
-              int* status, SplitTail split, QuantOut qo) {
+              int* status, SplitTail split, QuantOut qo, int e8) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
@@ -289,16 +298,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int m = tl.m0 + q * 32 + lane;
             const bool vrow = m < tl.row_end;
             const int nb0 = tl.n0 / 128;
-            const float* sb0 = sb + ((size_t)tl.g * NB + nb0) * KB;
+            const size_t sb0 = ((size_t)tl.g * NB + nb0) * KB;   // index of the tile's first B scale
             for (int kb0 = w.kb0; kb0 < w.kb1; kb0 += KB_PER_SF, ++gi) {
                 // Scales first (their latency overlaps the wait for the slot).
                 float fa[KB_PER_SF], fb0[KB_PER_SF], fb1[KB_PER_SF];
 #pragma unroll
                 for (int j = 0; j < KB_PER_SF; ++j) {
                     const int kb = kb0 + j;
-                    fa[j] = (!PER_TENSOR && kb < w.kb1 && vrow) ? sa[(size_t)kb * ldsa + m] : 1.0f;
-                    fb0[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0) ? sb0[kb] : 1.0f;
-                    fb1[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0 && nb0 + 1 < NB) ? sb0[KB + kb] : 1.0f;
+                    fa[j] = (!PER_TENSOR && kb < w.kb1 && vrow) ? scale_at(sa, (size_t)kb * ldsa + m, e8) : 1.0f;
+                    fb0[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0) ? scale_at(sb, sb0 + kb, e8) : 1.0f;
+                    fb1[j] = (!PER_TENSOR && kb < w.kb1 && ldsb == 0 && nb0 + 1 < NB) ? scale_at(sb, sb0 + KB + kb, e8)
+                                                                                        : 1.0f;
                 }
                 uint32_t wa = 0, wb0 = 0, wb1 = 0;
 #pragma unroll
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < KB_PER_SF; ++i) {
                             const int kb = kb0 + i;
-                            const float f = (kb < w.kb1 && n < N) ? sb[(size_t)kb * ldsb + n] : 1.0f;
+                            const float f = (kb < w.kb1 && n < N) ? scale_at(sb, (size_t)kb * ldsb + n, e8) : 1.0f;
                             wj |= ue8m0(f, bad) << (8 * i);
                         }
                         vb[j] = wj;
@@ -547,7 +557,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         }
     }
     kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, a.ldsb, static_cast<uint16_t*>(a.c), a.ldc,
-                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout);
+                                            (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout,
+                                            a.scales_e8);
     return cudaGetLastError();
 }
 

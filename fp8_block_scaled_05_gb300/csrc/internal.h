@@ -66,10 +66,11 @@ struct DeviceInfo {
 };
 
 // ------------------------------------------------------------- quantisers
+// s8 != nullptr: power-of-two scales written as UE8M0 bytes there (s unused).
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
-                                   float* s, int64_t lds, bool pow2, cudaStream_t st);
+                                   float* s, int64_t lds, bool pow2, cudaStream_t st, uint8_t* s8 = nullptr);
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                        int64_t ldq, float* s, bool pow2, cudaStream_t st);
+                                        int64_t ldq, float* s, bool pow2, cudaStream_t st, uint8_t* s8 = nullptr);
 
 // Transposing quantisers (training-side GEMM operands).  q == nullptr: the
 // non-transposed codes and scales are not written.
@@ -120,6 +121,7 @@ struct GemmArgs {
     int64_t ldsa;
     const float* sb;
     int per_tensor;                 // MX only: sa, sb point at one scale each (per-tensor scaling)
+    int scales_e8;                  // MX only: sa, sb hold UE8M0 bytes (same indices as the fp32 arrays)
     int64_t ldsb;                   // 0: sb holds 128x128 block scales [G][N/128][K/128];
                                     // > 0: a scale per B row, sb[kb * ldsb + n] (dense promote / MX)
     void* c;

@@ -42,7 +42,8 @@ static_assert(kActItems <= 16 && (kActItems & (kActItems - 1)) == 0, "items per 
 template <bool POW2>
 __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
                                                             int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
-                                                            float* __restrict__ s, int64_t lds) {
+                                                            float* __restrict__ s, int64_t lds,
+                                                            uint8_t* __restrict__ s8) {
     __shared__ float s_tile[kActKB][kActRows];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const int64_t m0 = (int64_t)blockIdx.x * kActRows;
@@ -106,19 +107,27 @@ __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __re
     if (threadIdx.x < kActKB * kActRows) {
         const int kbl = threadIdx.x / kActRows, rl = threadIdx.x % kActRows;
         const int64_t kb = kb0 + kbl, m = m0 + rl;
-        if (kb < KB && m < M) s[kb * lds + m] = s_tile[kbl][rl];
+        if (kb < KB && m < M) {
+            // s8: UE8M0 bytes (power-of-two scales): the fp32 exponent field,
+            // which is also right for 2^-127 (stored as a subnormal)
+            if (s8 != nullptr)
+                s8[kb * lds + m] = (uint8_t)(__float_as_uint(s_tile[kbl][rl]) >> 23);
+            else
+                s[kb * lds + m] = s_tile[kbl][rl];
+        }
     }
 }
 
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
-                                   float* s, int64_t lds, bool pow2, cudaStream_t st) {
+                                   float* s, int64_t lds, bool pow2, cudaStream_t st, uint8_t* s8) {
     if (M == 0) return cudaSuccess;
     const int64_t KB = K / 128;
     dim3 grid((unsigned)((M + kActRows - 1) / kActRows), (unsigned)((KB + kActKB - 1) / kActKB));
     auto kern = pow2 ? k_quant_act_1x128<true> : k_quant_act_1x128<false>;
     if (pdl_for_tokens(M))   // a decode step: overlap with the kernels around it
-        return launch_pdl(kern, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds);
-    kern<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds);
+        return launch_pdl(kern, grid, dim3(256), 0, st, static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds,
+                          s8);
+    kern<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, s, lds, s8);
     return cudaGetLastError();
 }
 
@@ -129,7 +138,7 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
                                                          uint8_t* __restrict__ q, int64_t ldq,
-                                                         float* __restrict__ s, int pow2) {
+                                                         float* __restrict__ s, int pow2, uint8_t* __restrict__ s8) {
     __shared__ float s_red[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const int64_t kb = blockIdx.x, nb = blockIdx.y;
@@ -155,14 +164,19 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restr
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         __stcs(reinterpret_cast<uint2*>(q + (row0 + 2 * i) * ldq + col), quant8(v[i], bs));
-    if (threadIdx.x == 0) s[nb * KB + kb] = bs.s;
+    if (threadIdx.x == 0) {
+        if (s8 != nullptr)
+            s8[nb * KB + kb] = (uint8_t)(__float_as_uint(bs.s) >> 23);   // UE8M0 byte of a power of two
+        else
+            s[nb * KB + kb] = bs.s;
+    }
 }
 
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                        int64_t ldq, float* s, bool pow2, cudaStream_t st) {
+                                        int64_t ldq, float* s, bool pow2, cudaStream_t st, uint8_t* s8) {
     const int64_t KB = K / 128, NB = N / 128;
     dim3 grid((unsigned)KB, (unsigned)NB);
-    k_quant_w_128x128<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(w), KB, ldw, q, ldq, s, pow2 ? 1 : 0);
+    k_quant_w_128x128<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(w), KB, ldw, q, ldq, s, pow2 ? 1 : 0, s8);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@ STATUS_NAMES = {
 FP8_SCALE_FP32_AMAX = 0
 FP8_SCALE_POW2 = 1
 FP8_GEMM_SCALES_POW2 = 0x1
+FP8_GEMM_SCALES_E8 = 0x2
 FP8_GEMM_PATH_AUTO = 0x00
 FP8_GEMM_PATH_PROMOTE = 0x10
 FP8_GEMM_PATH_MX = 0x20
@@ -55,6 +56,8 @@ SIGNATURES = {
                                                   ctypes.c_int, _vp]),
     "fp8_blockscaled_gemm_wgrad": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64,
                                                   _i64, _i64, _u32, _vp, _sz, _vp]),
+    "fp8_quant_act_1x128_e8": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "fp8_quant_weight_128x128_e8": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]),
     "fp8_quant_per_tensor": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, ctypes.c_int, _vp]),
     "fp8_tensorscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _u32,
                                              _vp, _sz, _vp]),
@@ -213,6 +216,28 @@ def fp8_blockscaled_gemm_wgrad(qa, sa, qb, sb, c, flags: int = 0, workspace: tor
            "fp8_blockscaled_gemm_wgrad")
 
 
+def fp8_quant_act_1x128_e8(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
+    """Power-of-two 1x128 quantisation with UE8M0 scale bytes: s uint8 [K/128, lds >= M]."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    M, K = x.shape
+    _check(lib().fp8_quant_act_1x128_e8(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), s.stride(0),
+                                        _stream(stream)), "fp8_quant_act_1x128_e8")
+
+
+def fp8_quant_weight_128x128_e8(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
+    """Power-of-two 128x128 quantisation with UE8M0 scale bytes: s uint8 [N/128, K/128] contiguous."""
+    _need(w, torch.bfloat16, "w")
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    if not s.is_contiguous():
+        raise ValueError("s must be contiguous")
+    N, K = w.shape
+    _check(lib().fp8_quant_weight_128x128_e8(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(s),
+                                             _stream(stream)), "fp8_quant_weight_128x128_e8")
+
+
 def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor, scale_amax: torch.Tensor,
                          mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
     """x bf16 [M, K]; q uint8 [M, K]; scale_amax fp32 [2] (scale, amax) on the device."""
@@ -292,11 +317,13 @@ def fp8_tensorscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Te
 
 def fp8_blockscaled_gemm(qa, sa, qb, sb, c, flags: int = 0, workspace: torch.Tensor | None = None,
                          stream=None) -> None:
-    """C[M, N] (bf16) = block-scaled qa[M, K] * qb[N, K]^T."""
+    """C[M, N] (bf16) = block-scaled qa[M, K] * qb[N, K]^T (sa, sb uint8 UE8M0
+    bytes with FP8_GEMM_SCALES_E8, else fp32)."""
+    sdt = torch.uint8 if flags & FP8_GEMM_SCALES_E8 else torch.float32
     _need(qa, torch.uint8, "qa")
     _need(qb, torch.uint8, "qb")
-    _need(sa, torch.float32, "sa")
-    _need(sb, torch.float32, "sb")
+    _need(sa, sdt, "sa")
+    _need(sb, sdt, "sb")
     _need(c, torch.bfloat16, "c")
     M, K = qa.shape
     N = qb.shape[0]
@@ -331,11 +358,13 @@ def fp8_blockscaled_gemm_quant(qa, sa, qb, sb, c, qc, sc, flags: int = 0, out_mo
 
 def fp8_blockscaled_grouped_gemm(qa, sa, offsets, qb, sb, c, flags: int = 0,
                                  workspace: torch.Tensor | None = None, stream=None) -> None:
-    """Per-expert GEMM; offsets int32 [G+1] on the device; qb uint8 [G, N, K]."""
+    """Per-expert GEMM; offsets int32 [G+1] on the device; qb uint8 [G, N, K]
+    (sa, sb uint8 UE8M0 bytes with FP8_GEMM_SCALES_E8, else fp32)."""
+    sdt = torch.uint8 if flags & FP8_GEMM_SCALES_E8 else torch.float32
     _need(qa, torch.uint8, "qa")
     _need(qb, torch.uint8, "qb")
-    _need(sa, torch.float32, "sa")
-    _need(sb, torch.float32, "sb")
+    _need(sa, sdt, "sa")
+    _need(sb, sdt, "sb")
     _need(c, torch.bfloat16, "c")
     _need(offsets, torch.int32, "offsets")
     if not (qb.is_contiguous() and sb.is_contiguous() and offsets.is_contiguous()):

@@ -76,6 +76,9 @@ typedef enum {
 #define FP8_GEMM_SCALES_POW2   0x1u  /* caller promises every sA, sB is an exact power of two
                                         in [2^-127, 2^127] (as FP8_SCALE_POW2 produces); lets the
                                         hardware block-scaled (UE8M0) path run */
+#define FP8_GEMM_SCALES_E8     0x2u  /* sA and sB are UE8M0 bytes (2^(b-127), as the _e8 quantisers
+                                        write them) at the indices of the fp32 arrays; MX path only
+                                        (AUTO picks it; PROMOTE and SKINNY return NOT_IMPLEMENTED) */
 #define FP8_GEMM_PATH_MASK     0xF0u /* kernel selection; 0 = automatic */
 #define FP8_GEMM_PATH_AUTO     0x00u
 #define FP8_GEMM_PATH_PROMOTE  0x10u /* large-M kernel, fp32 scale promotion per K-block */
@@ -102,6 +105,28 @@ FP8BS_API fp8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, in
                                fp8_scale_mode mode, fp8_stream_t stream);
 
 /*
+ * 1x128 activation quantisation with power-of-two scales stored as UE8M0
+ * bytes (OCP Microscaling E8M0: byte b means 2^(b - 127)): the codes are
+ * those of fp8_quant_act_1x128(..., FP8_SCALE_POW2) and s[kb * lds + m] is the
+ * byte of the scale that call writes as fp32 -- a quarter of the scale bytes,
+ * in the form the MX GEMM path takes (FP8_GEMM_SCALES_E8).
+ * s  device, uint8 [K/128][lds] (lds >= M, lds % 4 == 0; any address);
+ * everything else as fp8_quant_act_1x128.
+ */
+FP8BS_API fp8_status fp8_quant_act_1x128_e8(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                            uint8_t *q, int64_t ldq, uint8_t *s, int64_t lds,
+                                            fp8_stream_t stream);
+
+/*
+ * 128x128 weight quantisation with power-of-two scales stored as UE8M0 bytes:
+ * codes as fp8_quant_weight_128x128(..., FP8_SCALE_POW2), s uint8 [N/128][K/128]
+ * (contiguous, any address).
+ */
+FP8BS_API fp8_status fp8_quant_weight_128x128_e8(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                                 uint8_t *q, int64_t ldq, uint8_t *s,
+                                                 fp8_stream_t stream);
+
+/*
  * 128x128 weight quantisation (run after every optimizer step).
  *
  *   for every tile (nb, kb), nb < N/128, kb < K/128:
@@ -111,7 +136,8 @@ FP8BS_API fp8_status fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, in
  *
  * w   device, bf16 [N, K] row-major, row pitch ldw (>= K, ldw % 8 == 0, 16-byte aligned)
  * q   device, uint8 [N, K] row-major, row pitch ldq (>= K, ldq % 16 == 0, 16-byte aligned)
- * s   device, fp32 [N/128][K/128] row-major, contiguous, 16-byte aligned
+ * s   device, fp32 [N/128][K/128] row-major, contiguous, 4-byte aligned (so that
+ *     one expert's block of a [G][N/128][K/128] array can be passed)
  * N, K > 0, both multiples of 128.
  */
 FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,

@@ -298,6 +298,28 @@ def test_kv_cache_append_validation(L):
         assert f(A16, A16b, A16c, A16c, A16, A16b, A16c, 2, 8, 64, 128, NULL) == 6
 
 
+def test_e8_scales_validation(L):
+    qa = L.fp8_quant_act_1x128_e8
+    assert qa(NULL, 4, 256, 256, A16b, 256, A16c, 4, NULL) == 1
+    assert qa(A16, 4, 200, 256, A16b, 256, A16c, 4, NULL) == 2
+    assert qa(A16, 8, 256, 256, A16b, 256, A16c, 4, NULL) == 2      # lds < M
+    assert qa(A16, 4, 256, 256, MIS, 256, A16c, 4, NULL) == 3      # codes misaligned
+    qw = L.fp8_quant_weight_128x128_e8
+    assert qw(A16, 128, 200, 256, A16b, 256, A16c, NULL) == 2
+    assert qw(A16, 128, 256, 256, A16b, 256, NULL, NULL) == 1
+    g = L.fp8_blockscaled_gemm
+    args = (A16, 256, A16b, 8, A16c, 256, A16, A16b, 128, 8, 128, 256)
+    assert g(*args, 0x12, NULL, 0, NULL) == 9     # UE8M0 scales on the promote path
+    assert g(*args, 0x32, NULL, 0, NULL) == 9     # nor skinny
+    assert L.fp8_blockscaled_gemm_wgrad(A16, 256, A16b, 256, A16c, 256, A16, 128, A16b, 128, 256, 128, 256, 0x2,
+                                        NULL, 0, NULL) == 9
+    assert L.fp8_tensorscaled_gemm(A16, 256, A16b, A16c, 256, A16, A16b, 128, 8, 128, 256, 0x2, NULL, 0, NULL) == 4
+    if not _has_gpu():
+        assert qa(A16, 4, 256, 256, A16b, 256, A16c, 4, NULL) == 6
+        assert g(*args, 0x2, NULL, 0, NULL) == 6  # AUTO picks MX
+        assert g(*args, 0x22, NULL, 0, NULL) == 6
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0
