@@ -56,7 +56,7 @@ __all__ = [
     "dequant_act", "dequant_weight",
     "gemm_ref", "gemm_ref_rows", "grouped_gemm_ref",
     "block_amax_col", "quant_act_128x1", "quant_weight_128x128_t",
-    "dgrad_ref", "wgrad_ref", "wgrad_ref_rows",
+    "dgrad_ref", "wgrad_ref", "wgrad_ref_rows", "moe_wgrad_ref",
     "quant_per_tensor", "gemm_per_tensor_ref",
     "quant_with_scale", "decode_attention_ref",
     "scale_to_ue8m0", "ue8m0_to_scale",
@@ -297,10 +297,18 @@ def quant_act_128x1(x: np.ndarray, pow2: bool = False):
     x: float32 [M, K] (bf16 values), M tokens.  The block of column k, tokens
     mb*128 .. mb*128+127 gets scale s[mb, k] from its own amax, and
     q[m, k] = e4m3(x[m, k] / s[m/128, k]).  Returned transposed, the way the
-    wgrad GEMM reads them (token-contiguous rows): (qt uint8 [K, M] with
-    qt[k, m] = q[m, k], st float32 [K, M/128] with st[k, mb] = s[mb, k]).
+    wgrad GEMM reads them (token-contiguous rows): (qt uint8 [K, Mp] with
+    qt[k, m] = q[m, k], st float32 [K, Mp/128] with st[k, mb] = s[mb, k]).
+    A token count M that is not a multiple of 128 is padded with zero rows
+    to Mp (zero rows change no block's amax and add nothing to dW; their
+    codes are zero).
     """
     x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    if M % QBLOCK:
+        xp = np.zeros(((M + QBLOCK - 1) // QBLOCK * QBLOCK, K), np.float32)
+        xp[:M] = x
+        x = xp
     s = scale_from_amax(block_amax_col(x), pow2)
     q = _cast(x, np.repeat(s, QBLOCK, axis=0))
     return np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
@@ -336,6 +344,23 @@ def wgrad_ref(qt_dy, st_dy, qt_x, st_x) -> np.ndarray:
     qt_x uint8 [K, M] with st_x [K, M/128].
     """
     return dequant_act(qt_dy, st_dy) @ dequant_act(qt_x, st_x).T
+
+
+def moe_wgrad_ref(dy, x, offsets, pow2: bool = False) -> np.ndarray:
+    """Weight gradients of a mixture-of-experts layer: for each expert g,
+    dW_g = dY_g^T X_g over its token rows offsets[g] .. offsets[g+1]-1, each
+    operand quantised in 128x1 blocks of that expert's own tokens (the last
+    block zero-padded).  dy [T, N], x [T, K] float32; returns [G, N, K]."""
+    offsets = np.asarray(offsets, np.int64)
+    G = len(offsets) - 1
+    out = np.zeros((G, dy.shape[1], x.shape[1]), np.float64)
+    for g in range(G):
+        lo, hi = int(offsets[g]), int(offsets[g + 1])
+        if hi > lo:
+            qg, sg = quant_act_128x1(dy[lo:hi], pow2)
+            qx, sx = quant_act_128x1(x[lo:hi], pow2)
+            out[g] = wgrad_ref(qg, sg, qx, sx)
+    return out
 
 
 def wgrad_ref_rows(qt_dy, st_dy, qt_x, st_x, rows) -> np.ndarray:

@@ -82,6 +82,39 @@ def test_col_quant_is_row_quant_of_the_transpose():
         assert np.array_equal(qt, q1) and np.array_equal(st, s1)
 
 
+def test_col_quant_ragged_tokens_pad_with_zeros():
+    # 300 tokens: the last block holds 44 real rows; its scales and codes are
+    # those of the block padded with zero rows, and the pad codes are zero.
+    x = _col_sample(seed=34, M=384, K=40)
+    x[300:] = 0.0
+    qt, st = O.quant_act_128x1(x[:300])
+    qt_full, st_full = O.quant_act_128x1(x)
+    assert qt.shape == (40, 384) and np.array_equal(qt, qt_full) and np.array_equal(st, st_full)
+    assert np.all(qt[:, 300:] == 0)
+
+
+def test_moe_wgrad_is_per_expert_wgrad_and_autograd():
+    """Per expert: dL/dW_g of L = sum_g sum(G_g * (X_g W_g^T)) on the
+    dequantised (zero-padded) operands, by PyTorch autograd; an empty expert
+    gets zeros."""
+    rng = np.random.Generator(np.random.PCG64(40))
+    offs = [0, 70, 70, 300]
+    N, K = 128, 256
+    x = _bf16_round(rng.standard_normal((300, K)).astype(np.float32))
+    dy = _bf16_round((rng.standard_normal((300, N)) * 1e-3).astype(np.float32))
+    got = O.moe_wgrad_ref(dy, x, offs)
+    assert got.shape == (3, N, K) and np.all(got[1] == 0)
+    for g in (0, 2):
+        lo, hi = offs[g], offs[g + 1]
+        qg, sg = O.quant_act_128x1(dy[lo:hi])
+        qx, sx = O.quant_act_128x1(x[lo:hi])
+        Gc = _deq(qg, sg).T.contiguous()
+        Xc = _deq(qx, sx).T.contiguous()
+        W = torch.zeros((N, K), dtype=torch.float64, requires_grad=True)
+        (Gc * (Xc @ W.T)).sum().backward()
+        assert np.max(np.abs(got[g] - W.grad.numpy())) <= 1e-12 * np.max(np.abs(got[g]))
+
+
 # ---------------------------------------------------------------- W^T operand
 def test_weight_t_is_quantisation_of_the_transpose():
     # Quantising W^T directly (its own 128x128 blocks) gives the same codes
