@@ -268,11 +268,12 @@ fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                                float* st, int64_t ldst, uint8_t* q, int64_t ldq, float* s, int64_t lds,
                                fp8_scale_mode mode, fp8_stream_t stream) {
     if (fp8_status e = check_mode(mode)) return e;
-    if (M < 0 || K <= 0 || (M % 128) || (K % 128) || M / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
+    if (M < 0 || K <= 0 || (K % 128) || (M + 127) / 128 > 65535 || K > (1ll << 30)) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
     if (!x || !qt || !st) return FP8_ERR_NULL;
     if ((q == nullptr) != (s == nullptr)) return FP8_ERR_NULL;   // the 1x128 outputs come as a pair
-    if (ldx < K || ldqt < M || ldst < K) return FP8_ERR_SHAPE;
+    const int64_t Mp = (M + 127) / 128 * 128;                    // tokens padded to whole 128x1 blocks
+    if (ldx < K || ldqt < Mp || ldst < K) return FP8_ERR_SHAPE;
     if ((ldx % 8) || (ldqt % 16) || (ldst % 4) || !aligned16(x) || !aligned16(qt) || !aligned16(st))
         return FP8_ERR_ALIGN;
     if (q != nullptr) {

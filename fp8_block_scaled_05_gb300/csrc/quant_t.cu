@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
                                                          uint8_t *__restrict__ qt, int64_t ldqt,
                                                          float *__restrict__ st, int64_t ldst,
                                                          uint8_t *__restrict__ q, int64_t ldq,
-                                                         float *__restrict__ s, int64_t lds) {
+                                                         float *__restrict__ s, int64_t lds, int64_t M) {
     __shared__ __align__(16) uint8_t tcodes[kTT * kTT];
     __shared__ __align__(16) uint32_t colpart[8][16][4];   // per warp: packed |bf16| maxima of column pairs
     __shared__ float2 colscale[kTT];
@@ -133,10 +133,14 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
     const int cg = lane & 15, rg = 2 * warp + (lane >> 4);
     const int64_t k0 = (int64_t)blockIdx.x * kTT, m0 = (int64_t)blockIdx.y * kTT;
 
+    // rows past M (a ragged last token block) are zeros: they change no
+    // block's amax and their transposed codes are zero
     uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v[i] = __ldcs(reinterpret_cast<const uint4 *>(x + (m0 + 8 * rg + i) * ldx + k0 + 8 * cg));
+    for (int i = 0; i < 8; ++i) {
+        const int64_t m = m0 + 8 * rg + i;
+        v[i] = m < M ? __ldcs(reinterpret_cast<const uint4 *>(x + m * ldx + k0 + 8 * cg)) : make_uint4(0, 0, 0, 0);
+    }
 
     // column maxima over the thread's rows, then over the warp's two halves
     uint32_t cm[4] = {0u, 0u, 0u, 0u};
@@ -171,14 +175,15 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
             }
         }
         const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
-        if (cg < 8) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
+        if (cg < 8 && m0 + 8 * rg + cg < M) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int src = (lane & 16) | i;
             const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
             const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
-            __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
-                   POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
+            if (m0 + 8 * rg + i < M)
+                __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
+                       POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
         }
     }
     __syncthreads();
@@ -255,11 +260,11 @@ cudaError_t launch_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t 
                                    float *st, int64_t ldst, uint8_t *q, int64_t ldq, float *s, int64_t lds,
                                    bool pow2, cudaStream_t stream) {
     if (M == 0) return cudaSuccess;
-    const dim3 grid((unsigned)(K / kTT), (unsigned)(M / kTT));
+    const dim3 grid((unsigned)(K / kTT), (unsigned)((M + kTT - 1) / kTT));   // last token block padded with zeros
     const uint16_t *xp = static_cast<const uint16_t *>(x);
     auto kern = q != nullptr ? (pow2 ? k_quant_act_128x1<true, true> : k_quant_act_128x1<true, false>)
                              : (pow2 ? k_quant_act_128x1<false, true> : k_quant_act_128x1<false, false>);
-    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds);
+    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds, M);
     return cudaGetLastError();
 }
 

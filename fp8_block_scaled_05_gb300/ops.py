@@ -432,12 +432,14 @@ def quant_weight(w: torch.Tensor, pow2: bool = False, stream=None):
 
 
 def quant_act_t(x: torch.Tensor, pow2: bool = False, rowwise: bool = False, stream=None):
-    """128x1 quantisation of x [M, K] (M % 128 == 0), transposed: returns
-    (qt uint8 [K, M], st fp32 [M/128, round_up(K, 4)]), and with rowwise=True
-    also (q, s) as quant_act(x) returns them, from the same pass."""
+    """128x1 quantisation of x [M, K], transposed: returns (qt uint8 [K, Mp],
+    st fp32 [Mp/128, round_up(K, 4)]) with Mp = M rounded up to 128 (the pad
+    tokens are zeros), and with rowwise=True also (q, s) as quant_act(x)
+    returns them, from the same pass."""
     M, K = x.shape
-    qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
-    st = torch.empty((M // 128, max(round_up(K, 4), 4)), dtype=torch.float32, device=x.device)
+    Mp = round_up(M, 128)
+    qt = torch.empty((K, Mp), dtype=torch.uint8, device=x.device)
+    st = torch.empty((Mp // 128, max(round_up(K, 4), 4)), dtype=torch.float32, device=x.device)
     q = s = None
     if rowwise:
         q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
@@ -557,6 +559,26 @@ def decode_attention(q, sq, k_cache, sk, v_cache, sv, seq_lens, stream=None):
     ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
     fp8_decode_attention(q, sq[:1], k_cache, sk[:1], v_cache, sv[:1], seq_lens, out, ws, stream)
     return out
+
+
+def moe_wgrad(dy: torch.Tensor, x: torch.Tensor, offsets, pow2: bool = False, stream=None):
+    """Weight gradients of a mixture-of-experts layer, dW_g = dY_g^T X_g for
+    the expert-sorted token rows offsets[g] .. offsets[g+1]-1 (offsets: host
+    sequence of G+1 ints).  Each expert's rows are quantised in 128x1 blocks
+    of its own tokens (fp8_quant_act_128x1 pads the last block with zeros) and
+    run through the wgrad GEMM, one expert after another.  Returns bf16
+    [G, N, K]; experts without tokens get zeros."""
+    G = len(offsets) - 1
+    N, K = dy.shape[1], x.shape[1]
+    dw = torch.zeros((G, N, K), dtype=torch.bfloat16, device=dy.device)
+    for g in range(G):
+        lo, hi = int(offsets[g]), int(offsets[g + 1])
+        if hi <= lo:
+            continue
+        qt_dy, st_dy = quant_act_t(dy[lo:hi], pow2, stream=stream)
+        qt_x, st_x = quant_act_t(x[lo:hi], pow2, stream=stream)
+        wgrad(qt_dy, st_dy, qt_x, st_x, pow2, out=dw[g], stream=stream)
+    return dw
 
 
 def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):

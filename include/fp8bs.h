@@ -173,12 +173,15 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  * itself, as fp8_quant_act_1x128(x) would: one read of x for both layouts.
  *
  * x   device, bf16 [M, K] row-major, row pitch ldx (>= K, % 8 == 0)
- * qt  device, uint8 [K, M] row-major (token-contiguous), row pitch ldqt (>= M, % 16 == 0)
- * st  device, fp32 [M/128][ldst]: the scale of column k, token block mb is
+ * qt  device, uint8 [K, Mp] row-major (token-contiguous), row pitch ldqt (>= Mp, % 16 == 0),
+ *     Mp = M rounded up to a multiple of 128
+ * st  device, fp32 [Mp/128][ldst]: the scale of column k, token block mb is
  *     st[mb * ldst + k] (ldst >= K, % 4 == 0) -- the layout a GEMM's sA/sB takes
  * q, s  optional (both NULL, or both set): as fp8_quant_act_1x128 (ldq, lds)
- * M >= 0 and M % 128 == 0 (pad ragged token counts with zero rows: they add
- * nothing to dW), M/128 <= 65535; K > 0, K % 128 == 0.  Pointers 16-byte aligned.
+ * M >= 0 (0 is a no-op); a last token block of fewer than 128 rows is padded
+ * with zero rows (they change no block's amax and add nothing to dW; their
+ * codes in qt are zero), Mp/128 <= 65535; K > 0, K % 128 == 0.  Pointers
+ * 16-byte aligned.
  */
 FP8BS_API fp8_status fp8_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t ldx,
                                          uint8_t *qt, int64_t ldqt, float *st, int64_t ldst,

@@ -143,7 +143,7 @@ def test_quant_act_128x1_validation(L):
     assert call(qt=NULL) == 1
     assert call(st=NULL) == 1
     assert call(q=A16) == 1                       # q without s
-    assert call(M=200, ldqt=256) == 2             # M % 128: token blocks are whole
+    assert call(M=200, ldqt=200) == 2             # qt rows hold the padded 256 tokens
     assert call(K=200) == 2
     assert call(ldqt=128) == 2                    # ldqt < M
     assert call(ldst=64) == 2                     # ldst < K
@@ -158,6 +158,7 @@ def test_quant_act_128x1_validation(L):
     if not _has_gpu():
         assert call() == 6
         assert call(q=A16, s=A16, ldq=128, lds=256) == 6
+        assert call(M=200, ldqt=256) == 6         # a ragged last token block is padded
 
 
 def test_quant_weight_t_validation(L):

@@ -275,3 +275,37 @@ def test_llama_gate_up_backward_full_size_sampled(ops, pow2):
     assert np.array_equal(st_dy[:, nrows].cpu().numpy(), stg_o.T)
     assert np.array_equal(qt_x.cpu().numpy(), qtx_o)
     assert_gemm_close(bf16_to_np(dw[nrows]), O.wgrad_ref(qtg_o, stg_o, qtx_o, stx_o), "wgrad full size")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_act_128x1_ragged_tokens(ops, pow2):
+    """300 tokens: the last 128x1 block holds 44 real rows and is padded with
+    zeros inside the kernel (codes of the pad are zero)."""
+    x = _edge_act(384, 256, seed=77)[:300].contiguous()
+    qt, st, q, s = ops.quant_act_t(x.cuda(), pow2, rowwise=True)
+    _sync_ok(ops)
+    qt_o, st_o = O.quant_act_128x1(bf16_to_np(x), pow2)
+    assert qt.shape == (256, 384) and np.array_equal(qt.cpu().numpy(), qt_o)
+    assert np.array_equal(st[:, :256].cpu().numpy(), st_o.T)
+    q_o, s_o = O.quant_act_1x128(bf16_to_np(x), pow2)
+    assert np.array_equal(q.cpu().numpy(), q_o) and np.array_equal(s[:, :300].cpu().numpy(), s_o.T)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_moe_wgrad(ops, pow2):
+    """MoE weight gradients over Zipf-routed, expert-sorted tokens with ragged
+    and empty experts (each expert's token blocks padded with zeros)."""
+    offs = [0, 5, 5, 140, 140, 300, 301, 557]
+    N, K = 256, 384
+    T = offs[-1]
+    x = _act(81, (T, K))
+    dy = _grad(82, (T, N))
+    dw = ops.moe_wgrad(dy.cuda(), x.cuda(), offs, pow2)
+    _sync_ok(ops)
+    ref = O.moe_wgrad_ref(bf16_to_np(dy), bf16_to_np(x), offs, pow2)
+    got = bf16_to_np(dw)
+    for g in range(len(offs) - 1):
+        if offs[g + 1] == offs[g]:
+            assert np.all(got[g] == 0)
+        else:
+            assert_gemm_close(got[g], ref[g], f"moe wgrad expert {g}")
