@@ -321,6 +321,34 @@ def test_e8_scales_validation(L):
         assert g(*args, 0x22, NULL, 0, NULL) == 6
 
 
+def test_plan_with_scale_flags(L):
+    from fp8_block_scaled_05_gb300 import ops
+    # UE8M0 byte scales always take the MX kernel (the only one that reads them),
+    # power-of-two fp32 scales take it above the decode sizes
+    assert ops.fp8_gemm_plan(4096, 4096, 4096, ops.FP8_GEMM_SCALES_E8)[0] == ops.FP8_GEMM_PATH_MX
+    assert ops.fp8_gemm_plan(8, 4096, 4096, ops.FP8_GEMM_SCALES_E8)[0] == ops.FP8_GEMM_PATH_MX
+    assert ops.fp8_gemm_plan(4096, 4096, 4096, ops.FP8_GEMM_SCALES_POW2)[0] == ops.FP8_GEMM_PATH_MX
+    assert ops.fp8_gemm_plan(8, 4096, 4096, ops.FP8_GEMM_SCALES_POW2)[0] == ops.FP8_GEMM_PATH_SKINNY
+
+
+def test_grouped_scale_flag_validation(L):
+    f = L.fp8_blockscaled_grouped_gemm
+    base = (A16, 256, A16b, 8, A16c, 2, 8, A16, A16b, A16c, 128, 128, 256)
+    assert f(*base, 0x12, NULL, 0, NULL) == 9     # UE8M0 scales on the promote kernel
+    assert f(*base, 0x20, NULL, 0, NULL) == 4     # MX needs power-of-two (or UE8M0) scales
+    assert f(*base, 0x40, NULL, 0, NULL) == 4     # unknown path bits
+    if not _has_gpu():
+        assert f(*base, 0x2, NULL, 0, NULL) == 6  # AUTO takes MX for byte scales
+
+
+def test_attention_workspace_sizes(L):
+    # one split (T <= 512): the kernel writes the output directly
+    assert L.fp8_decode_attention_workspace_size(64, 32, 512) == 0
+    # T = 4096: 8 splits of (max, sum, 128 partial outputs) per (sequence, head)
+    assert L.fp8_decode_attention_workspace_size(64, 32, 4096) == 64 * 32 * 8 * 130 * 4
+    assert L.fp8_decode_attention_workspace_size(0, 32, 4096) == 0
+
+
 def test_grouped_validation(L):
     f = L.fp8_blockscaled_grouped_gemm
     assert f(A16, 256, A16b, 8, A16c, 0, 8, A16, A16b, A16c, 128, 128, 256, 0, NULL, 0, NULL) == 2   # G=0
