@@ -60,6 +60,9 @@ def parse_args(argv=None):
                                                                 "measurement")
     p.add_argument("--no-per-tensor", action="store_true", help="skip the per-tensor scaling measurement")
     p.add_argument("--no-attention", action="store_true", help="skip the FP8 KV-cache decode attention measurement")
+    p.add_argument("--no-qwen", action="store_true", help="skip the Qwen3-8B prefill (M = 16384) measurement")
+    p.add_argument("--no-decode", action="store_true", help="skip the decode-sized (M <= 256) measurement")
+    p.add_argument("--no-moe", action="store_true", help="skip the Qwen3-30B-A3B grouped MoE measurement")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3) if a.impl == "ours" else max(a.warmup, 0)
     return a
@@ -510,6 +513,19 @@ def run_ours(args, world, rank, local):
         per_tensor = per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_peak)
 
     # ---------------- one decode step of attention over an FP8 KV cache
+    # ---------------- the other workloads of the layer: Qwen3-8B long-rollout
+    # prefill (M = 16384, both scale modes), decode-sized GEMMs (M <= 256,
+    # weight-stream bound) and the Qwen3-30B-A3B grouped expert GEMMs.
+    qwen = None
+    if not args.no_qwen:
+        qwen = qwen_measure(args, ops, stream, dev, flush, fp8_peak)
+    decode = None
+    if not args.no_decode:
+        decode = decode_measure(args, ops, stream, dev, flush, peaks["hbm_gbs"])
+    moe = None
+    if not args.no_moe:
+        moe = moe_measure(args, ops, stream, dev, flush, fp8_peak, peaks["hbm_gbs"])
+
     attention = None
     if not args.no_attention:
         attention = attention_measure(args, ops, stream, dev, flush, peaks["hbm_gbs"])
@@ -556,6 +572,9 @@ def run_ours(args, world, rank, local):
             "training": training,
             "per_tensor": per_tensor,
             "attention": attention,
+            "qwen_prefill": qwen,
+            "decode": decode,
+            "moe": moe,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
@@ -609,6 +628,211 @@ def per_tensor_measure(args, layers, ops, stream, dev, flush, flops_step, fp8_pe
             "ms_per_step": total / args.steps, "gemm_only_tflops": flops_step / (gemm_ms / 1e3) / 1e12,
             "gemm_frac_fp8": flops_step / (gemm_ms / 1e3) / 1e12 / fp8_peak, "kernels_ms": kern,
             "gpu_launches": 5 * len(layers) * args.steps}
+
+
+def time_calls(args, stream, dev, flush, calls, graph=False):
+    """Mean CUDA-event time (ms) of each callable in `calls` (a list of
+    zero-argument functions run back to back on `stream`), over args.steps
+    flushed steps after args.warmup untimed ones; returns (per-call ms,
+    whole-sequence ms).  With graph=True the sequence is captured once into a
+    CUDA graph and each call replayed from its own graph, so that host launch
+    overhead does not land inside the event pairs of short kernels."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush()
+            for f in calls:
+                f()
+    torch.cuda.synchronize(dev)
+    runs = calls
+    if graph:
+        runs = []
+        for f in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                f()
+            runs.append(g.replay)
+        with torch.cuda.stream(stream):
+            for r in runs:
+                r()
+        torch.cuda.synchronize(dev)
+    n = len(runs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush()
+            for i, r in enumerate(runs):
+                evs[k][i].record(stream)
+                r()
+            evs[k][n].record(stream)
+    torch.cuda.synchronize(dev)
+    per = [sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)) / args.steps for i in range(n)]
+    total = sum(evs[k][0].elapsed_time(evs[k][n]) for k in range(args.steps)) / args.steps
+    return per, total
+
+
+def qwen_measure(args, ops, stream, dev, flush, fp8_peak):
+    """Qwen3-8B-shaped long-rollout prefill, M = 16384 tokens (Student-t nu = 4
+    activations, seeded host draws; W ~ N(0, 0.02)): per layer the 1x128
+    activation quantiser, the 128x128 weight quantiser and the GEMM, timed per
+    call over flushed steps, in both scale modes (fp32 scales: promote
+    kernel; power-of-two scales: MX kernel)."""
+    import torch
+
+    from fp8_block_scaled_05_gb300 import inputs as I
+
+    out = {"workload": "qwen3-8b prefill, M=16384: gate_up(K4096,N24576) down(K12288,N4096) o_proj(K4096,N4096)",
+           "inputs": "A ~ Student-t(nu=4), W ~ N(0,0.02), seeded PCG64", "modes": {}}
+    layers = []
+    for case in I.qwen_prefill_layers(args.seed):
+        M, N, K = case.shape
+        layers.append(dict(name=case.name.split(".")[1], M=M, N=N, K=K, a=case.a.to(dev), w=case.w.to(dev),
+                           qa=torch.empty((M, K), dtype=torch.uint8, device=dev),
+                           sa=torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev),
+                           qw=torch.empty((N, K), dtype=torch.uint8, device=dev),
+                           sw=torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
+                           c=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                           ws=ops.workspace_for(M, N, K, 1, dev)))
+    flops = sum(2.0 * L["M"] * L["N"] * L["K"] for L in layers)
+    for pow2 in (False, True):
+        mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+        flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
+        calls = []
+        for L in layers:
+            calls += [lambda L=L: ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], mode, stream),
+                      lambda L=L: ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream),
+                      lambda L=L: ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags,
+                                                           L["ws"], stream)]
+        per, total = time_calls(args, stream, dev, flush, calls)
+        rows, gemm_ms = {}, 0.0
+        for i, L in enumerate(layers):
+            qa_ms, qw_ms, g_ms = per[3 * i:3 * i + 3]
+            gf = 2.0 * L["M"] * L["N"] * L["K"]
+            gemm_ms += g_ms
+            rows[L["name"]] = {"quant_act_ms": qa_ms, "quant_weight_ms": qw_ms, "gemm_ms": g_ms,
+                               "quant_gemm_tflops": gf / ((qa_ms + qw_ms + g_ms) / 1e3) / 1e12,
+                               "gemm_tflops": gf / (g_ms / 1e3) / 1e12,
+                               "gemm_frac_fp8": gf / (g_ms / 1e3) / 1e12 / fp8_peak}
+        out["modes"]["pow2" if pow2 else "fp32"] = {
+            "gemm_kernel": "mx" if pow2 else "promote", "ms_per_step": total,
+            "quant_gemm_tflops": flops / (total / 1e3) / 1e12, "gemm_only_tflops": flops / (gemm_ms / 1e3) / 1e12,
+            "gemm_frac_fp8": flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, "layers": rows,
+            "gpu_launches": 3 * len(layers) * args.steps}
+    return out
+
+
+def decode_measure(args, ops, stream, dev, flush, hbm_peak):
+    """Decode-sized layers: M in {1, 8, 64, 256} tokens at (K, N) = (4096,
+    6144) and (14336, 4096), weights pre-quantised 128x128 (fp32 scales).  A
+    decode step is the 1x128 quantiser of the bf16 activations and the skinny
+    GEMM; each is replayed from a CUDA graph with the L2 flushed before every
+    step.  Algorithmic bytes of the step: N K (weight codes) + 4 N K / 16384
+    (weight scales) + 2 M K (bf16 activations) + 2 M N (bf16 output); of the
+    GEMM alone the activations count as M K codes + 4 M K / 128 scales."""
+    import torch
+
+    from fp8_block_scaled_05_gb300 import inputs as I
+
+    out = {"what": "quant_act (bf16 A -> E4M3 1x128) + skinny GEMM on pre-quantised weights, CUDA-graph replays, "
+                   "L2 flushed before each step", "points": {}}
+    fracs = []
+    for K, N in I.DECODE_SHAPES:
+        w = I.decode_case(1, K, N, args.seed).w.to(dev)
+        qw, sw = ops.quant_weight(w)
+        del w
+        for M in I.DECODE_TOKENS:
+            a = I.decode_case(M, K, N, args.seed).a.to(dev)
+            qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            sa = torch.empty((K // 128, max(ops.round_up(M, 4), 4)), dtype=torch.float32, device=dev)
+            c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = ops.workspace_for(M, N, K, 1, dev)
+
+            def step():
+                ops.fp8_quant_act_1x128(a, qa, sa, 0, stream)
+                ops.fp8_blockscaled_gemm(qa, sa, qw, sw, c, 0, ws, stream)
+
+            def gemm_only():
+                ops.fp8_blockscaled_gemm(qa, sa, qw, sw, c, 0, ws, stream)
+
+            (step_ms,), _ = time_calls(args, stream, dev, flush, [step], graph=True)
+            (gemm_ms,), _ = time_calls(args, stream, dev, flush, [gemm_only], graph=True)
+            wbytes = N * K + 4.0 * N * K / 16384
+            step_bytes = wbytes + 2.0 * M * K + 2.0 * M * N
+            gemm_bytes = wbytes + M * K + 4.0 * M * K / 128 + 2.0 * M * N
+            path, ctas = ops.fp8_gemm_plan(M, N, K)
+            pt = {"step_us": step_ms * 1e3, "step_GB/s": step_bytes / (step_ms / 1e3) / 1e9,
+                  "step_frac_hbm": step_bytes / (step_ms / 1e3) / 1e9 / hbm_peak,
+                  "gemm_us": gemm_ms * 1e3, "gemm_GB/s": gemm_bytes / (gemm_ms / 1e3) / 1e9,
+                  "gemm_frac_hbm": gemm_bytes / (gemm_ms / 1e3) / 1e9 / hbm_peak,
+                  "gemm_tflops": 2.0 * M * N * K / (gemm_ms / 1e3) / 1e12, "ctas": ctas}
+            fracs.append(pt["step_frac_hbm"])
+            out["points"][f"M{M}.K{K}.N{N}"] = pt
+    out["min_step_frac_hbm"] = min(fracs)
+    out["gpu_launches"] = 3 * len(fracs) * args.steps
+    return out
+
+
+def moe_measure(args, ops, stream, dev, flush, fp8_peak, hbm_peak):
+    """Qwen3-30B-A3B-shaped mixture-of-experts layer: 8192 tokens, top-8 of 128
+    experts with Zipf(1.1) popularity (seeded Gumbel-top-8), rows sorted by
+    expert (65536 rows); expert gate+up (K 2048, N 1536) and down (K 768,
+    N 2048).  Per projection: the 1x128 quantiser of the expert-sorted
+    activations, the 128x128 quantiser of all experts' weights (one launch on
+    the [G N, K] view; no tile straddles two experts since N % 128 == 0) and
+    the grouped GEMM with device-side offsets, in both scale modes.  FLOPs
+    are 2 sum(M_e) N K; the weight stream is G N K code bytes."""
+    import numpy as np
+    import torch
+
+    from fp8_block_scaled_05_gb300 import inputs as I
+
+    m = I.moe_case(args.seed)
+    G = m.w_gate_up.shape[0]
+    offs = torch.from_numpy(m.offsets).to(dev)
+    projs = []
+    for name, a, w in (("gate_up", m.a_gate_up, m.w_gate_up), ("down", m.a_down, m.w_down)):
+        Mt, K = a.shape
+        N = w.shape[1]
+        projs.append(dict(name=name, M=Mt, N=N, K=K, a=a.to(dev), w=w.to(dev).view(G * N, K),
+                          qa=torch.empty((Mt, K), dtype=torch.uint8, device=dev),
+                          sa=torch.empty((K // 128, ops.round_up(Mt, 4)), dtype=torch.float32, device=dev),
+                          qw=torch.empty((G, N, K), dtype=torch.uint8, device=dev),
+                          sw=torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=dev),
+                          c=torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)))
+    sizes = m.offsets[1:] - m.offsets[:-1]
+    out = {"workload": "qwen3-30b-a3b MoE: 8192 tokens, 128 experts, top-8, Zipf(1.1) routing; "
+                       "gate_up (K2048,N1536), down (K768,N2048) per expert",
+           "rows_per_expert": {"min": int(sizes.min()), "median": float(np.median(sizes)), "max": int(sizes.max())},
+           "modes": {}}
+    for pow2 in (False, True):
+        mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+        flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
+        calls = []
+        for P in projs:
+            calls += [lambda P=P: ops.fp8_quant_act_1x128(P["a"], P["qa"], P["sa"], mode, stream),
+                      lambda P=P: ops.fp8_quant_weight_128x128(P["w"], P["qw"].view(-1, P["K"]),
+                                                               P["sw"].view(-1, P["K"] // 128), mode, stream),
+                      lambda P=P: ops.fp8_blockscaled_grouped_gemm(P["qa"], P["sa"], offs, P["qw"], P["sw"], P["c"],
+                                                                   flags, None, stream)]
+        per, total = time_calls(args, stream, dev, flush, calls)
+        rows = {}
+        for i, P in enumerate(projs):
+            qa_ms, qw_ms, g_ms = per[3 * i:3 * i + 3]
+            gf = 2.0 * P["M"] * P["N"] * P["K"]
+            wbytes = G * P["N"] * P["K"]
+            rows[P["name"]] = {"quant_act_ms": qa_ms, "quant_weight_ms": qw_ms, "gemm_ms": g_ms,
+                               "gemm_tflops": gf / (g_ms / 1e3) / 1e12,
+                               "gemm_frac_fp8": gf / (g_ms / 1e3) / 1e12 / fp8_peak,
+                               "weight_stream_GB/s": wbytes / (g_ms / 1e3) / 1e9,
+                               "weight_stream_frac_hbm": wbytes / (g_ms / 1e3) / 1e9 / hbm_peak,
+                               "quant_gemm_tflops": gf / ((qa_ms + qw_ms + g_ms) / 1e3) / 1e12}
+        flops = sum(2.0 * P["M"] * P["N"] * P["K"] for P in projs)
+        out["modes"]["pow2" if pow2 else "fp32"] = {
+            "gemm_kernel": "mx (grouped)" if pow2 else "promote (grouped)", "ms_per_step": total,
+            "quant_gemm_tflops": flops / (total / 1e3) / 1e12, "projections": rows,
+            "gpu_launches": 3 * len(projs) * args.steps}
+    return out
 
 
 def attention_measure(args, ops, stream, dev, flush, hbm_peak):

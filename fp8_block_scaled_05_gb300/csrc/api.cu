@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -187,6 +188,31 @@ int promote_tile_n(int64_t M, int64_t N, int64_t K, int32_t G) {
     }();
     if (forced) return forced;
     return (N % 256 == 0) ? 256 : 128;
+}
+
+// Failure-path test hook (fp8_debug_inject): read by every GEMM call.
+namespace {
+std::atomic<uint64_t> g_inject_wait_ns{0};
+std::atomic<int32_t> g_inject_skip{0};
+}  // namespace
+
+void fault_injection(uint64_t* wait_ns, int32_t* skip_first_load) {
+    *wait_ns = g_inject_wait_ns.load(std::memory_order_relaxed);
+    *skip_first_load = g_inject_skip.load(std::memory_order_relaxed);
+}
+
+// Dense fp32-scale GEMMs run on CTA pairs (gemm_pair.cu) when the device can
+// place them; FP8BS_PROMOTE_PAIR=0 selects the one-CTA promote kernel instead
+// (for comparison).
+bool promote_use_pair(int64_t M, int64_t N, int64_t K) {
+    (void)M;
+    (void)N;
+    (void)K;
+    static int off = [] {
+        const char* e = std::getenv("FP8BS_PROMOTE_PAIR");
+        return (e && e[0] == '0') ? 1 : 0;
+    }();
+    return !off && pair_max_clusters() > 0;
 }
 
 }  // namespace fp8bs
@@ -418,6 +444,7 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
     if (fp8_status e = current_device(&d)) return e;
 
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.sa = sa;
     a.ldsa = ldsa;
     a.sb = sb;
@@ -456,15 +483,18 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         a.workspace = workspace;
         a.ws_bytes = ws_bytes;
     }
+    const bool pair = !mx && promote_use_pair(M, N, K);
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
         return e;
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
+    // the pair kernel's CTAs each load 64 of a tile's 128 B rows
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, pair ? 64u : (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
+    if (pair) return cuda_status(launch_gemm_pair(a, st));
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
@@ -484,6 +514,7 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
     if (fp8_status e = current_device(&d)) return e;
 
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.sa = sa;
     a.ldsa = ldsa;
     a.sb = sb;
@@ -509,10 +540,12 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
+    const bool pair = !mx && promote_use_pair(M, N, K);
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, pair ? 64u : (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (pair) return cuda_status(launch_gemm_pair(a, st));
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
@@ -534,6 +567,7 @@ fp8_status fp8_tensorscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa
     if (fp8_status e = current_device(&d)) return e;
 
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.per_tensor = 1;
     a.sa = sa;
     a.sb = sb;
@@ -587,6 +621,7 @@ fp8_status fp8_blockscaled_gemm_quant(const uint8_t* qa, int64_t lda, const floa
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.sa = sa;
     a.ldsa = ldsa;
     a.sb = sb;
@@ -646,6 +681,7 @@ fp8_status fp8_blockscaled_grouped_gemm(const uint8_t* qa, int64_t lda, const fl
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.sa = sa;
     a.ldsa = ldsa;
     a.sb = sb;
@@ -682,6 +718,7 @@ fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, c
     if (fp8_status e = check_gemm_common(qa, lda, sa, ldsa, qb, sb, c, ldc, M, N, K, flags)) return e;
     const uint32_t path = flags & FP8_GEMM_PATH_MASK;
     if (path != FP8_GEMM_PATH_AUTO && path != FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_ERR_NOT_IMPLEMENTED;   // the skinny kernel reads fp32 scales
     if (M == 0) return FP8_OK;
     if (M > 256 || K / 128 > 1024) return FP8_ERR_SHAPE;
     if (ldb < K) return FP8_ERR_SHAPE;
@@ -689,6 +726,7 @@ fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, c
     DeviceInfo* d;
     if (fp8_status e = current_device(&d)) return e;
     GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
     a.sa = sa;
     a.ldsa = ldsa;
     a.sb = sb;
@@ -711,6 +749,13 @@ fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, c
                                   &a.tm_b))
         return e;
     return cuda_status(launch_gemm_skinny_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_debug_inject(int32_t skip_first_load, uint64_t wait_limit_ns) {
+    if (wait_limit_ns > kWaitLimitNs) return FP8_ERR_SHAPE;
+    g_inject_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+    g_inject_skip.store(skip_first_load ? 1 : 0, std::memory_order_relaxed);
+    return FP8_OK;
 }
 
 fp8_status fp8_last_device_status(fp8_stream_t stream) {

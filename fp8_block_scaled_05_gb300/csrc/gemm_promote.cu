@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
-                   const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo) {
+                   const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo,
+                   uint64_t wait_ns, int skip_first_load) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -193,10 +194,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
-                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
+                    if (!mbar_wait(&ctl->empty[s], ph ^ 1, wait_ns)) {
                         ok = false;
                         break;
                     }
+                    if (skip_first_load && it == 0) continue;   // failure-path test: K-block 0 never lands
                     uint8_t* sA = smem + (size_t)s * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&ctl->full[s], C::STAGE_BYTES);
                     tma_load_2d(sA, &tm_a, &ctl->full[s], kb * BK, tl.m0);
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 // Let the copies already issued land before the CTA can exit.
                 const uint32_t n = it < (uint32_t)C::STAGES ? it : (uint32_t)C::STAGES;
                 for (uint32_t j = it - n; j < it; ++j)
-                    mbar_wait(&ctl->full[j % C::STAGES], (j / C::STAGES) & 1, kWaitLimitNs);
+                    mbar_wait(&ctl->full[j % C::STAGES], (j / C::STAGES) & 1, wait_ns);
             }
         }
         __syncwarp();
@@ -231,9 +233,9 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     // whose loop is the critical path, find the scales in place once
                     // the K-block's partial is in TMEM and wait on one barrier only.
                     const uint32_t slot = it % SRING, sph = (it / SRING) & 1;
-                    if (!mbar_wait(&ctl->full[s], ph, kWaitLimitNs) ||
-                        !mbar_wait(&ctl->sfull[slot], sph, kWaitLimitNs) ||
-                        !mbar_wait(&ctl->tempty[b], tph ^ 1, kWaitLimitNs)) {
+                    if (!mbar_wait(&ctl->full[s], ph, wait_ns) ||
+                        !mbar_wait(&ctl->sfull[slot], sph, wait_ns) ||
+                        !mbar_wait(&ctl->tempty[b], tph ^ 1, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             }
             // All MMAs this thread issued are complete before TMEM is released.
             umma_commit(&ctl->mma_done[me]);
-            mbar_wait(&ctl->mma_done[me], 0, kWaitLimitNs);
+            mbar_wait(&ctl->mma_done[me], 0, wait_ns);
         }
         __syncwarp();
     } else if (warp == SCALE_WARP) {
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             const int nb0 = tl.n0 / 128;
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++sit) {
                 const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
-                bool got = mbar_wait(&ctl->sempty[slot], ph ^ 1, kWaitLimitNs);
+                bool got = mbar_wait(&ctl->sempty[slot], ph ^ 1, wait_ns);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) {
                     ok = false;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                 const uint32_t slot = kbg % SRING, sph = (kbg / SRING) & 1;
                 const uint32_t b = kbg % C::NBUF, tph = (kbg / C::NBUF) & 1;
                 (void)sph;   // the issuer waited for the scale slot before this K-block's MMAs
-                bool got = __all_sync(0xFFFFFFFFu, ready) || mbar_wait(&ctl->tfull[b], tph, kWaitLimitNs);
+                bool got = __all_sync(0xFFFFFFFFu, ready) || mbar_wait(&ctl->tfull[b], tph, wait_ns);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) {
                     ok = false;
@@ -573,7 +575,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     }
     kern<<<grid, C::THREADS, smem_bytes<BN, ROWB>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
                                                            a.ldsb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
-                                                     (int)a.K, a.offsets, a.G, a.status, split, a.qout);
+                                                     (int)a.K, a.offsets, a.G, a.status, split, a.qout,
+                                                     wait_bound(a), a.skip_first_load);
     return cudaGetLastError();
 }
 

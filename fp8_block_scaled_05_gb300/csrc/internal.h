@@ -135,7 +135,17 @@ struct GemmArgs {
     int32_t bn;                     // promote kernel tile width (128 or 256)
     int* status;
     int sm_count;
+    // failure-path test hook (fp8_debug_inject): 0 = the default wait bound
+    // (kWaitLimitNs); skip_first_load != 0 makes the TMA producer skip the
+    // first K-block's operands, so the waits on them run out
+    uint64_t wait_ns;
+    int32_t skip_first_load;
 };
+
+// The current fault-injection setting (fp8_debug_inject), copied into every
+// GEMM's arguments.
+void fault_injection(uint64_t* wait_ns, int32_t* skip_first_load);
+inline uint64_t wait_bound(const GemmArgs& a) { return a.wait_ns ? a.wait_ns : kWaitLimitNs; }
 
 // Dense / grouped kernel with per-K-block fp32 promotion (tcgen05, TMEM);
 // output tile 128 x bn with bn = 128 or 256 (promote_tile_n picks it).
@@ -154,6 +164,14 @@ constexpr int kPromoteMaxParts = 4, kMxMaxParts = 2;
 constexpr int kMxTileN = 256;   // MX kernel output tile width
 TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts);
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
+
+// Dense kernel with per-K-block promotion on CTA pairs (cta_group::2):
+// 256 x 128 tiles, a.tm_b with box {128, 64} (each CTA of a pair loads 64
+// of the tile's 128 B rows).  pair_max_clusters(): pairs that fit on the
+// current device at once (0 if the kernel cannot run there).
+int pair_max_clusters();
+cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t st);
+bool promote_use_pair(int64_t M, int64_t N, int64_t K);
 
 // Dense / grouped kernel for power-of-two scales: the tensor core applies the
 // scales as UE8M0 block scale factors (tcgen05.mma kind::mxf8f6f4); output

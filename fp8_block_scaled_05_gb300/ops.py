@@ -70,6 +70,7 @@ SIGNATURES = {
     "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
     "fp8_gemm_plan": (_u32, [_i64, _i64, _i64, _u32, ctypes.POINTER(_i32)]),
+    "fp8_debug_inject": (ctypes.c_int, [_i32, ctypes.c_uint64]),
 }
 
 _lib = None
@@ -402,6 +403,12 @@ def fp8_gemm_plan(M: int, N: int, K: int, flags: int = 0):
     sp = ctypes.c_int32(0)
     path = lib().fp8_gemm_plan(M, N, K, flags, ctypes.byref(sp))
     return int(path), int(sp.value)
+
+
+def fp8_debug_inject(skip_first_load: bool = False, wait_limit_ns: int = 0) -> None:
+    """Failure-path test hook: shortened kernel waits and a skipped first
+    K-block for the GEMMs launched after it (see include/fp8bs.h)."""
+    _check(lib().fp8_debug_inject(1 if skip_first_load else 0, int(wait_limit_ns)), "fp8_debug_inject")
 
 
 def fp8_last_device_status(stream=None) -> int:

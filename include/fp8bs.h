@@ -83,7 +83,7 @@ typedef enum {
 #define FP8_GEMM_PATH_AUTO     0x00u
 #define FP8_GEMM_PATH_PROMOTE  0x10u /* large-M kernel, fp32 scale promotion per K-block */
 #define FP8_GEMM_PATH_MX       0x20u /* large-M kernel, hardware UE8M0 block scaling (needs SCALES_POW2) */
-#define FP8_GEMM_PATH_SKINNY   0x30u /* M <= 256: weights as the MMA's M side, split-K */
+#define FP8_GEMM_PATH_SKINNY   0x30u /* M <= 256: weights as the MMA's M side, K split over all SMs */
 
 /*
  * 1x128 activation quantisation.
@@ -241,8 +241,10 @@ FP8BS_API fp8_status fp8_quant_weight_128x128_t(const void *w, int64_t N, int64_
  *     that must be zero before the first use; every completed call leaves them
  *     zero again (allocate it zero-filled once and reuse it, for any shapes).
  *     Calls that share a workspace must not run concurrently.
- *     - Skinny path (M <= 256): required; smaller or NULL returns
- *       FP8_ERR_WORKSPACE.
+ *     - Skinny path (M <= 256): required when the size is not 0 (the
+ *       K-blocks of all output tiles are shared evenly by up to one CTA per
+ *       SM, so a tile may be computed in pieces whose fp32 partials are then
+ *       added in CTA order); smaller or NULL returns FP8_ERR_WORKSPACE.
  *     - Promote and MX paths: optional.  With it, when the output tiles do
  *       not fill whole waves of the GPU's SMs, the tiles of the last wave are
  *       split along K and their fp32 parts added in a fixed order; without it
@@ -448,9 +450,10 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
  * Decode-sized GEMM (M <= 256) that allocates nothing and takes no workspace.
  *
  * The web pages have no counterpart: this is an interface convenience.  It
- * computes the same C as fp8_blockscaled_gemm on the split-K skinny path
- * (same kernels, same split count, same fixed-order reduction), but keeps the
- * split-K tickets and fp32 partials in an 8 MiB array inside the library's own
+ * computes the same C as fp8_blockscaled_gemm on the skinny path (same
+ * kernels, same division of the K-blocks over the CTAs, same fixed-order
+ * reduction, so the output is bit-identical), but keeps the reduction's
+ * tickets and fp32 partials in an 8 MiB array inside the library's own
  * device memory instead of a caller-provided workspace.  It is meant for
  * callers that cannot call cudaMalloc: plugins hosted by a runtime that
  * reserves all device memory at start-up and fails or mis-accounts later
@@ -466,14 +469,19 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
  * - All calls share the array, and it keeps what the last call left in it.
  *   The call clears the ticket words on `stream` before its launch.  Calls
  *   that overlap on the GPU (unordered streams) race on the array: order them.
- * - The scratch needed is 65536 bytes of tickets plus
- *   splits * T * NT * 128 * 4 bytes of partials, where NT = M rounded up to
- *   16, 32, 64 or 128 (128 for M > 64), T = (N/128) * ceil(M / NT) (tokens
- *   beyond 128 run as further 128-token chunks), and splits is as reported by
- *   fp8_gemm_plan.  Sizes that need more than 8 MiB return
+ * - The scratch needed is fp8_gemm_workspace_size(M, N, K, 1): 0 when every
+ *   output tile is computed by one CTA, else 65536 bytes of tickets plus
+ *   (P + T - 1) * NT * 128 * 4 bytes of partials, where NT = M rounded up to
+ *   16, 32, 64 or 128 (128 for M > 64), T = (N/128) * ceil(M / NT) output
+ *   tiles (tokens beyond 128 run as further 128-token chunks), and P is the
+ *   CTA count fp8_gemm_plan reports.  Sizes that need more than 8 MiB return
  *   FP8_ERR_WORKSPACE without launching.
  *   M > 256 returns FP8_ERR_SHAPE.
- * - flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_SKINNY (plus FP8_GEMM_SCALES_POW2).
+ * - flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_SKINNY (plus FP8_GEMM_SCALES_POW2);
+ *   FP8_GEMM_SCALES_E8 returns FP8_ERR_NOT_IMPLEMENTED (fp32 scales only).
+ * - The array's address is looked up once per device and kept for the life of
+ *   the process: after cudaDeviceReset (or anything else that replaces the
+ *   device's primary context) this entry point must not be called again.
  */
 FP8BS_API fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t *qa, int64_t lda, const float *sa,
                                                          int64_t ldsa, const uint8_t *qb, int64_t ldb,
@@ -488,13 +496,29 @@ FP8BS_API size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_
 /* Static, human-readable name of a status code. */
 FP8BS_API const char *fp8_status_string(fp8_status status);
 
+/*
+ * Failure-path test hook (the pages have no counterpart).  Until called
+ * again, GEMMs launched by this process on the promote, pair and skinny
+ * kernels bound every wait inside the kernel by `wait_limit_ns` nanoseconds
+ * (0: the default of 2 s; at most 2 s), and with skip_first_load != 0 their
+ * TMA producer leaves out the first K-block's operands, so the waits on them
+ * run out: the kernel records FP8_ERR_TIMEOUT in the status word, releases
+ * its TMEM and returns; its output is unspecified.  The CUDA context stays
+ * usable.  fp8_debug_inject(0, 0) restores normal operation.  A workspace
+ * used by such a call may hold non-zero tickets afterwards: zero it again.
+ * Returns FP8_ERR_SHAPE for a limit above 2 s.
+ */
+FP8BS_API fp8_status fp8_debug_inject(int32_t skip_first_load, uint64_t wait_limit_ns);
+
 /* Synchronises `stream`, returns the current device's status word (FP8_OK
  * or the first error a kernel recorded, e.g. FP8_ERR_TIMEOUT) and clears it. */
 FP8BS_API fp8_status fp8_last_device_status(fp8_stream_t stream);
 
 /* Which kernel fp8_blockscaled_gemm would run for these arguments
  * (one of the FP8_GEMM_PATH_* values, never AUTO), and, through
- * `splits` (may be NULL), how many K-splits it would use. */
+ * `splits` (may be NULL), for the skinny path the number of CTAs P that
+ * share the K-blocks of all output tiles (stream-K: CTA c takes K-blocks
+ * [c U / P, (c+1) U / P) of the U = tiles * K/128, tile after tile), else 1. */
 FP8BS_API uint32_t fp8_gemm_plan(int64_t M, int64_t N, int64_t K, uint32_t flags, int32_t *splits);
 
 #ifdef __cplusplus

@@ -122,3 +122,35 @@ def weight_block_cols(w: torch.Tensor, kbs, pow2: bool = False):
     cols = np.concatenate([np.arange(kb * 128, (kb + 1) * 128) for kb in kbs])
     q, s = O.quant_weight_128x128(bf16_to_np(w[:, torch.from_numpy(cols)]), pow2)
     return cols, q, s
+
+
+def assert_gemm_close_whole(c_gpu: torch.Tensor, c_ref: np.ndarray, what: str = "", rows: int = 2048) -> dict:
+    """assert_gemm_close over a whole (large) output, compared in row chunks so
+    that the temporaries stay small: the same criteria (relative Frobenius
+    error, the per-element bound with rms(C_ref) of the whole output, no
+    non-finite values) computed over every element."""
+    c_ref = np.asarray(c_ref, np.float64)
+    rms = float(np.sqrt(np.mean(np.square(c_ref)))) if c_ref.size else 0.0
+    ref2 = diff2 = 0.0
+    viol = lit = nonfin = 0
+    emax = 0.0
+    for r0 in range(0, c_ref.shape[0], rows):
+        r1 = min(c_ref.shape[0], r0 + rows)
+        g = c_gpu[r0:r1].float().cpu().numpy().astype(np.float64)
+        ref = c_ref[r0:r1]
+        nonfin += int(np.sum(~np.isfinite(g)))
+        d = g - ref
+        err = np.abs(d)
+        diff2 += float(np.sum(np.square(d)))
+        ref2 += float(np.sum(np.square(ref)))
+        viol += int(np.sum(err > ABS_RMS * rms + BF16_HALF_ULP_REL * np.abs(ref)))
+        lit += int(np.sum(err > ABS_RMS * rms))
+        if err.size:
+            emax = max(emax, float(err.max()))
+    e = {"rel_frob": float(np.sqrt(diff2 / ref2)) if ref2 > 0 else float(np.sqrt(diff2)),
+         "max_err_over_rms": emax / rms if rms > 0 else 0.0, "violations": viol, "literal_violations": lit,
+         "nonfinite": nonfin, "n": int(c_ref.size)}
+    assert e["nonfinite"] == 0, (what, e)
+    assert e["rel_frob"] <= REL_FROB, (what, e)
+    assert e["violations"] == 0, (what, e)
+    return e

@@ -374,3 +374,22 @@ def test_workspace_size_and_plan(L):
 def _has_gpu():
     import torch
     return torch.cuda.is_available()
+
+
+def test_noalloc_validation(L):
+    """The no-allocation decode GEMM takes fp32 scales only: UE8M0 byte scales
+    (FP8_GEMM_SCALES_E8) are refused before anything launches, as are the
+    large-M paths and M > 256."""
+    f = L.fp8_blockscaled_gemm_skinny_noalloc
+
+    def call(M=8, flags=0, qa=A16):
+        return f(qa, 256, A16b, 8, A16c, 256, A16, A16b, 128, M, 128, 256, flags, NULL)
+
+    assert call(flags=0x2) == 9                   # E8 byte scales, AUTO path
+    assert call(flags=0x32) == 9                  # E8 byte scales, SKINNY path
+    assert call(flags=0x10) == 4                  # promote path
+    assert call(flags=0x21) == 4                  # MX path
+    assert call(qa=NULL) == 1
+    assert call(qa=MIS) == 3
+    assert call(M=0) == 0
+    assert call(M=300) == 2                       # beyond 256 tokens (ldsa < M first would also say SHAPE)
