@@ -832,6 +832,59 @@ def moe_measure(args, ops, stream, dev, flush, fp8_peak, hbm_peak):
             "gemm_kernel": "mx (grouped)" if pow2 else "promote (grouped)", "ms_per_step": total,
             "quant_gemm_tflops": flops / (total / 1e3) / 1e12, "projections": rows,
             "gpu_launches": 3 * len(projs) * args.steps}
+    out["wgrad"] = moe_wgrad_measure(args, ops, stream, dev, flush, fp8_peak, m, projs, offs)
+    return out
+
+
+def moe_wgrad_measure(args, ops, stream, dev, flush, fp8_peak, m, projs, offs):
+    """Weight gradients of the same experts, dW_g = dY_g^T X_g over each
+    expert's rows: the grouped 128x1 quantiser of dY and of X (each expert's
+    last token block padded with zeros) and the grouped wgrad GEMM, three
+    launches per projection for all 128 experts.  dY is drawn on the device
+    (N(0,1) x 1e-4; only the timing matters here, parity is tested
+    separately).  FLOPs are 2 T N K (T = 65536 expert-sorted rows)."""
+    import torch
+
+    G = len(m.offsets) - 1
+    offs32 = offs.to(torch.int32)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 91)
+    nb = (projs[0]["M"] + 127) // 128 + G
+    W = []
+    for P in projs:
+        T, N, K = P["M"], P["N"], P["K"]
+        dy = (torch.randn((T, N), generator=gen, device=dev) * 1e-4).to(torch.bfloat16)
+        W.append(dict(name=P["name"], T=T, N=N, K=K, dy=dy, x=P["a"],
+                      qg=torch.empty((N, 128 * nb), dtype=torch.uint8, device=dev),
+                      sg=torch.empty((nb, ops.round_up(N, 4)), dtype=torch.float32, device=dev),
+                      qx=torch.empty((K, 128 * nb), dtype=torch.uint8, device=dev),
+                      sx=torch.empty((nb, ops.round_up(K, 4)), dtype=torch.float32, device=dev),
+                      dw=torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)))
+    out = {"what": "per projection: grouped 128x1 quantiser of dY and of X, grouped wgrad GEMM (promote "
+                   "kernel, per-expert K ranges from device offsets); 3 launches for all experts",
+           "modes": {}}
+    for pow2 in (False, True):
+        mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
+        flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
+        calls = []
+        for P in W:
+            calls += [lambda P=P: ops.fp8_quant_act_128x1_grouped(P["dy"], offs32, P["qg"], P["sg"], mode, stream),
+                      lambda P=P: ops.fp8_quant_act_128x1_grouped(P["x"], offs32, P["qx"], P["sx"], mode, stream),
+                      lambda P=P: ops.fp8_blockscaled_grouped_gemm_wgrad(P["qg"], P["sg"], P["qx"], P["sx"], offs32,
+                                                                         P["T"], P["dw"], flags, stream)]
+        per, total = time_calls(args, stream, dev, flush, calls)
+        rows = {}
+        for i, P in enumerate(W):
+            qg_ms, qx_ms, g_ms = per[3 * i:3 * i + 3]
+            gf = 2.0 * P["T"] * P["N"] * P["K"]
+            rows[P["name"]] = {"quant_dy_ms": qg_ms, "quant_x_ms": qx_ms, "wgrad_ms": g_ms,
+                               "wgrad_tflops": gf / (g_ms / 1e3) / 1e12,
+                               "wgrad_frac_fp8": gf / (g_ms / 1e3) / 1e12 / fp8_peak,
+                               "quant_wgrad_tflops": gf / ((qg_ms + qx_ms + g_ms) / 1e3) / 1e12}
+        flops = sum(2.0 * P["T"] * P["N"] * P["K"] for P in W)
+        out["modes"]["pow2" if pow2 else "fp32"] = {
+            "ms_per_step": total, "quant_wgrad_tflops": flops / (total / 1e3) / 1e12, "projections": rows,
+            "gpu_launches": 3 * len(W) * args.steps}
     return out
 
 

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfp8bs.so")
 
-SOURCES = ["api.cu", "quant.cu", "quant_t.cu", "quant_pt.cu", "attn.cu", "gemm_promote.cu", "gemm_pair.cu", "gemm_mx.cu", "gemm_skinny.cu"]
+SOURCES = ["api.cu", "quant.cu", "quant_t.cu", "quant_pt.cu", "attn.cu", "gemm_promote.cu", "gemm_mx.cu", "gemm_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-std=c++17", "-lineinfo",

@@ -201,20 +201,6 @@ void fault_injection(uint64_t* wait_ns, int32_t* skip_first_load) {
     *skip_first_load = g_inject_skip.load(std::memory_order_relaxed);
 }
 
-// Dense fp32-scale GEMMs run on CTA pairs (gemm_pair.cu) when the device can
-// place them; FP8BS_PROMOTE_PAIR=0 selects the one-CTA promote kernel instead
-// (for comparison).
-bool promote_use_pair(int64_t M, int64_t N, int64_t K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    static int off = [] {
-        const char* e = std::getenv("FP8BS_PROMOTE_PAIR");
-        return (e && e[0] == '0') ? 1 : 0;
-    }();
-    return !off && pair_max_clusters() > 0;
-}
-
 }  // namespace fp8bs
 
 using namespace fp8bs;
@@ -310,6 +296,27 @@ fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
     if (fp8_status e = current_device(&d)) return e;
     return cuda_status(launch_quant_act_128x1(x, M, K, ldx, qt, ldqt, st, ldst, q, ldq, s, lds,
                                               mode == FP8_SCALE_POW2, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fp8_status fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx, const int32_t* offsets,
+                                      int32_t G, uint8_t* qt, int64_t ldqt, float* st, int64_t ldst,
+                                      fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (T < 0 || K <= 0 || (K % 128) || G < 1 || G > kMaxGroupedQuantExperts || T > INT32_MAX / 2 ||
+        K > (1ll << 30))
+        return FP8_ERR_SHAPE;
+    const int64_t nbmax = grouped_token_blocks(T, G);
+    if (nbmax > 65535) return FP8_ERR_SHAPE;
+    if (T == 0) return FP8_OK;
+    if (!x || !offsets || !qt || !st) return FP8_ERR_NULL;
+    if (ldx < K || ldqt < 128 * nbmax || ldst < K) return FP8_ERR_SHAPE;
+    if ((ldx % 8) || (ldqt % 16) || (ldst % 4) || !aligned16(x) || !aligned16(qt) || !aligned16(st) ||
+        (reinterpret_cast<uintptr_t>(offsets) % 4))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_act_128x1_grouped(x, T, K, ldx, offsets, G, qt, ldqt, st, ldst,
+                                                      mode == FP8_SCALE_POW2, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fp8_status fp8_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
@@ -467,6 +474,8 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace))) return FP8_ERR_WORKSPACE;
         a.workspace = workspace;
         a.ws_bytes = ws_bytes;
+        a.qb = qb;
+        a.ldb = ldb;
         if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, nt,
                                       CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
             return e;
@@ -483,18 +492,15 @@ fp8_status fp8_blockscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa,
         a.workspace = workspace;
         a.ws_bytes = ws_bytes;
     }
-    const bool pair = !mx && promote_use_pair(M, N, K);
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
         return e;
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    // the pair kernel's CTAs each load 64 of a tile's 128 B rows
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, pair ? 64u : (uint32_t)a.bn,
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
-    if (pair) return cuda_status(launch_gemm_pair(a, st));
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
@@ -540,13 +546,64 @@ fp8_status fp8_blockscaled_gemm_wgrad(const uint8_t* qa, int64_t lda, const floa
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, 128,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
         return e;
-    const bool pair = !mx && promote_use_pair(M, N, K);
-    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, pair ? 64u : (uint32_t)a.bn,
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (pair) return cuda_status(launch_gemm_pair(a, st));
     return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
+}
+
+fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                              const uint8_t* qb, int64_t ldb, const float* sb, int64_t ldsb,
+                                              const int32_t* offsets, int32_t G, int64_t T, void* c, int64_t ldc,
+                                              int64_t M, int64_t N, uint32_t flags, fp8_stream_t stream) {
+    if (flags & FP8_GEMM_SCALES_E8) return FP8_ERR_NOT_IMPLEMENTED;   // fp32 scales only
+    if (flags & ~kKnownFlags) return FP8_ERR_SCALE_MODE;
+    const uint32_t path = flags & FP8_GEMM_PATH_MASK;
+    if (path > FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
+    if (path == FP8_GEMM_PATH_MX || path == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    if (M < 0 || N < 0 || (M % 128) || (N % 128) || M > (1ll << 24) || N > (1ll << 24)) return FP8_ERR_SHAPE;
+    if (G < 1 || G > kMaxGroupedQuantExperts || T < 0 || T > INT32_MAX / 2) return FP8_ERR_SHAPE;
+    if ((int64_t)G * M > INT32_MAX) return FP8_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8_OK;
+    const int64_t kcap = 128 * grouped_token_blocks(T, G);   // padded token slots the quantiser may fill
+    if (!qa || !sa || !qb || !sb || !c || !offsets) return FP8_ERR_NULL;
+    if (lda < kcap || ldb < kcap || ldsa < M || ldsb < N || ldc < N) return FP8_ERR_SHAPE;
+    if ((lda % 16) || (ldb % 16) || (ldsa % 4) || (ldsb % 4) || (ldc % 8)) return FP8_ERR_ALIGN;
+    if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(c) ||
+        (reinterpret_cast<uintptr_t>(offsets) % 4))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    GemmArgs a{};
+    fault_injection(&a.wait_ns, &a.skip_first_load);
+    a.sa = sa;
+    a.ldsa = ldsa;
+    a.sb = sb;
+    a.ldsb = ldsb;
+    a.c = c;
+    a.ldc = ldc;
+    a.M = M;
+    a.N = N;
+    a.K = kcap;
+    a.offsets = offsets;
+    a.G = G;
+    a.kgroup = 1;
+    a.kg_tokens = T;
+    a.status = d->status;
+    a.sm_count = d->sm_count;
+    a.splits = 1;
+    a.bn = promote_tile_n(M, N, kcap, G);
+    if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, (uint64_t)G * M, ldc * 2, 32, 32,
+                                  CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
+        return e;
+    if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, kcap, M, lda, 128, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_a))
+        return e;
+    if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, kcap, N, ldb, 128, (uint32_t)a.bn,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
+        return e;
+    return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fp8_status fp8_tensorscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, const uint8_t* qb, int64_t ldb,
@@ -741,6 +798,8 @@ fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t* qa, int64_t lda, c
     a.sm_count = d->sm_count;
     a.splits = skinny_splits(M, N, K, d->sm_count);
     if (skinny_workspace_bytes(M, N, K, a.splits) > kNoAllocScratchBytes) return FP8_ERR_WORKSPACE;
+    a.qb = qb;
+    a.ldb = ldb;
     const int nt = skinny_tile_n(M);
     if (fp8_status e = tensor_map(qa, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 128, nt, CU_TENSOR_MAP_SWIZZLE_128B,
                                   &a.tm_a))

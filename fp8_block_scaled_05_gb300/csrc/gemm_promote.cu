@@ -118,14 +118,21 @@ __device__ __forceinline__ void record_timeout(int* status) {
 
 // ROWB: sb holds a scale per B row (sb[kb * ldsb + n]), so the promotion
 // multiplies by a per-column scale product (dense only).
-template <int BN, bool GROUPED, bool ROWB>
+// KGROUP (with ROWB; mixture-of-experts weight gradients): G independent
+// GEMMs C_g [M, N] = A_g B_g^T that reduce over each expert's own tokens:
+// the K-blocks of expert g are the padded token blocks P_g .. P_{g+1}-1 (P_g
+// = sum_{g' < g} ceil(M_g' / 128), M_g' from the device offsets over
+// kg_tokens tokens), the layout the grouped 128x1 quantiser writes.  Tiles
+// run expert by expert; C_g is rows g M .. g M + M - 1 of the output (M %
+// 128 == 0); an expert without tokens gets zeros.
+template <int BN, bool GROUPED, bool ROWB, bool KGROUP = false>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo,
-                   uint64_t wait_ns, int skip_first_load) {
+                   uint64_t wait_ns, int skip_first_load, int kg_tokens) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -134,6 +141,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
     float* sb_ring = reinterpret_cast<float*>(cum + MAX_GROUPS + 4);   // ROWB: [SRING][BN], 16-byte aligned
     static_assert(!(ROWB && GROUPED), "per-row B scales are dense only");
+    static_assert(!KGROUP || (ROWB && !GROUPED), "K-grouped tiles are the weight-gradient form");
 
     const int warp = (int)warp_id(), lane = (int)lane_id();
     const int KB = K / BK;
@@ -169,6 +177,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         if (GROUPED) {
             const int total = build_group_table<BM>(offsets, G, M, NT, cum);
             if (lane == 0) ctl->n_tiles = total;
+        } else if (KGROUP) {
+            // cum[g]: the first padded token block of expert g
+            build_group_table<BM>(offsets, G, kg_tokens, 1, cum);
+            if (lane == 0) ctl->n_tiles = G * ((M + BM - 1) / BM) * NT;
         } else if (lane == 0) {
             ctl->n_tiles = ((M + BM - 1) / BM) * NT;
         }
@@ -180,6 +192,26 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     const int n_tiles = ctl->n_tiles;
     const int n_items = work_items(n_tiles, split);
     volatile int32_t* abort_flag = &ctl->abort_flag;
+    const int tiles_per_expert = ((M + BM - 1) / BM) * NT;   // KGROUP
+    // Work item t and its tile (with KGROUP: the expert's K range and tile).
+    auto item_at = [&](int t) -> Item {
+        Item w = decode_item(t, split, KB);
+        if constexpr (KGROUP) {
+            const int g = w.tile / tiles_per_expert;
+            w.kb0 = cum[g];
+            w.kb1 = cum[g + 1];
+        }
+        return w;
+    };
+    auto tile_at = [&](const Item& w) -> Tile {
+        if constexpr (KGROUP) {
+            Tile tl = decode_tile<BM, BN, false>(w.tile % tiles_per_expert, M, N, cum, offsets, G);
+            tl.g = w.tile / tiles_per_expert;
+            return tl;
+        } else {
+            return decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+        }
+    };
 
     if constexpr (C::SPLIT_REGS) {
         if (warp < EPI_WARP0) regs_dealloc<C::REGS_CTRL>();
@@ -190,8 +222,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-                const Item w = decode_item(t, split, KB);
-                const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+                const Item w = item_at(t);
+                const Tile tl = tile_at(w);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, wait_ns)) {
@@ -222,7 +254,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-                const Item w = decode_item(t, split, KB);
+                const Item w = item_at(t);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     if ((it & 1) != me) continue;
                     const uint32_t s = it % C::STAGES, ph = (it / C::STAGES) & 1;
@@ -266,8 +298,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         uint32_t sit = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item w = decode_item(t, split, KB);
-            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+            const Item w = item_at(t);
+            const Tile tl = tile_at(w);
             const int nb0 = tl.n0 / 128;
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++sit) {
                 const uint32_t slot = sit % SRING, ph = (sit / SRING) & 1;
@@ -320,8 +352,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         bool ok = true;
         bool ready = false;   // tfull of K-block kbg already seen complete (early probe)
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item w = decode_item(t, split, KB);
-            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+            const Item w = item_at(t);
+            const Tile tl = tile_at(w);
             const int m = tl.m0 + row_in_tile;
             const int col0 = tl.n0 + sl * C::EPI_COLS;
             const bool vrow = m < tl.row_end;
@@ -504,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, tl.m0 + q * 32);
+                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, (KGROUP ? tl.g * M : 0) + tl.m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
@@ -542,11 +574,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     }
 }
 
-template <int BN, bool GROUPED, bool ROWB = false>
+template <int BN, bool GROUPED, bool ROWB = false, bool KGROUP = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<BN>;
     static DeviceOnce attr_done;     // kernel attributes set on this device
-    auto kern = k_gemm_promote<BN, GROUPED, ROWB>;
+    auto kern = k_gemm_promote<BN, GROUPED, ROWB, KGROUP>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done.test(dev)) {
@@ -561,10 +593,11 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         attr_done.set(dev);
     }
     const int64_t NT = (a.N + BN - 1) / BN;
-    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
+    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT
+                                  : ((a.M + BM - 1) / BM) * NT * (KGROUP ? a.G : 1);
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
-    if (!GROUPED) {
+    if (!GROUPED && !KGROUP) {
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kPromoteMaxParts);
         if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
             split.n_full = (int)tp.n_full;
@@ -576,7 +609,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     kern<<<grid, C::THREADS, smem_bytes<BN, ROWB>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
                                                            a.ldsb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
                                                      (int)a.K, a.offsets, a.G, a.status, split, a.qout,
-                                                     wait_bound(a), a.skip_first_load);
+                                                     wait_bound(a), a.skip_first_load, (int)a.kg_tokens);
     return cudaGetLastError();
 }
 
@@ -624,6 +657,12 @@ size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
 cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;
     const bool grouped = a.offsets != nullptr;
+    if (a.ldsb > 0 && a.kgroup) {   // per-expert weight gradients over the experts' token blocks
+        if (!grouped) return cudaErrorInvalidValue;
+        if (a.bn == 128) return promote::launch<128, false, true, true>(a, st);
+        if (a.bn == 256) return promote::launch<256, false, true, true>(a, st);
+        return cudaErrorInvalidValue;
+    }
     if (a.ldsb > 0) {   // a scale per B row (dense only)
         if (grouped) return cudaErrorInvalidValue;
         if (a.bn == 128) return promote::launch<128, false, true>(a, st);

@@ -77,6 +77,16 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt, int64_t ldqt,
                                    float* st, int64_t ldst, uint8_t* q, int64_t ldq, float* s, int64_t lds,
                                    bool pow2, cudaStream_t stream);
+// Grouped 128x1 quantiser (mixture-of-experts weight gradients): each
+// expert's tokens in 128x1 blocks of their own, written to padded token slots
+// (see quant_t.cu).  grouped_token_blocks(T, G): the padded blocks an
+// expert-sorted T-token batch can need at most (the grid, and the columns of
+// qt / 128 and rows of st the caller provides).
+constexpr int kMaxGroupedQuantExperts = 1024;
+inline int64_t grouped_token_blocks(int64_t T, int64_t G) { return (T + 127) / 128 + G; }
+cudaError_t launch_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx, const int32_t* offsets,
+                                           int32_t G, uint8_t* qt, int64_t ldqt, float* st, int64_t ldst, bool pow2,
+                                           cudaStream_t stream);
 cudaError_t launch_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
                                           float* s, uint8_t* qt, int64_t ldqt, float* st, bool pow2,
                                           cudaStream_t stream);
@@ -126,9 +136,13 @@ struct GemmArgs {
                                     // > 0: a scale per B row, sb[kb * ldsb + n] (dense promote / MX)
     void* c;
     int64_t ldc;
+    const uint8_t* qb;              // skinny: the weight codes, streamed with cp.async
+    int64_t ldb;
     int64_t M, N, K;
     const int32_t* offsets;         // grouped: [G+1] on device; nullptr for dense
     int32_t G;
+    int32_t kgroup;                 // promote wgrad: G GEMMs over the experts' padded token blocks
+    int64_t kg_tokens;              //   (tokens the offsets range over)
     void* workspace;
     size_t ws_bytes;
     int32_t splits;
@@ -164,14 +178,6 @@ constexpr int kPromoteMaxParts = 4, kMxMaxParts = 2;
 constexpr int kMxTileN = 256;   // MX kernel output tile width
 TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts);
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
-
-// Dense kernel with per-K-block promotion on CTA pairs (cta_group::2):
-// 256 x 128 tiles, a.tm_b with box {128, 64} (each CTA of a pair loads 64
-// of the tile's 128 B rows).  pair_max_clusters(): pairs that fit on the
-// current device at once (0 if the kernel cannot run there).
-int pair_max_clusters();
-cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t st);
-bool promote_use_pair(int64_t M, int64_t N, int64_t K);
 
 // Dense / grouped kernel for power-of-two scales: the tensor core applies the
 // scales as UE8M0 block scale factors (tcgen05.mma kind::mxf8f6f4); output

@@ -147,6 +147,23 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, bool val
                  : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy with an L2 eviction-priority
+// hint (a createpolicy value); both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16_hint(void *dst, const void *src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's most recent cp.async groups are
+// still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Arrives on `bar` once all of this thread's earlier cp.async copies have
 // landed (the barrier's expected count must include this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
@@ -431,123 +448,6 @@ __device__ __forceinline__ void regs_dealloc() {
 template <int N>
 __device__ __forceinline__ void regs_alloc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-// ----------------------------------------------------------------- CTA pairs (cta_group::2)
-// A cluster of two CTAs on two SMs computes one 256-row tile: each CTA holds
-// its own 128 rows of A and half of the tile's B rows in its shared memory,
-// and the even CTA (the leader) issues MMAs that read both CTAs' operands and
-// write each CTA's 128 rows of the result into that CTA's own TMEM.  Every
-// tcgen05 instruction of such a kernel takes .cta_group::2.
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Shared::cluster address of the object at shared::cta address `saddr` in
-// the CTA of cluster rank `rank` (the same offset in that CTA's shared memory).
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-// All threads of both CTAs: release this CTA's earlier memory operations to
-// the cluster and wait for every thread of the cluster to arrive.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster
-// address, which may lie in the other CTA of the pair.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// Non-blocking test with cluster-scope acquire: for barriers that the other
-// CTA of the pair (its threads, or its tensor core through a multicast
-// commit) arrives on.
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait with cluster-scope acquire (as mbar_wait).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-#pragma unroll 1
-    for (int i = 0; i < 1024; ++i)
-        if (mbar_test_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 1024; ++i)
-            if (mbar_test_wait_cluster(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
-// 2-D tiled load into this CTA's shared memory whose completion (transaction
-// bytes) is signalled on the mbarrier at shared::cluster address
-// `bar_cluster`, which may be in the other CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int32_t c0,
-                                                 int32_t c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Pair TMEM allocation: one warp of each CTA of the pair executes it; both
-// receive the same base address.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Pair MMA, issued by one thread of the leader CTA: M = 256 (128 rows from
-// each CTA's A at the descriptor's address), N from both CTAs' halves of B.
-__device__ __forceinline__ void umma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives once on the mbarrier at the same shared-memory offset in every CTA
-// of `cta_mask` when the pair MMAs this thread issued so far have completed.
-__device__ __forceinline__ void umma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Same, arriving on this CTA's own barrier only.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
 }
 
 // ----------------------------------------------------------------- programmatic dependent launch

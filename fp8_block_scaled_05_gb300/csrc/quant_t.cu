@@ -28,6 +28,7 @@
 
 #include "codec.cuh"
 #include "internal.h"
+#include "sched.cuh"
 
 namespace fp8bs {
 
@@ -120,18 +121,53 @@ __device__ __forceinline__ void store_transposed(const uint8_t *tcodes, uint8_t 
 // codes qt[k][m] and scales st[mb * ldst + k]; with ROWWISE also the 1x128
 // codes q[m][k] and scales s[kb * lds + m] of the same tile.
 // ---------------------------------------------------------------------------
-template <bool ROWWISE, bool POW2>
+//
+// GROUPED (mixture-of-experts weight gradients): x holds the tokens of G
+// experts sorted by expert, expert g on rows offsets[g] .. offsets[g+1]-1
+// (device array).  Each expert's tokens are blocked on their own, the last
+// block of an expert padded with zero rows, and the blocks are written to
+// consecutive token slots: blockIdx.y = b is the b-th padded block overall,
+// expert g's blocks are b = P_g .. P_{g+1}-1 with P_g = sum_{g' < g}
+// ceil(M_g' / 128), and its codes go to qt columns 128 b .. 128 b + 127 and
+// its scales to st[b * ldst + k].  Blocks past P_G do nothing.
+template <bool ROWWISE, bool POW2, bool GROUPED = false>
 __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const uint16_t *__restrict__ x, int64_t ldx,
                                                          uint8_t *__restrict__ qt, int64_t ldqt,
                                                          float *__restrict__ st, int64_t ldst,
                                                          uint8_t *__restrict__ q, int64_t ldq,
-                                                         float *__restrict__ s, int64_t lds, int64_t M) {
+                                                         float *__restrict__ s, int64_t lds, int64_t M,
+                                                         const int32_t *__restrict__ offsets = nullptr,
+                                                         int G = 0) {
     __shared__ __align__(16) uint8_t tcodes[kTT * kTT];
     __shared__ __align__(16) uint32_t colpart[8][16][4];   // per warp: packed |bf16| maxima of column pairs
     __shared__ float2 colscale[kTT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cg = lane & 15, rg = 2 * warp + (lane >> 4);
-    const int64_t k0 = (int64_t)blockIdx.x * kTT, m0 = (int64_t)blockIdx.y * kTT;
+    const int64_t k0 = (int64_t)blockIdx.x * kTT;
+    // m0: first input row of the block; rows at or past M are zeros; the
+    // transposed codes go to qt columns mo .. mo + 127
+    int64_t m0 = (int64_t)blockIdx.y * kTT, mo = m0;
+    if constexpr (GROUPED) {
+        __shared__ int32_t cum[kMaxGroupedQuantExperts + 1];
+        __shared__ int32_t total;
+        if (warp == 0) {
+            const int t = build_group_table<kTT>(offsets, G, (int)M, 1, cum);
+            if (lane == 0) total = t;
+        }
+        __syncthreads();
+        const int b = (int)blockIdx.y;
+        if (b >= total) return;   // past the last expert's blocks (the grid is an upper bound)
+        int lo = 0, hi = G;       // largest g with cum[g] <= b
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= b) lo = mid; else hi = mid;
+        }
+        int rlo, rhi;
+        group_rows(offsets, lo, (int)M, rlo, rhi);
+        m0 = rlo + (int64_t)(b - cum[lo]) * kTT;
+        M = rhi;                  // the expert's rows end here
+        mo = (int64_t)b * kTT;
+    }
 
     // rows past M (a ragged last token block) are zeros: they change no
     // block's amax and their transposed codes are zero
@@ -203,7 +239,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
         return scale_from_sr(sr.x, sr.y, POW2);
     });
     __syncthreads();
-    store_transposed(tcodes, qt, ldqt, k0, m0, warp, lane);
+    store_transposed(tcodes, qt, ldqt, k0, mo, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -264,7 +300,18 @@ cudaError_t launch_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t 
     const uint16_t *xp = static_cast<const uint16_t *>(x);
     auto kern = q != nullptr ? (pow2 ? k_quant_act_128x1<true, true> : k_quant_act_128x1<true, false>)
                              : (pow2 ? k_quant_act_128x1<false, true> : k_quant_act_128x1<false, false>);
-    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds, M);
+    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, q, ldq, s, lds, M, nullptr, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_128x1_grouped(const void *x, int64_t T, int64_t K, int64_t ldx, const int32_t *offsets,
+                                           int32_t G, uint8_t *qt, int64_t ldqt, float *st, int64_t ldst, bool pow2,
+                                           cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((unsigned)(K / kTT), (unsigned)grouped_token_blocks(T, G));
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    auto kern = pow2 ? k_quant_act_128x1<false, true, true> : k_quant_act_128x1<false, false, true>;
+    kern<<<grid, 256, 0, stream>>>(xp, ldx, qt, ldqt, st, ldst, nullptr, 0, nullptr, 0, T, offsets, G);
     return cudaGetLastError();
 }
 

@@ -27,12 +27,15 @@ def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", required=True,
                    choices=["quant_act", "quant_weight", "gemm", "grouped", "quant_act_t", "quant_weight_t", "wgrad",
-                            "pt_gemm", "attention"])
+                            "pt_gemm", "attention", "moe_wgrad"])
     p.add_argument("--dual", action="store_true", help="quant_act_t / quant_weight_t: also the other layout")
     p.add_argument("--M", type=int, default=4096)
     p.add_argument("--N", type=int, default=4096)
     p.add_argument("--K", type=int, default=4096)
     p.add_argument("--G", type=int, default=128, help="experts (grouped)")
+    p.add_argument("--moe", choices=["gate_up", "down"], default=None,
+                   help="grouped, moe_wgrad: the Qwen3-30B-A3B expert shapes and Zipf(1.1) top-8 routing of "
+                        "8192 tokens (overrides M, N, K, G)")
     p.add_argument("--pow2", action="store_true")
     p.add_argument("--path", default="auto", choices=list(ops.PATHS))
     p.add_argument("--iters", type=int, default=20)
@@ -106,6 +109,25 @@ def main(argv=None):
         kc4, vc4, qc3 = kc.view(B, Hkv, T, D), vc.view(B, Hkv, T, D), qc.view(B, Hq, D)
         run = lambda: ops.decode_attention(qc3, ssq, kc4, ssk, vc4, ssk, lens)  # noqa: E731
         work, unit = 2.0 * B * Hkv * T * D + 3.0 * B * Hq * D, "GB/s"
+    elif a.kernel == "moe_wgrad":
+        # grouped weight gradients dW_g [M, N] = dY_g^T X_g of the expert
+        # projection (gate_up: M 1536, N 2048; down: M 2048, N 768) over the
+        # Zipf-routed expert-sorted rows; operands from the grouped quantiser
+        from . import inputs as I
+        mc = I.moe_case(with_weights=False)
+        G, T = len(mc.offsets) - 1, int(mc.offsets[-1])
+        M, N = (1536, 2048) if (a.moe or "gate_up") == "gate_up" else (2048, 768)
+        K = T
+        offs = torch.from_numpy(mc.offsets).to(dev)
+        dy = (torch.randn((T, M), generator=g, device=dev) * 1e-4).to(torch.bfloat16)
+        x = torch.randn((T, N), generator=g, device=dev).to(torch.bfloat16)
+        qg, sg = ops.quant_act_t_grouped(dy, offs, a.pow2)
+        qx, sx = ops.quant_act_t_grouped(x, offs, a.pow2)
+        del dy, x
+        c = torch.empty((G, M, N), dtype=torch.bfloat16, device=dev)
+        flags = ops.FP8_GEMM_SCALES_POW2 if a.pow2 else 0
+        run = lambda: ops.fp8_blockscaled_grouped_gemm_wgrad(qg, sg, qx, sx, offs, T, c, flags)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
     elif a.kernel == "gemm":
         qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
         qw, sw = ops.quant_weight((torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16), a.pow2)
@@ -114,11 +136,18 @@ def main(argv=None):
         work, unit = 2.0 * M * N * K, "TFLOP/s"
     else:
         G = a.G
-        sizes = torch.full((G,), M // G, dtype=torch.int64)
-        sizes[: M - int(sizes.sum())] += 1
-        offs = torch.zeros(G + 1, dtype=torch.int32)
-        offs[1:] = torch.cumsum(sizes, 0)
-        offs = offs.to(dev)
+        if a.moe:
+            from . import inputs as I
+            mc = I.moe_case(with_weights=False)
+            G, M = len(mc.offsets) - 1, int(mc.offsets[-1])
+            N, K = (1536, 2048) if a.moe == "gate_up" else (2048, 768)
+            offs = torch.from_numpy(mc.offsets).to(dev)
+        else:
+            sizes = torch.full((G,), M // G, dtype=torch.int64)
+            sizes[: M - int(sizes.sum())] += 1
+            offs = torch.zeros(G + 1, dtype=torch.int32)
+            offs[1:] = torch.cumsum(sizes, 0)
+            offs = offs.to(dev)
         qa, sa = ops.quant_act(torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16), a.pow2)
         qw = torch.randint(0, 0x7E, (G, N, K), dtype=torch.uint8, device=dev, generator=g)
         sw = torch.rand((G, N // 128, K // 128), generator=g, device=dev) * 1e-3

@@ -71,6 +71,10 @@ SIGNATURES = {
     "fp8_last_device_status": (ctypes.c_int, [_vp]),
     "fp8_gemm_plan": (_u32, [_i64, _i64, _i64, _u32, ctypes.POINTER(_i32)]),
     "fp8_debug_inject": (ctypes.c_int, [_i32, ctypes.c_uint64]),
+    "fp8_quant_act_128x1_grouped": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i32, _vp, _i64, _vp, _i64,
+                                                   ctypes.c_int, _vp]),
+    "fp8_blockscaled_grouped_gemm_wgrad": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i32,
+                                                          _i64, _vp, _i64, _i64, _i64, _u32, _vp]),
 }
 
 _lib = None
@@ -215,6 +219,36 @@ def fp8_blockscaled_gemm_wgrad(qa, sa, qb, sb, c, flags: int = 0, workspace: tor
                                             _ptr(sb), sb.stride(0), _ptr(c), c.stride(0), M, N, K, int(flags),
                                             _ptr(workspace), ws_bytes, _stream(stream)),
            "fp8_blockscaled_gemm_wgrad")
+
+
+def fp8_quant_act_128x1_grouped(x: torch.Tensor, offsets: torch.Tensor, qt: torch.Tensor, st: torch.Tensor,
+                                mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
+    """x bf16 [T, K] expert-sorted; offsets int32 [G+1] (device); qt uint8
+    [K, >= 128 (ceil(T/128) + G)]; st fp32 [ceil(T/128) + G, >= K]."""
+    _need(x, torch.bfloat16, "x")
+    _need(offsets, torch.int32, "offsets")
+    _need(qt, torch.uint8, "qt")
+    _need(st, torch.float32, "st")
+    T, K = x.shape
+    _check(lib().fp8_quant_act_128x1_grouped(_ptr(x), T, K, x.stride(0), _ptr(offsets), offsets.numel() - 1,
+                                             _ptr(qt), qt.stride(0), _ptr(st), st.stride(0), int(mode),
+                                             _stream(stream)), "fp8_quant_act_128x1_grouped")
+
+
+def fp8_blockscaled_grouped_gemm_wgrad(qa, sa, qb, sb, offsets, T: int, c, flags: int = 0, stream=None) -> None:
+    """c bf16 [G, M, N] (or [G M, N]) = per-expert dY^T X from the grouped
+    128x1 operands (qa [M, slots], qb [N, slots])."""
+    _need(qa, torch.uint8, "qa")
+    _need(qb, torch.uint8, "qb")
+    _need(sa, torch.float32, "sa")
+    _need(sb, torch.float32, "sb")
+    _need(offsets, torch.int32, "offsets")
+    _need(c, torch.bfloat16, "c")
+    M, N = qa.shape[0], qb.shape[0]
+    _check(lib().fp8_blockscaled_grouped_gemm_wgrad(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb),
+                                                    qb.stride(0), _ptr(sb), sb.stride(0), _ptr(offsets),
+                                                    offsets.numel() - 1, T, _ptr(c), c.stride(-2), M, N, int(flags),
+                                                    _stream(stream)), "fp8_blockscaled_grouped_gemm_wgrad")
 
 
 def fp8_quant_act_1x128_e8(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
@@ -568,23 +602,36 @@ def decode_attention(q, sq, k_cache, sk, v_cache, sv, seq_lens, stream=None):
     return out
 
 
+def quant_act_t_grouped(x: torch.Tensor, offsets: torch.Tensor, pow2: bool = False, stream=None):
+    """Grouped 128x1 quantisation of expert-sorted x [T, K]: returns (qt uint8
+    [K, 128 (ceil(T/128) + G)], st fp32 [ceil(T/128) + G, round_up(K, 4)])."""
+    T, K = x.shape
+    nb = (T + 127) // 128 + offsets.numel() - 1
+    qt = torch.empty((K, 128 * nb), dtype=torch.uint8, device=x.device)
+    st = torch.empty((nb, max(round_up(K, 4), 4)), dtype=torch.float32, device=x.device)
+    fp8_quant_act_128x1_grouped(x, offsets, qt, st, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
+    return qt, st
+
+
 def moe_wgrad(dy: torch.Tensor, x: torch.Tensor, offsets, pow2: bool = False, stream=None):
     """Weight gradients of a mixture-of-experts layer, dW_g = dY_g^T X_g for
-    the expert-sorted token rows offsets[g] .. offsets[g+1]-1 (offsets: host
-    sequence of G+1 ints).  Each expert's rows are quantised in 128x1 blocks
-    of its own tokens (fp8_quant_act_128x1 pads the last block with zeros) and
-    run through the wgrad GEMM, one expert after another.  Returns bf16
-    [G, N, K]; experts without tokens get zeros."""
-    G = len(offsets) - 1
-    N, K = dy.shape[1], x.shape[1]
-    dw = torch.zeros((G, N, K), dtype=torch.bfloat16, device=dy.device)
-    for g in range(G):
-        lo, hi = int(offsets[g]), int(offsets[g + 1])
-        if hi <= lo:
-            continue
-        qt_dy, st_dy = quant_act_t(dy[lo:hi], pow2, stream=stream)
-        qt_x, st_x = quant_act_t(x[lo:hi], pow2, stream=stream)
-        wgrad(qt_dy, st_dy, qt_x, st_x, pow2, out=dw[g], stream=stream)
+    the expert-sorted token rows offsets[g] .. offsets[g+1]-1 (offsets: an
+    int32 device tensor or a host sequence of G+1 ints).  Each expert's rows
+    are quantised in 128x1 blocks of its own tokens (the last block padded
+    with zeros) by one grouped quantiser launch per operand, and one grouped
+    GEMM launch computes every expert's gradient.  Returns bf16 [G, N, K];
+    experts without tokens get zeros."""
+    if not isinstance(offsets, torch.Tensor):
+        offsets = torch.tensor([int(v) for v in offsets], dtype=torch.int32)
+    offsets = offsets.to(device=dy.device, dtype=torch.int32)
+    G = offsets.numel() - 1
+    T, N = dy.shape
+    K = x.shape[1]
+    qt_dy, st_dy = quant_act_t_grouped(dy, offsets, pow2, stream)
+    qt_x, st_x = quant_act_t_grouped(x, offsets, pow2, stream)
+    dw = torch.empty((G, N, K), dtype=torch.bfloat16, device=dy.device)
+    fp8_blockscaled_grouped_gemm_wgrad(qt_dy, st_dy, qt_x, st_x, offsets, T, dw,
+                                       FP8_GEMM_SCALES_POW2 if pow2 else 0, stream)
     return dw
 
 

@@ -257,6 +257,48 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
                                 fp8_stream_t stream);
 
 /*
+ * Mixture-of-experts weight gradients in two launches per operand pair
+ * (end-to-end FP8 training of the MoE models the recipe covers: upppp.jp
+ * NeMo RL FP8 article, §まとめ; greentreeone.com page, §Технический прорыв).
+ * For each expert g with token rows offsets[g] .. offsets[g+1]-1 of the
+ * expert-sorted dY [T, M] and X [T, N]:  dW_g [M, N] = dY_g^T X_g, every
+ * operand quantised in 128x1 blocks of that expert's own tokens (the last
+ * block padded with zero rows).
+ *
+ * fp8_quant_act_128x1_grouped: the 128x1 codes of each expert's tokens,
+ * transposed, in padded token slots: with P_g = sum_{g' < g} ceil(M_g' / 128),
+ * expert g's blocks are slots 128 P_g .. 128 P_{g+1} - 1, i.e. qt columns,
+ * and their scales rows P_g .. P_{g+1} - 1 of st.  Slots past P_G are not
+ * written.
+ *   x        device, bf16 [T, K] (row pitch ldx), tokens sorted by expert
+ *   offsets  device, int32 [G+1] (as fp8_blockscaled_grouped_gemm); G <= 1024
+ *   qt       device, uint8 [K][ldqt], ldqt >= 128 * (ceil(T/128) + G), % 16 == 0
+ *   st       device, fp32 [ceil(T/128) + G][ldst], ldst >= K, % 4 == 0
+ *   K % 128 == 0; ceil(T/128) + G <= 65535.
+ *
+ * fp8_blockscaled_grouped_gemm_wgrad: all G weight gradients in one launch,
+ *   C[g M + m, n] = bf16( sum over expert g's slots kb of
+ *                         sA[kb, m] sB[kb, n] sum_{k in kb} dec(qa[m, k]) dec(qb[n, k]) )
+ *   qa, sa   the grouped quantiser's output for dY (M rows of qa, ldsa >= M)
+ *   qb, sb   the same for X (N rows, ldsb >= N)
+ *   c        device, bf16 [G * M, N] (row pitch ldc): dW_g at rows g M ..; an
+ *            expert without tokens gets zeros
+ *   M, N multiples of 128 (0: nothing to do); T and offsets as given to the quantiser;
+ *   lda, ldb >= 128 * (ceil(T/128) + G).  flags: FP8_GEMM_SCALES_POW2 |
+ *   FP8_GEMM_PATH_AUTO or _PROMOTE (the per-K-block promotion kernel);
+ *   _MX, _SKINNY and FP8_GEMM_SCALES_E8 return FP8_ERR_NOT_IMPLEMENTED.
+ */
+FP8BS_API fp8_status fp8_quant_act_128x1_grouped(const void *x, int64_t T, int64_t K, int64_t ldx,
+                                                 const int32_t *offsets, int32_t G, uint8_t *qt, int64_t ldqt,
+                                                 float *st, int64_t ldst, fp8_scale_mode mode,
+                                                 fp8_stream_t stream);
+FP8BS_API fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t *qa, int64_t lda, const float *sa,
+                                                        int64_t ldsa, const uint8_t *qb, int64_t ldb,
+                                                        const float *sb, int64_t ldsb, const int32_t *offsets,
+                                                        int32_t G, int64_t T, void *c, int64_t ldc, int64_t M,
+                                                        int64_t N, uint32_t flags, fp8_stream_t stream);
+
+/*
  * Per-tensor dynamic scaling: one scale for the whole tensor, recomputed from
  * its current amax so that every value fits the FP8 range (ai.warp-studio.com
  * end-to-end FP8 RL article, §FP8強化学習における精度と安定性の確保).
@@ -498,7 +540,7 @@ FP8BS_API const char *fp8_status_string(fp8_status status);
 
 /*
  * Failure-path test hook (the pages have no counterpart).  Until called
- * again, GEMMs launched by this process on the promote, pair and skinny
+ * again, GEMMs launched by this process on the promote and skinny
  * kernels bound every wait inside the kernel by `wait_limit_ns` nanoseconds
  * (0: the default of 2 s; at most 2 s), and with skip_first_load != 0 their
  * TMA producer leaves out the first K-block's operands, so the waits on them

@@ -92,3 +92,22 @@ def gemm_ref(qa, sa, qw, sw, cols: int = 4096) -> np.ndarray:
         n1 = min(N, n0 + cols)
         out[:, n0:n1] = O.gemm_ref(qa, sa, qw[n0:n1], sw[n0 // 128:(n1 + 127) // 128])
     return out
+
+
+def _moe_wgrad_expert(args):
+    dy, x, pow2 = args
+    qg, sg = O.quant_act_128x1(dy, pow2)
+    qx, sx = O.quant_act_128x1(x, pow2)
+    return qg, sg, qx, sx, O.wgrad_ref(qg, sg, qx, sx)
+
+
+def moe_wgrad_experts(dy: np.ndarray, x: np.ndarray, offsets, pow2: bool = False):
+    """Yields (g, qt_dy, st_dy, qt_x, st_x, dW_g) for every expert with
+    tokens: O.quant_act_128x1 of the expert's rows of dy and x, and
+    O.wgrad_ref of them (fp64), one expert per task."""
+    offsets = [int(v) for v in offsets]
+    live = [g for g in range(len(offsets) - 1) if offsets[g + 1] > offsets[g]]
+    tasks = ((dy[offsets[g]:offsets[g + 1]], x[offsets[g]:offsets[g + 1]], pow2) for g in live)
+    for g, r in zip(live, pool().map(_moe_wgrad_expert, tasks)):
+        yield (g,) + tuple(r)
+

@@ -393,3 +393,58 @@ def test_noalloc_validation(L):
     assert call(qa=MIS) == 3
     assert call(M=0) == 0
     assert call(M=300) == 2                       # beyond 256 tokens (ldsa < M first would also say SHAPE)
+
+
+def test_quant_act_128x1_grouped_validation(L):
+    """Grouped 128x1 quantiser: ldqt must hold 128 (ceil(T/128) + G) slots."""
+    f = L.fp8_quant_act_128x1_grouped
+    ok = dict(x=A16, T=300, K=256, ldx=256, offs=A16b, G=3, qt=A16c, ldqt=768, st=A16, ldst=256, mode=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["T"], a["K"], a["ldx"], a["offs"], a["G"], a["qt"], a["ldqt"], a["st"], a["ldst"],
+                 a["mode"], NULL)
+
+    assert call(x=NULL) == 1
+    assert call(offs=NULL) == 1
+    assert call(K=200) == 2
+    assert call(G=0) == 2
+    assert call(G=1025) == 2
+    assert call(ldqt=640) == 2                    # 128 x (3 + 3) slots needed
+    assert call(ldst=128) == 2                    # ldst < K
+    assert call(ldqt=776) == 3                    # row pitch not a multiple of 16 bytes
+    assert call(offs=A16b + 2) == 3               # int32 offsets misaligned
+    assert call(mode=7) == 4
+    assert call(T=0) == 0                         # nothing to quantise
+    if not _has_gpu():
+        assert call() == 6
+
+
+def test_grouped_wgrad_validation(L):
+    """Grouped weight-gradient GEMM: fp32 scales on the promote path only."""
+    f = L.fp8_blockscaled_grouped_gemm_wgrad
+    ok = dict(qa=A16, lda=768, sa=A16b, ldsa=256, qb=A16c, ldb=768, sb=A16, ldsb=128, offs=A16b, G=3, T=300,
+              c=A16c, ldc=128, M=256, N=128, flags=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["qa"], a["lda"], a["sa"], a["ldsa"], a["qb"], a["ldb"], a["sb"], a["ldsb"], a["offs"], a["G"],
+                 a["T"], a["c"], a["ldc"], a["M"], a["N"], a["flags"], NULL)
+
+    assert call(flags=0x2) == 9                   # UE8M0 byte scales
+    assert call(flags=0x20) == 9                  # MX path
+    assert call(flags=0x30) == 9                  # skinny path
+    assert call(M=200) == 2
+    assert call(G=0) == 2
+    assert call(lda=640) == 2                     # fewer slots than the quantiser may fill
+    assert call(ldsb=64) == 2                     # ldsb < N
+    assert call(ldc=64) == 2                      # ldc < N
+    assert call(offs=NULL) == 1
+    assert call(sb=NULL) == 1
+    assert call(lda=776) == 3
+    assert call(c=A16c + 8) == 3
+    assert call(M=0) == 0                         # empty output
+    if not _has_gpu():
+        assert call() == 6
+        assert call(flags=0x11) == 6              # promote path, pow2 scales
+

@@ -6,8 +6,8 @@ returns.  Here the bound is shortened to 20 ms and the TMA producer leaves
 out the first K-block's operands (fp8_debug_inject), so the waits on them run
 out for certain: the status word must read FP8_ERR_TIMEOUT, and afterwards a
 normal call on the same CUDA context must still compute the right result.
-Covered: the one-CTA promote kernel, the CTA-pair kernel and the decode
-(skinny) kernel.
+Covered: the promote kernel (plain and with its fused output quantisation)
+and the decode (skinny) kernel with one and two token chunks.
 """
 from __future__ import annotations
 
@@ -45,15 +45,14 @@ def _operands(M, N, K, seed):
     return dev, O.gemm_ref(qa, sa, qw, sw)
 
 
-@pytest.mark.parametrize("kernel,M,N,K", [("promote", 384, 512, 1024), ("pair", 512, 512, 1024),
-                                          ("skinny", 8, 1024, 2048)])
+@pytest.mark.parametrize("kernel,M,N,K", [("promote", 384, 512, 1024), ("promote_fused", 384, 512, 1024),
+                                          ("skinny", 8, 1024, 2048), ("skinny", 200, 512, 4096)])
 def test_wait_timeout_is_reported_and_the_context_survives(ops, kernel, M, N, K):
     (qa, sa, qw, sw), ref = _operands(M, N, K, seed=M + K)
     ws = ops.workspace_for(M, N, K, 1, "cuda")
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    if kernel == "promote":
-        # the GEMM with fused output quantisation runs on the one-CTA promote
-        # kernel (plain dense fp32-scale GEMMs run on CTA pairs)
+    if kernel == "promote_fused":
+        # the promote kernel with the next layer's quantisation in its epilogue
         qc = torch.empty((M, N), dtype=torch.uint8, device="cuda")
         sc = torch.empty((N // 128, (M + 3) // 4 * 4), dtype=torch.float32, device="cuda")
 

@@ -309,3 +309,53 @@ def test_moe_wgrad(ops, pow2):
             assert np.all(got[g] == 0)
         else:
             assert_gemm_close(got[g], ref[g], f"moe wgrad expert {g}")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_act_128x1_grouped_layout(ops, pow2):
+    """The grouped 128x1 quantiser: expert g's tokens go to padded slots
+    128 P_g .. 128 P_{g+1} - 1 (P_g = blocks of the experts before it), each
+    expert's last block padded with zero codes; codes and scales bit-exact
+    with the oracle's per-expert quantisation.  Experts: empty, 5 tokens,
+    exactly 128, 256, 39, 1 and 256 tokens; the edge-case columns (an all-zero
+    block, a subnormal amax, a tiny block, a huge value) are planted."""
+    offs = [0, 0, 5, 133, 389, 389, 428, 429, 685]
+    T, K = offs[-1], 384
+    x = _edge_act(768, K, seed=91)[:T].contiguous()
+    qt, st = ops.quant_act_t_grouped(x.cuda(), torch.tensor(offs, dtype=torch.int32, device="cuda"), pow2)
+    _sync_ok(ops)
+    qt, st = qt.cpu().numpy(), st.cpu().numpy()
+    xn = bf16_to_np(x)
+    P = 0
+    for g in range(len(offs) - 1):
+        lo, hi = offs[g], offs[g + 1]
+        nb = (hi - lo + 127) // 128
+        if nb:
+            q_o, s_o = O.quant_act_128x1(xn[lo:hi], pow2)
+            assert np.array_equal(qt[:, 128 * P:128 * (P + nb)], q_o), f"codes of expert {g}"
+            assert np.array_equal(st[P:P + nb, :K], s_o.T), f"scales of expert {g}"
+        P += nb
+
+
+def test_moe_wgrad_one_expert_matches_dense_wgrad(ops):
+    """With a single expert holding every token the grouped path is the dense
+    weight gradient: the same codes, scales and (to the bit) the same dW."""
+    T, N, K = 300, 256, 384
+    x = _act(93, (T, K)).cuda()
+    dy = _grad(94, (T, N)).cuda()
+    dw = ops.moe_wgrad(dy, x, [0, T])
+    qt_dy, st_dy = ops.quant_act_t(dy)
+    qt_x, st_x = ops.quant_act_t(x)
+    ref = ops.wgrad(qt_dy, st_dy, qt_x, st_x)
+    _sync_ok(ops)
+    assert torch.equal(dw[0].view(torch.int16), ref.view(torch.int16))
+
+
+def test_moe_wgrad_no_tokens(ops):
+    """T = 0: nothing to quantise, every expert's gradient is zero."""
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    dy = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    dw = ops.moe_wgrad(dy, x, [0, 0, 0, 0])
+    _sync_ok(ops)
+    assert dw.shape == (3, 128, 256) and not torch.any(dw.float() != 0)
+

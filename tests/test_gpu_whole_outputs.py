@@ -15,7 +15,8 @@ the layers the pages measure on):
     C of o_proj, both modes;
   * decode, M in {1, 8, 64, 256} at both shapes: whole weight codes and C;
   * Qwen3-30B-A3B experts (Zipf routing): codes, scales and whole C of both
-    grouped GEMMs, both modes;
+    grouped GEMMs, both modes; the gate+up experts' weight gradients (grouped
+    128x1 quantisers and the grouped wgrad GEMM), both modes;
   * Llama gate+up backward: the dual-layout quantisers' codes and scales,
     whole dX (dgrad on W^T codes) and whole dW (wgrad on 128x1 operands),
     both modes.
@@ -162,6 +163,40 @@ def test_moe_whole_grouped_output(ops, proj, pow2):
     del qa, sa, qw, sw
     ref = O.grouped_gemm_ref(qa_o, sa_o, m.offsets, qw_o.reshape(G, N, K), sw_o.reshape(G, N // 128, K // 128))
     assert_gemm_close_whole(c, ref, f"moe {proj} pow2={pow2}")
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_moe_wgrad_whole(ops, pow2):
+    """Weight gradients of the gate+up experts, dW_g = dY_g^T X_g over the
+    Zipf-routed expert-sorted rows (65536 rows, 128 experts): both grouped
+    128x1 quantisers and the grouped wgrad GEMM, every code, scale and dW
+    element of every expert against the oracle's per-expert quantisation and
+    wgrad (dY ~ Student-t, nu = 4, x 1e-4)."""
+    m = _moe_case()
+    x = m.a_gate_up
+    T, K = x.shape
+    N = m.w_gate_up.shape[1]
+    G = len(m.offsets) - 1
+    dy = (I.student_t_bf16(I.stream(7, 85), (T, N), nu=4.0).float() * 1e-4).to(torch.bfloat16)
+    offs = torch.from_numpy(m.offsets.astype(np.int32)).cuda()
+    qt_dy, st_dy = ops.quant_act_t_grouped(dy.cuda(), offs, pow2)
+    qt_x, st_x = ops.quant_act_t_grouped(x.cuda(), offs, pow2)
+    dw = torch.empty((G, N, K), dtype=torch.bfloat16, device="cuda")
+    ops.fp8_blockscaled_grouped_gemm_wgrad(qt_dy, st_dy, qt_x, st_x, offs, T, dw,
+                                           ops.FP8_GEMM_SCALES_POW2 if pow2 else 0)
+    _sync_ok(ops)
+    live = set()
+    blocks = np.cumsum([0] + [(int(m.offsets[g + 1]) - int(m.offsets[g]) + 127) // 128 for g in range(G)])
+    for g, qg, sg, qx, sx, ref in par.moe_wgrad_experts(bf16_to_np(dy), bf16_to_np(x), m.offsets, pow2):
+        live.add(g)
+        b0, b1 = int(blocks[g]), int(blocks[g + 1])
+        assert torch.equal(qt_dy[:, 128 * b0:128 * b1].cpu(), torch.from_numpy(qg)), f"dY codes, expert {g}"
+        assert torch.equal(qt_x[:, 128 * b0:128 * b1].cpu(), torch.from_numpy(qx)), f"X codes, expert {g}"
+        assert np.array_equal(st_dy[b0:b1, :N].cpu().numpy(), sg.T), f"dY scales, expert {g}"
+        assert np.array_equal(st_x[b0:b1, :K].cpu().numpy(), sx.T), f"X scales, expert {g}"
+        assert_gemm_close_whole(dw[g], ref, f"moe wgrad expert {g} pow2={pow2}")
+    for g in set(range(G)) - live:
+        assert not torch.any(dw[g].float() != 0), f"expert {g} has no tokens"
 
 
 # ------------------------------------------------------------ Llama gate+up backward
