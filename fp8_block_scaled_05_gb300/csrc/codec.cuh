@@ -139,26 +139,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)r;
 }
 
-// Codes of two elements, e4m3(RN(x/s)) each.
-//
-// Fast path for mode 0: q0 = RN(x r) is within 1.5 ulp of x/s, so the
-// correctly rounded quotient t = RN(x/s) is within 2 ulp of q0 and lies
-// strictly between q0 (1 - 2^-21) and q0 (1 + 2^-21) (both products, rounded,
-// stay at least 3.5 ulp away from q0).  E4M3 conversion is monotone, so when
-// those two ends convert to the same code, t converts to it as well.  Only
-// pairs whose interval contains an E4M3 rounding boundary (a few in a
-// million) take the two-step corrected quotient.
-__device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
-    if (bs.mode == 1) return e4m3x2(xa * bs.r, xb * bs.r);
-    if (bs.mode == 0) {
-        const float qa = xa * bs.r, qb = xb * bs.r;
-        constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
-        const uint32_t lo = e4m3x2(qa * kLo, qb * kLo), hi = e4m3x2(qa * kHi, qb * kHi);
-        if (lo == hi) return lo;
-    }
-    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
-}
-
 // Both elements of a pair times one factor, as one packed multiply (each
 // lane an IEEE mul.rn.f32, so the products equal two scalar multiplies).
 __device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float &pb) {
@@ -167,6 +147,31 @@ __device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float
     asm("mov.b64 %0, {%1, %1};" : "=l"(k) : "f"(f));
     asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(k));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(x));
+}
+
+// Codes of two elements, e4m3(RN(x/s)) each.
+//
+// Fast path for mode 0: q0 = RN(x r) is within 1.5 ulp of x/s, so the
+// correctly rounded quotient t = RN(x/s) is within 2 ulp of q0 and lies
+// strictly between q0 (1 - 2^-21) and q0 (1 + 2^-21) (both products, rounded,
+// stay at least 3.5 ulp away from q0).  E4M3 conversion is monotone, so when
+// those two ends convert to the same code, t converts to it as well.  Only
+// pairs whose interval contains an E4M3 rounding boundary (a few in a
+// million) take the two-step corrected quotient.  The three products of the
+// pair (q0 and the two ends) are packed multiplies, one per product pair.
+__device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
+    float qa, qb;
+    mul2(xa, xb, bs.r, qa, qb);
+    if (bs.mode == 1) return e4m3x2(qa, qb);
+    if (bs.mode == 0) {
+        constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
+        float la, lb, ha, hb;
+        mul2(qa, qb, kLo, la, lb);
+        mul2(qa, qb, kHi, ha, hb);
+        const uint32_t lo = e4m3x2(la, lb), hi = e4m3x2(ha, hb);
+        if (lo == hi) return lo;
+    }
+    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
 }
 
 // Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes).
