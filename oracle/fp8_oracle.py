@@ -27,10 +27,16 @@ What it computes, and where each step comes from:
 
 Readings where the pages are silent (each also listed in the design notes):
 scale = amax/448 rounded to fp32; an all-zero block gets scale 1; the cast
-divides by the scale (x/s, IEEE fp32) before rounding to E4M3 with
-round-to-nearest-even and saturation at +-448; the power-of-two scale is
-2**ceil(log2(amax/448)) with the exponent clamped to [-127, 127]; the GEMM
-reference is dequantise-then-multiply in fp64.
+multiplies by the reciprocal factor r = 448/amax rounded to fp32 (RN(x r),
+then E4M3 with round-to-nearest-even and saturation at +-448) -- the pages
+give the scale as amax/448 and leave open whether the cast divides by it or
+multiplies by its reciprocal; where 448/amax overflows fp32 (amax below
+448 * 2**-128) the cast divides by the scale instead.  A cast with a given
+scale s (not from an amax) multiplies by RN(1/s), or divides where that
+overflows.  The power-of-two scale is 2**ceil(log2(amax/448)) with the
+exponent clamped to [-127, 127], and its cast multiplies by 2**-e, which is
+the quotient exactly.  The GEMM reference is dequantise-then-multiply in
+fp64.
 
 Every function below is pinned by the CPU tests in tests/test_oracle_pins.py
 and (training-side functions) tests/test_oracle_pins_training.py, (per-tensor
@@ -51,7 +57,7 @@ __all__ = [
     "E4M3_MAX", "QBLOCK",
     "e4m3_decode", "e4m3_encode", "bf16_bits_to_f32",
     "block_amax_act", "block_amax_weight",
-    "scale_from_amax_fp32", "scale_from_amax_pow2", "scale_from_amax",
+    "scale_from_amax_fp32", "scale_from_amax_pow2", "scale_from_amax", "recip_from_amax", "recip_from_scale",
     "quant_act_1x128", "quant_weight_128x128",
     "dequant_act", "dequant_weight",
     "gemm_ref", "gemm_ref_rows", "grouped_gemm_ref",
@@ -177,13 +183,36 @@ def scale_from_amax(amax, pow2: bool) -> np.ndarray:
     return scale_from_amax_pow2(amax) if pow2 else scale_from_amax_fp32(amax)
 
 
+def recip_from_amax(amax, pow2: bool) -> np.ndarray:
+    """The cast's factor r: fp32 mode RN(448 / amax) (IEEE float32 division;
+    +inf where it overflows), 1 for amax == 0; power-of-two mode 2**-e, the
+    exact reciprocal of the scale."""
+    amax = np.asarray(amax, dtype=np.float32)
+    if pow2:
+        return (np.float64(1.0) / scale_from_amax_pow2(amax).astype(np.float64)).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        r = np.float32(E4M3_MAX) / amax
+    return np.where(amax > 0, r, np.float32(1.0)).astype(np.float32)
+
+
+def recip_from_scale(s) -> np.ndarray:
+    """The cast's factor for a given scale s: RN(1 / s) (+inf where it overflows)."""
+    with np.errstate(divide="ignore", over="ignore"):
+        return (np.float32(1.0) / np.asarray(s, dtype=np.float32)).astype(np.float32)
+
+
 # --------------------------------------------------------------------------
 # Quantisers
 # --------------------------------------------------------------------------
-def _cast(x: np.ndarray, s_broadcast: np.ndarray) -> np.ndarray:
-    """codes = e4m3(RN_fp32(x / s)) elementwise (IEEE float32 division)."""
-    q32 = (x.astype(np.float32) / s_broadcast.astype(np.float32)).astype(np.float32)
-    return e4m3_encode(q32)
+def _cast(x: np.ndarray, s_broadcast: np.ndarray, r_broadcast: np.ndarray) -> np.ndarray:
+    """codes = e4m3(RN_fp32(x * r)) elementwise (IEEE float32 multiply), or
+    e4m3(RN_fp32(x / s)) where r is not finite (IEEE float32 division)."""
+    x = x.astype(np.float32)
+    r = r_broadcast.astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        prod = (x * r).astype(np.float32)
+        quot = (x / s_broadcast.astype(np.float32)).astype(np.float32)
+    return e4m3_encode(np.where(np.isfinite(r), prod, quot))
 
 
 def quant_act_1x128(x: np.ndarray, pow2: bool = False):
@@ -191,27 +220,32 @@ def quant_act_1x128(x: np.ndarray, pow2: bool = False):
 
     x: float32 [M, K] (bf16 values).  Returns (q uint8 [M, K],
     s float32 [M, K/128]) where s[m, kb] is the scale of row m, columns
-    kb*128 .. kb*128+127, and q = e4m3(x / s).  (The library stores the
+    kb*128 .. kb*128+127, and q = e4m3(RN(x r)) with r = RN(448 / amax) of
+    the block (the quotient x / s where r overflows; x 2**-e exactly for
+    power-of-two scales).  (The library stores the
     scales K-block-major, s[kb][m]; that is a layout choice, the values are
     these.)
     """
     x = np.asarray(x, dtype=np.float32)
     M, K = x.shape
-    s = scale_from_amax(block_amax_act(x), pow2)
-    sb = np.repeat(s, QBLOCK, axis=1)
-    return _cast(x, sb), s
+    amax = block_amax_act(x)
+    s = scale_from_amax(amax, pow2)
+    r = recip_from_amax(amax, pow2)
+    return _cast(x, np.repeat(s, QBLOCK, axis=1), np.repeat(r, QBLOCK, axis=1)), s
 
 
 def quant_weight_128x128(w: np.ndarray, pow2: bool = False):
     """128x128 weight quantisation.
 
     w: float32 [N, K] (bf16 values).  Returns (q uint8 [N, K],
-    s float32 [N/128, K/128]) with q = e4m3(w / s) tile by tile.
+    s float32 [N/128, K/128]) with q the cast of quant_act_1x128 tile by tile.
     """
     w = np.asarray(w, dtype=np.float32)
-    s = scale_from_amax(block_amax_weight(w), pow2)
-    sb = np.repeat(np.repeat(s, QBLOCK, axis=0), QBLOCK, axis=1)
-    return _cast(w, sb), s
+    amax = block_amax_weight(w)
+    s = scale_from_amax(amax, pow2)
+    r = recip_from_amax(amax, pow2)
+    grow = lambda t: np.repeat(np.repeat(t, QBLOCK, axis=0), QBLOCK, axis=1)  # noqa: E731
+    return _cast(w, grow(s), grow(r)), s
 
 
 # --------------------------------------------------------------------------
@@ -295,8 +329,9 @@ def quant_act_128x1(x: np.ndarray, pow2: bool = False):
     """128x1 (column-wise) activation quantisation, the wgrad operand.
 
     x: float32 [M, K] (bf16 values), M tokens.  The block of column k, tokens
-    mb*128 .. mb*128+127 gets scale s[mb, k] from its own amax, and
-    q[m, k] = e4m3(x[m, k] / s[m/128, k]).  Returned transposed, the way the
+    mb*128 .. mb*128+127 gets scale s[mb, k] from its own amax, and q[m, k]
+    is x[m, k] cast with that block's scale (as in quant_act_1x128).
+    Returned transposed, the way the
     wgrad GEMM reads them (token-contiguous rows): (qt uint8 [K, Mp] with
     qt[k, m] = q[m, k], st float32 [K, Mp/128] with st[k, mb] = s[mb, k]).
     A token count M that is not a multiple of 128 is padded with zero rows
@@ -309,8 +344,10 @@ def quant_act_128x1(x: np.ndarray, pow2: bool = False):
         xp = np.zeros(((M + QBLOCK - 1) // QBLOCK * QBLOCK, K), np.float32)
         xp[:M] = x
         x = xp
-    s = scale_from_amax(block_amax_col(x), pow2)
-    q = _cast(x, np.repeat(s, QBLOCK, axis=0))
+    amax = block_amax_col(x)
+    s = scale_from_amax(amax, pow2)
+    r = recip_from_amax(amax, pow2)
+    q = _cast(x, np.repeat(s, QBLOCK, axis=0), np.repeat(r, QBLOCK, axis=0))
     return np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
 
 
@@ -383,12 +420,13 @@ def quant_per_tensor(x: np.ndarray, pow2: bool = False):
     """Per-tensor quantisation of a float32 matrix (bf16 values).
 
     Returns (q uint8 of x's shape, s float32 scalar): s from max |x| over the
-    whole tensor, q = e4m3(x / s).
+    whole tensor, q the block cast with that scale (x times RN(448/amax)).
     """
     x = np.asarray(x, dtype=np.float32)
     amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
     s = scale_from_amax(np.array([amax], np.float32), pow2)[0]
-    return _cast(x, np.full(x.shape, s, np.float32)), np.float32(s)
+    r = recip_from_amax(np.array([amax], np.float32), pow2)[0]
+    return _cast(x, np.full(x.shape, s, np.float32), np.full(x.shape, r, np.float32)), np.float32(s)
 
 
 def gemm_per_tensor_ref(qa, sa, qb, sb) -> np.ndarray:
@@ -410,9 +448,11 @@ def gemm_per_tensor_ref(qa, sa, qb, sb) -> np.ndarray:
 # computes softmax(q.K^T / sqrt(D)) V, here in float64.
 # --------------------------------------------------------------------------
 def quant_with_scale(x: np.ndarray, s) -> np.ndarray:
-    """Codes of x under a given fp32 scale: e4m3(RN_fp32(x / s))."""
+    """Codes of x under a given fp32 scale: e4m3(RN_fp32(x * RN(1/s))), or
+    e4m3(RN_fp32(x / s)) where 1/s overflows."""
     x = np.asarray(x, dtype=np.float32)
-    return _cast(x, np.full(x.shape, np.float32(s), np.float32))
+    r = recip_from_scale(np.float32(s))
+    return _cast(x, np.full(x.shape, np.float32(s), np.float32), np.full(x.shape, r, np.float32))
 
 
 def decode_attention_ref(q, sq, k_cache, sk, v_cache, sv, seq_lens) -> np.ndarray:

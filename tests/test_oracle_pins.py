@@ -233,6 +233,34 @@ def _bf16_round(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).float().numpy()
 
 
+def expected_cast(x, s, amax=None, pow2=False) -> np.ndarray:
+    """The float32 value the cast rounds to E4M3, from exact arithmetic.
+
+    Power-of-two scale: the quotient x / s (exact in float64, rounded once).
+    fp32 scale: r = RN(448 / amax) when the scale comes from an amax (amax 0:
+    r = 1), r = RN(1 / s) for a given scale -- a float64 quotient rounded to
+    float32 is the correctly rounded float32 quotient (Figueroa: 53 >= 2*24 +
+    2) -- then RN(x r), the float64 product of two float32 values being exact.
+    Where r overflows float32 the quotient x / s, rounded once."""
+    x64 = np.asarray(x, np.float32).astype(np.float64)
+    if pow2:
+        return (x64 / np.float64(s)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        if amax is None:
+            r = np.float32(np.float64(1.0) / np.float64(s))
+        else:
+            r = np.float32(1.0) if amax == 0 else np.float32(np.float64(448.0) / np.float64(amax))
+    if np.isfinite(r):
+        return (x64 * np.float64(r)).astype(np.float32)
+    return (x64 / np.float64(s)).astype(np.float32)
+
+
+# amax 1.0 and the element 2**-16: 2**-16 * 448 = 3.5 * 2**-9 is an exact
+# E4M3 tie (rounds to the even code 0x04), while 2**-16 / RN(1/448) lies just
+# off it, so a cast that divides by the stored scale gives another code here.
+TIE_AMAX, TIE_X = 1.0, 2.0 ** -16
+
+
 def _act_sample(seed=3, M=37, K=640):
     rng = np.random.Generator(np.random.PCG64(seed))
     x = rng.standard_normal((M, K)).astype(np.float32)
@@ -241,13 +269,16 @@ def _act_sample(seed=3, M=37, K=640):
     x[4, 256:384] = 0.0
     x[4, 300] = -2.0 ** -130                  # a block whose amax is a bf16 subnormal
     x[5, :128] *= 1e-30
+    x[6, :128] = np.clip(x[6, :128] * 0.25, -0.9, 0.9)
+    x[6, 0], x[6, 1] = TIE_AMAX, TIE_X        # the cast multiplies by RN(448/amax), not divides
     return _bf16_round(x)
 
 
 def check_act_quant(quant):
-    """Codes against exact rational arithmetic, block by block:
-    amax element -> +-448 (fp32 mode), and every code equals the nearest-even
-    E4M3 rounding of the correctly rounded float32 quotient x/s."""
+    """Codes against exact arithmetic, block by block: amax element -> +-448
+    (fp32 mode), and every code equals the nearest-even E4M3 rounding of
+    RN(x RN(448/amax)) (fp32 scales; the quotient x/s where the reciprocal
+    overflows) or of x/s (power-of-two scales), see expected_cast."""
     x = _act_sample()
     for pow2 in (False, True):
         q, s = quant(x, pow2=pow2)
@@ -263,9 +294,7 @@ def check_act_quant(quant):
                     np.array([amax], np.float32))[0]
                 if si != float(want_s):
                     return False
-                # Figueroa: float64 quotient rounded to float32 is the correctly
-                # rounded float32 quotient for division (53 >= 2*24 + 2).
-                q32 = (blk.astype(np.float64) / np.float64(si)).astype(np.float32)
+                q32 = expected_cast(blk, si, amax=amax, pow2=pow2)
                 if not np.array_equal(q[m, kb * 128:(kb + 1) * 128], brute_force_encode(q32)):
                     return False
                 if amax > 0 and not pow2:
@@ -320,7 +349,7 @@ def test_weight_quant_matches_per_tile_act_quant():
             amax = np.float32(np.max(np.abs(t)))
             assert Fraction(float(s[nb, kb])) == Fraction(float(np.float32(
                 np.float64(amax) / 448.0)))
-            q32 = (t.astype(np.float64) / np.float64(s[nb, kb])).astype(np.float32)
+            q32 = expected_cast(t, s[nb, kb], amax=float(amax))
             assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128],
                                   brute_force_encode(q32.ravel()).reshape(128, 128))
 
@@ -512,6 +541,23 @@ def _quant_act_transposed_blocks(x, pow2=False):
     return q, O.scale_from_amax(np.roll(amax, 1, axis=0), pow2)
 
 
+def _quant_act_divides(x, pow2=False):
+    # mistake: the cast divides by the stored scale instead of multiplying by
+    # RN(448/amax)
+    x = np.asarray(x, np.float32)
+    s = O.scale_from_amax(O.block_amax_act(x), pow2)
+    return O.e4m3_encode((x / np.repeat(s, 128, axis=1)).astype(np.float32)), s
+
+
+def _quant_act_recip_of_scale(x, pow2=False):
+    # mistake: the factor is RN(1/s) of the rounded scale instead of RN(448/amax)
+    x = np.asarray(x, np.float32)
+    s = O.scale_from_amax(O.block_amax_act(x), pow2)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        r = (np.float32(1.0) / s).astype(np.float32)
+        return O.e4m3_encode((x * np.repeat(r, 128, axis=1)).astype(np.float32)), s
+
+
 def _quant_w_wrong_tile(w, pow2=False):
     w = np.asarray(w, np.float32)
     N, K = w.shape
@@ -543,6 +589,23 @@ def test_mutant_scales_are_caught():
 def test_mutant_gemms_are_caught(mutant):
     checks = [check_gemm_integer, check_gemm_rational, check_gemm_orientation]
     assert not all(c(mutant) for c in checks)
+
+
+@pytest.mark.parametrize("mutant", [_quant_act_divides, _quant_act_recip_of_scale])
+def test_mutant_casts_are_caught(mutant):
+    assert not check_act_quant(mutant)
+
+
+def test_the_planted_tie_separates_the_two_readings():
+    # independent of the oracle: multiplying by RN(448/amax) gives the exact
+    # tie 3.5 * 2**-9, rounded to the even code 4; dividing by RN(amax/448)
+    # does not land on it
+    s = np.float32(np.float64(TIE_AMAX) / 448.0)
+    by_mul = expected_cast(np.array([TIE_X], np.float32), s, amax=TIE_AMAX)
+    by_div = (np.float64(TIE_X) / np.float64(s)).astype(np.float32)
+    assert Fraction(float(by_mul[0])) == Fraction(7, 2 ** 10)
+    assert brute_force_encode(by_mul)[0] == 0x04
+    assert brute_force_encode(np.array([by_div], np.float32))[0] != 0x04
 
 
 def test_mutant_block_geometry_is_caught():

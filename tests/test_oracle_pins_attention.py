@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle.fp8_oracle as O
-from tests.test_oracle_pins import FINITE_CODES, _bf16_round, brute_force_encode
+from tests.test_oracle_pins import FINITE_CODES, _bf16_round, brute_force_encode, expected_cast
 
 
 def _case(seed=61, B=3, Hq=8, Hkv=2, T=40, D=128):
@@ -90,11 +90,16 @@ def test_quant_with_scale_exact():
     rng = np.random.Generator(np.random.PCG64(65))
     x = _bf16_round(rng.standard_normal((6, 256)).astype(np.float32) * 3)
     x[2, 5] = 900.0                                  # beyond the calibrated range: saturates
-    for s in (np.float32(0.0123), np.float32(2.0 ** -4)):
+    x[3, 9] = 0.000732421875                         # 3 * 2**-12: x RN(1/0.03) and x / 0.03 round apart
+    for s in (np.float32(0.0123), np.float32(2.0 ** -4), np.float32(0.03)):
         q = O.quant_with_scale(x, s)
-        q32 = (x.astype(np.float64) / np.float64(s)).astype(np.float32)
+        q32 = expected_cast(x, s)
         assert np.array_equal(q, brute_force_encode(q32.ravel()).reshape(x.shape))
     assert (O.quant_with_scale(x, np.float32(0.0123))[2, 5] & 0x7F) == 0x7E
+    # the planted element tells the multiply from the division
+    s = np.float32(0.03)
+    by_div = (np.float64(x[3, 9]) / np.float64(s)).astype(np.float32)
+    assert brute_force_encode(np.array([by_div], np.float32))[0] != O.quant_with_scale(x, s)[3, 9]
 
 
 # ---------------------------------------------------------------- mutations

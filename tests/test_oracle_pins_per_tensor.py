@@ -12,13 +12,15 @@ import numpy as np
 import pytest
 
 import oracle.fp8_oracle as O
-from tests.test_oracle_pins import CODE_0, CODE_M1, CODE_P1, FINITE_CODES, _bf16_round, brute_force_encode
+from tests.test_oracle_pins import (CODE_0, CODE_M1, CODE_P1, FINITE_CODES, TIE_AMAX, TIE_X, _bf16_round,
+                                    brute_force_encode, expected_cast)
 
 
 def _sample(seed=51, shape=(37, 300)):
     rng = np.random.Generator(np.random.PCG64(seed))
-    x = rng.standard_normal(shape).astype(np.float32)
-    x[3, 7] = 85.0                      # the tensor's amax
+    x = np.clip(rng.standard_normal(shape).astype(np.float32) * 0.2, -0.9, 0.9)
+    x[3, 7] = TIE_AMAX * 64             # the tensor's amax
+    x[3, 8] = TIE_X * 64                # an exact E4M3 tie under RN(448/amax), not under x/s
     x[5, :] = 0.0
     x[6, 11] = -2.0 ** -130             # bf16 subnormal
     return _bf16_round(x)
@@ -26,8 +28,9 @@ def _sample(seed=51, shape=(37, 300)):
 
 def check_per_tensor_exact(quant):
     """One scale from the whole tensor's amax (exact rational check of the
-    scale rule) and every code the nearest-even E4M3 rounding of the correctly
-    rounded float32 quotient."""
+    scale rule) and every code the nearest-even E4M3 rounding of
+    RN(x RN(448/amax)) (fp32 scale) or of x/s (power of two); see
+    expected_cast."""
     x = _sample()
     for pow2 in (False, True):
         q, s = quant(x, pow2=pow2)
@@ -40,7 +43,7 @@ def check_per_tensor_exact(quant):
         if not pow2 and Fraction(float(s)) != Fraction(amax) / 448 and \
                 abs(Fraction(float(s)) - Fraction(amax) / 448) > Fraction(float(s)) / 2 ** 24:
             return False
-        q32 = (x.astype(np.float64) / np.float64(s)).astype(np.float32)
+        q32 = expected_cast(x, s, amax=amax, pow2=pow2)
         if not np.array_equal(q, brute_force_encode(q32.ravel()).reshape(x.shape)):
             return False
         if not pow2 and not np.all((q[np.abs(x) == amax] & 0x7F) == 0x7E):
@@ -138,19 +141,19 @@ def _per_row_amax(x, pow2=False):
     return O.e4m3_encode((x / s).astype(np.float32)), np.float32(s)
 
 
-def _scale_by_amax(x, pow2=False):
-    # mistake: multiply by 448/amax instead of dividing by the stored scale
+def _divide_by_scale(x, pow2=False):
+    # mistake: divide by the stored scale instead of multiplying by RN(448/amax)
     x = np.asarray(x, np.float32)
     amax = np.float32(np.max(np.abs(x)))
     s = O.scale_from_amax(np.array([amax], np.float32), pow2)[0]
-    return O.e4m3_encode((x * (np.float32(448.0) / amax)).astype(np.float32)), np.float32(s)
+    return O.e4m3_encode((x / s).astype(np.float32)), np.float32(s)
 
 
 def _gemm_one_scale(qa, sa, qb, sb):
     return (O.e4m3_decode(qa) @ O.e4m3_decode(qb).T) * np.float64(sa)
 
 
-@pytest.mark.parametrize("mutant", [_per_row_amax, _scale_by_amax])
+@pytest.mark.parametrize("mutant", [_per_row_amax, _divide_by_scale])
 def test_mutant_per_tensor_quantisers_are_caught(mutant):
     assert not (check_per_tensor_exact(mutant) and check_per_tensor_single_block(mutant))
 

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle.fp8_oracle as O
-from tests.test_oracle_pins import CODE_0, CODE_M1, CODE_P1, FINITE_CODES, _bf16_round, brute_force_encode
+from tests.test_oracle_pins import (CODE_0, CODE_M1, CODE_P1, FINITE_CODES, TIE_AMAX, TIE_X, _bf16_round,
+                                    brute_force_encode, expected_cast)
 
 
 # ---------------------------------------------------------------- 128x1 activation quantiser
@@ -26,13 +27,15 @@ def _col_sample(seed=31, M=256, K=40):
     x[:128, 4] = 0.0
     x[9, 4] = -2.0 ** -130                     # a block whose amax is a bf16 subnormal
     x[:128, 5] *= 1e-30
+    x[:128, 6] = np.clip(x[:128, 6] * 0.25, -0.9, 0.9)
+    x[0, 6], x[1, 6] = TIE_AMAX, TIE_X         # separates multiply-by-RN(448/amax) from x/s
     return _bf16_round(x)
 
 
 def check_col_quant(quant_col):
     """Codes and scales of every 128x1 block against exact arithmetic: the
     scale from the block's amax, each code the nearest-even E4M3 rounding of
-    the correctly rounded float32 quotient; outputs transposed (qt[k, m])."""
+    the cast value of expected_cast; outputs transposed (qt[k, m])."""
     x = _col_sample()
     M, K = x.shape
     for pow2 in (False, True):
@@ -47,7 +50,7 @@ def check_col_quant(quant_col):
                 si = float(st[k, mb])
                 if si != float(rule(np.array([amax], np.float32))[0]):
                     return False
-                q32 = (blk.astype(np.float64) / np.float64(si)).astype(np.float32)
+                q32 = expected_cast(blk, si, amax=amax, pow2=pow2)
                 if not np.array_equal(qt[k, mb * 128:(mb + 1) * 128], brute_force_encode(q32)):
                     return False
     return True
@@ -315,7 +318,15 @@ def _wgrad_drops_last_block(qt_dy, st_dy, qt_x, st_x):
     return O.wgrad_ref(qt_dy, st_dy, qt_x, st_x)
 
 
-@pytest.mark.parametrize("mutant", [_col_quant_whole_slab, _col_quant_untransposed_scales])
+def _col_quant_divides(x, pow2=False):
+    # mistake: the cast divides by the stored scale
+    x = np.asarray(x, np.float32)
+    s = O.scale_from_amax(O.block_amax_col(x), pow2)
+    q = O.e4m3_encode((x / np.repeat(s, 128, axis=0)).astype(np.float32))
+    return np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
+@pytest.mark.parametrize("mutant", [_col_quant_whole_slab, _col_quant_untransposed_scales, _col_quant_divides])
 def test_mutant_col_quantisers_are_caught(mutant):
     assert not (check_col_quant(mutant) and check_col_geometry(mutant))
 
