@@ -25,7 +25,7 @@ SOURCES = ["api.cu", "quant.cu", "quant_t.cu", "quant_pt.cu", "attn.cu", "gemm_p
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-std=c++17", "-lineinfo",
-    # exact IEEE behaviour: subnormal amax/scales and the cast's division must
+    # exact IEEE behaviour: subnormal amax/scales and the scale's division must
     # round exactly as specified
     "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=true",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

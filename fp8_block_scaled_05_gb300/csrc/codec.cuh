@@ -1,12 +1,14 @@
 // Device-side pieces of the block quantisers: bf16 unpacking, block amax,
-// the two scale rules, the per-element division and the E4M3 conversion.
+// the two scale rules, the per-element cast and the E4M3 conversion.
 //
 // Method (page "NVIDIA NeMo RL достигает ускорения на 48% благодаря
 // сквозному обучению с точностью FP8", greentreeone.com, §Технический
 // прорыв; power-of-two option: upppp.jp NeMo RL FP8 article, §設定方法):
 //   s = RN_fp32(amax / 448)   or   s = 2^ceil(log2(amax / 448)) (clamped to
 //   [2^-127, 2^127]); s = 1 for an all-zero block;
-//   q = e4m3_RNE_satfinite( RN_fp32(x / s) ).
+//   q = e4m3_RNE_satfinite( RN_fp32(x * r) ),  r = RN_fp32(448 / amax)
+//   (r = 2^-e for the power-of-two scale; the division x / s where r
+//   overflows fp32).
 #pragma once
 #include <cstdint>
 
@@ -59,12 +61,22 @@ __device__ __forceinline__ float exp2_int(int e) {
     return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// Per-block constants for the cast x -> x / s.
+// Per-block constants of the cast.  The pages give the scale as amax/448 and
+// leave open whether the cast divides by it or multiplies by its
+// reciprocal; the cast here multiplies by the reciprocal factor r (the usual
+// form of an FP8 cast): code = e4m3(RN(x r)) with r = RN(448/amax) for an
+// fp32 scale, r = 2^-e (exact, so x r = x/s) for a power-of-two scale, and
+// r = RN(1/s) for a cast with a given scale.  Where r overflows fp32 (amax
+// below 448 * 2^-128, or s below 2^-128) the cast divides by s instead.
 struct BlockScale {
     float s;         // the stored scale
-    float r;         // RN(1 / s) (fp32 mode) or 2^-e exactly (pow2 mode)
-    int mode;        // 0: two-step corrected quotient, 1: exact product, 2: IEEE division
+    float r;         // the cast's factor (see above)
+    int mode;        // 1: product x * r, 2: IEEE division x / s (r not finite)
 };
+
+__device__ __forceinline__ int cast_mode(float r) {
+    return (__float_as_uint(r) & 0x7FFFFFFFu) < 0x7F800000u ? 1 : 2;
+}
 
 __device__ __forceinline__ BlockScale make_scale(float amax, bool pow2) {
     BlockScale bs;
@@ -82,22 +94,19 @@ __device__ __forceinline__ BlockScale make_scale(float amax, bool pow2) {
         return bs;
     }
     bs.s = __fdiv_rn(amax, 448.0f);
-    bs.r = __frcp_rn(bs.s);
-    // The two-step correction needs every remainder x - s*q to be exact; that
-    // holds for s >= 2^-90 (see quotient_rn).  Smaller scales (amax below
-    // about 2^-81) take the IEEE division.
-    bs.mode = (__float_as_uint(bs.s) >= (uint32_t)(127 - 90) << 23) ? 0 : 2;
+    bs.r = __fdiv_rn(448.0f, amax);
+    bs.mode = cast_mode(bs.r);
     return bs;
 }
 
-// The per-block constants from a stored scale s and its reciprocal factor r
-// (as make_scale produced them); lets one lane compute a block's scale and
-// others rebuild it from two shuffled values.
+// The per-block constants from a stored scale s and the cast's factor r (as
+// make_scale produced them); lets one lane compute a block's scale and others
+// rebuild it from two shuffled values.
 __device__ __forceinline__ BlockScale scale_from_sr(float s, float r, bool pow2) {
     BlockScale bs;
     bs.s = s;
     bs.r = r;
-    bs.mode = pow2 ? 1 : ((__float_as_uint(s) >= (uint32_t)(127 - 90) << 23) ? 0 : 2);
+    bs.mode = pow2 ? 1 : cast_mode(r);
     return bs;
 }
 
@@ -105,30 +114,6 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
-}
-
-// RN_fp32(x / s).
-//
-// mode 0 uses a hoisted correctly rounded reciprocal r = RN(1/s) and two
-// residual corrections (Markstein's theorem, as stated in Muller et al.,
-// "Handbook of Floating-Point Arithmetic", division via FMA):
-//   q0 = RN(x r)                   -- within 1.5 ulp of x/s
-//   q1 = RN(q0 + RN(x - s q0) r)   -- faithful (within 1 ulp)
-//   q2 = RN(q1 + (x - s q1) r)     -- x - s q1 is exact for a faithful q1,
-//                                     and the theorem gives q2 = RN(x/s)
-// valid while no remainder underflows: |x/s| >= 2^-11 matters for the E4M3
-// code and s >= 2^-90 keeps x - s q a multiple of 2^-149; quotients below
-// 2^-11 round to a signed zero code either way.  The corrections can turn a
-// zero quotient's sign positive ((+0) + (-0) = +0 under round-to-nearest), so
-// the sign of x is put back: RN(x/s) always carries the sign of x.
-__device__ __forceinline__ float quotient_rn(float x, const BlockScale &bs) {
-    if (bs.mode == 1) return x * bs.r;
-    if (bs.mode == 2) return __fdiv_rn(x, bs.s);
-    float q = x * bs.r;
-    float rem = fmaf(-bs.s, q, x);
-    q = fmaf(rem, bs.r, q);
-    rem = fmaf(-bs.s, q, x);
-    return copysignf(fmaf(rem, bs.r, q), x);
 }
 
 // Two fp32 values to two E4M3 codes (round to nearest even, saturating to
@@ -149,29 +134,15 @@ __device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float
     asm("mov.b64 {%0, %1}, %2;" : "=f"(pa), "=f"(pb) : "l"(x));
 }
 
-// Codes of two elements, e4m3(RN(x/s)) each.
-//
-// Fast path for mode 0: q0 = RN(x r) is within 1.5 ulp of x/s, so the
-// correctly rounded quotient t = RN(x/s) is within 2 ulp of q0 and lies
-// strictly between q0 (1 - 2^-21) and q0 (1 + 2^-21) (both products, rounded,
-// stay at least 3.5 ulp away from q0).  E4M3 conversion is monotone, so when
-// those two ends convert to the same code, t converts to it as well.  Only
-// pairs whose interval contains an E4M3 rounding boundary (a few in a
-// million) take the two-step corrected quotient.  The three products of the
-// pair (q0 and the two ends) are packed multiplies, one per product pair.
+// Codes of two elements: one packed multiply and one conversion per pair
+// (mode 2, a block whose reciprocal factor overflows, divides).
 __device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
-    float qa, qb;
-    mul2(xa, xb, bs.r, qa, qb);
-    if (bs.mode == 1) return e4m3x2(qa, qb);
-    if (bs.mode == 0) {
-        constexpr float kLo = 1.0f - 0x1p-21f, kHi = 1.0f + 0x1p-21f;
-        float la, lb, ha, hb;
-        mul2(qa, qb, kLo, la, lb);
-        mul2(qa, qb, kHi, ha, hb);
-        const uint32_t lo = e4m3x2(la, lb), hi = e4m3x2(ha, hb);
-        if (lo == hi) return lo;
+    if (bs.mode == 1) {
+        float qa, qb;
+        mul2(xa, xb, bs.r, qa, qb);
+        return e4m3x2(qa, qb);
     }
-    return e4m3x2(quotient_rn(xa, bs), quotient_rn(xb, bs));
+    return e4m3x2(__fdiv_rn(xa, bs.s), __fdiv_rn(xb, bs.s));
 }
 
 // Quantises eight bf16 values (one 16-byte load) to eight codes (8 bytes).
@@ -183,9 +154,9 @@ __device__ __forceinline__ uint2 quant8(const uint4 &v, const BlockScale &bs) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// quant8 for a power-of-two scale (r = 2^-e exactly): x * r is x / s with no
-// rounding, so no check is needed; both elements of a pair in one packed
-// multiply.
+// quant8 for a block in mode 1 (every power-of-two scale, and every fp32
+// scale whose factor r is finite): both elements of a pair in one packed
+// multiply, then one conversion.
 __device__ __forceinline__ uint2 quant8_pow2(const uint4 &v, float r) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t p[4];

@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_quant_tensor(const uint16_t* 
 }
 
 // Cast under a given scale (scale[0], a positive normal fp32 in device
-// memory: a calibrated KV-cache or query scale): q = e4m3(RN(x / s)), values
-// beyond +-448 s saturating.
+// memory: a calibrated KV-cache or query scale): q = e4m3(RN(x * RN(1/s))),
+// values beyond +-448 s saturating.
 __global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __restrict__ x, ChunkWalk w,
                                                              uint8_t* __restrict__ q, int64_t ldq,
                                                              const float* __restrict__ scale) {

@@ -42,6 +42,8 @@ _i64, _u32, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int32, ct
 SIGNATURES = {
     "fp8_quant_act_1x128": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, ctypes.c_int, _vp]),
     "fp8_quant_weight_128x128": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, ctypes.c_int, _vp]),
+    "fp8_quant_act_weight": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _i64,
+                                            _vp, ctypes.c_int, _vp]),
     "fp8_blockscaled_gemm": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64,
                                             _u32, _vp, _sz, _vp]),
     "fp8_blockscaled_grouped_gemm": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64,
@@ -162,6 +164,24 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor,
     N, K = w.shape
     _check(lib().fp8_quant_weight_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(s), int(mode),
                                           _stream(stream)), "fp8_quant_weight_128x128")
+
+
+def fp8_quant_act_weight(x: torch.Tensor, qa: torch.Tensor, sa: torch.Tensor, w: torch.Tensor, qw: torch.Tensor,
+                         sw: torch.Tensor, mode: int = FP8_SCALE_FP32_AMAX, stream=None) -> None:
+    """fp8_quant_act_1x128(x, qa, sa) and fp8_quant_weight_128x128(w, qw, sw)
+    in one launch; x bf16 [M, K], w bf16 [N, K]."""
+    for t, dt, n in ((x, torch.bfloat16, "x"), (qa, torch.uint8, "qa"), (sa, torch.float32, "sa"),
+                     (w, torch.bfloat16, "w"), (qw, torch.uint8, "qw"), (sw, torch.float32, "sw")):
+        _need(t, dt, n)
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("x and w must share K")
+    _check(lib().fp8_quant_act_weight(_ptr(x), M, K, x.stride(0), _ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0),
+                                      _ptr(w), N, w.stride(0), _ptr(qw), qw.stride(0), _ptr(sw), int(mode),
+                                      _stream(stream)), "fp8_quant_act_weight")
 
 
 def fp8_quant_act_128x1(x: torch.Tensor, qt: torch.Tensor, st: torch.Tensor, q: torch.Tensor | None = None,
@@ -287,7 +307,7 @@ def fp8_quant_per_tensor(x: torch.Tensor, q: torch.Tensor, scale_amax: torch.Ten
 
 
 def fp8_quant_with_scale(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None) -> None:
-    """q = e4m3(x / scale[0]); x bf16 [M, K] (or any 2-D view), q uint8 of the same shape."""
+    """q = e4m3(RN(x * RN(1 / scale[0]))); x bf16 [M, K] (or any 2-D view), q uint8 of the same shape."""
     _need(x, torch.bfloat16, "x")
     _need(q, torch.uint8, "q")
     _need(scale, torch.float32, "scale")
@@ -636,8 +656,13 @@ def moe_wgrad(dy: torch.Tensor, x: torch.Tensor, offsets, pow2: bool = False, st
 
 
 def linear(x: torch.Tensor, w: torch.Tensor, pow2: bool = False, stream=None):
-    """bf16 y = FP8 linear layer: quantise x (1x128) and w (128x128), then the
-    block-scaled GEMM.  Returns (y, (qa, sa), (qw, sw))."""
-    qa, sa = quant_act(x, pow2, stream)
-    qw, sw = quant_weight(w, pow2, stream)
+    """bf16 y = FP8 linear layer: quantise x (1x128) and w (128x128) in one
+    launch, then the block-scaled GEMM.  Returns (y, (qa, sa), (qw, sw))."""
+    M, K = x.shape
+    N = w.shape[0]
+    qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty((K // 128, max(round_up(M, 4), 4)), dtype=torch.float32, device=x.device)
+    qw = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8_quant_act_weight(x, qa, sa, w, qw, sw, FP8_SCALE_POW2 if pow2 else FP8_SCALE_FP32_AMAX, stream)
     return gemm(qa, sa, qw, sw, pow2, stream=stream), (qa, sa), (qw, sw)

@@ -64,11 +64,21 @@ typedef enum {
     FP8_ERR_NOT_IMPLEMENTED = 9  /* the requested path is not built */
 } fp8_status;
 
+/*
+ * Scale rules.  Each block has a stored scale s (dequantisation: x ~ dec(q) s)
+ * and a cast factor r: the codes are q = e4m3(RN_fp32(x r)), rounded to
+ * nearest even and saturated at +-448.  The pages give the scale as amax/448
+ * and leave open whether the cast divides by it or multiplies by the
+ * reciprocal; the library multiplies (the usual FP8 cast), with r =
+ * RN_fp32(448 / amax).  Where that reciprocal overflows fp32 (amax below
+ * 448 * 2^-128) the cast divides, q = e4m3(RN_fp32(x / s)).
+ */
 typedef enum {
-    /* s = RN_fp32(amax / 448); an all-zero block gets s = 1. */
+    /* s = RN_fp32(amax / 448), r = RN_fp32(448 / amax); an all-zero block
+     * gets s = r = 1. */
     FP8_SCALE_FP32_AMAX = 0,
-    /* s = 2^e, e = ceil(log2(amax / 448)) clamped to [-127, 127]; an
-     * all-zero block gets s = 1.  The cast is then an exact multiply. */
+    /* s = 2^e, e = ceil(log2(amax / 448)) clamped to [-127, 127], r = 2^-e
+     * (so x r is the exact quotient x / s); an all-zero block gets s = 1. */
     FP8_SCALE_POW2 = 1
 } fp8_scale_mode;
 
@@ -91,7 +101,7 @@ typedef enum {
  *   for every row m < M and K-block kb < K/128:
  *     amax      = max_{k in kb} |x[m, k]|
  *     s[kb, m]  = scale(amax)           (see fp8_scale_mode)
- *     q[m, k]   = e4m3( RN_fp32(x[m, k] / s[kb, m]) )
+ *     q[m, k]   = e4m3( RN_fp32(x[m, k] * r(amax)) )   (see fp8_scale_mode)
  *
  * x   device, bf16 [M, K] row-major, row pitch ldx (>= K, ldx % 8 == 0, x 16-byte aligned)
  * q   device, uint8 E4M3 codes [M, K] row-major, row pitch ldq (>= K, ldq % 16 == 0, 16-byte aligned)
@@ -132,7 +142,7 @@ FP8BS_API fp8_status fp8_quant_weight_128x128_e8(const void *w, int64_t N, int64
  *   for every tile (nb, kb), nb < N/128, kb < K/128:
  *     amax        = max over the 128x128 tile of |w|
  *     s[nb, kb]   = scale(amax)
- *     q[n, k]     = e4m3( RN_fp32(w[n, k] / s[n/128, k/128]) )
+ *     q[n, k]     = e4m3( RN_fp32(w[n, k] * r(amax of the tile)) )
  *
  * w   device, bf16 [N, K] row-major, row pitch ldw (>= K, ldw % 8 == 0, 16-byte aligned)
  * q   device, uint8 [N, K] row-major, row pitch ldq (>= K, ldq % 16 == 0, 16-byte aligned)
@@ -143,6 +153,21 @@ FP8BS_API fp8_status fp8_quant_weight_128x128_e8(const void *w, int64_t N, int64
 FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
                                     uint8_t *q, int64_t ldq, float *s,
                                     fp8_scale_mode mode, fp8_stream_t stream);
+
+/*
+ * A layer's two quantisations in one launch: exactly fp8_quant_act_1x128(x,
+ * M, K, ...) and fp8_quant_weight_128x128(w, N, K, ...) (same codes, same
+ * scales, same layouts and argument rules), the activations and weights of a
+ * linear layer y = x W^T sharing K.  One grid covers both, so the two HBM
+ * streams share one ramp-up and one tail instead of paying each (the weights
+ * are re-quantised every step, greentreeone.com NeMo RL FP8 page,
+ * §Реальные прирост производительности).  M may be 0 (weights only).
+ */
+FP8BS_API fp8_status fp8_quant_act_weight(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t *qa, int64_t ldqa, float *sa, int64_t ldsa,
+                                          const void *w, int64_t N, int64_t ldw, uint8_t *qw,
+                                          int64_t ldqw, float *sw, fp8_scale_mode mode,
+                                          fp8_stream_t stream);
 
 /*
  * Training-side operands.  The pages run FP8 through training as well as
@@ -166,7 +191,7 @@ FP8BS_API fp8_status fp8_quant_weight_128x128(const void *w, int64_t N, int64_t 
  *   for every column k < K and token block mb < M/128:
  *     amax          = max_{m in mb} |x[m, k]|
  *     st[mb, k]     = scale(amax)
- *     qt[k, m]      = e4m3( RN_fp32(x[m, k] / st[m/128, k]) )
+ *     qt[k, m]      = e4m3( RN_fp32(x[m, k] * r(amax of the block)) )
  *
  * i.e. exactly what fp8_quant_act_1x128 writes for x^T.  Optionally (q and s
  * both non-NULL) the same pass also writes the 1x128 codes and scales of x
@@ -306,7 +331,7 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t *qa, int64
  *   amax           = max over the whole tensor of |x[m, k]|
  *   s              = scale(amax)        (see fp8_scale_mode; the block rule
  *                                        applied to one block, the tensor)
- *   q[m, k]        = e4m3( RN_fp32(x[m, k] / s) )
+ *   q[m, k]        = e4m3( RN_fp32(x[m, k] * r(amax)) )
  *
  * Two kernels on `stream` (an amax reduction, then the cast); the call also
  * clears the amax word first.
@@ -331,7 +356,8 @@ FP8BS_API fp8_status fp8_quant_per_tensor(const void *x, int64_t M, int64_t K, i
  */
 
 /*
- * Cast under a given scale:  q[m, k] = e4m3( RN_fp32(x[m, k] / s) ),  s = scale[0].
+ * Cast under a given scale:  q[m, k] = e4m3( RN_fp32(x[m, k] * RN_fp32(1 / s)) ),
+ * s = scale[0] (the division x / s if 1 / s overflows fp32).
  * Values beyond +-448 s saturate to the largest code (a calibrated scale can
  * be exceeded by later activations).
  * x      device, bf16 [M, K] row-major, row pitch ldx (>= K, % 8 == 0)
@@ -346,7 +372,7 @@ FP8BS_API fp8_status fp8_quant_with_scale(const void *x, int64_t M, int64_t K, i
 
 /*
  * Cache append of one decode step: for every sequence b and KV head g,
- *   k_cache[b, g, seq_lens[b], :] = e4m3( RN_fp32(k_new[b, g, :] / sk[0]) )
+ *   k_cache[b, g, seq_lens[b], :] = e4m3( RN_fp32(k_new[b, g, :] * RN_fp32(1 / sk[0])) )
  * and likewise v with sv[0] (values beyond +-448 s saturate).  Rows whose
  * slot seq_lens[b] is outside [0, T) are skipped; seq_lens is not changed
  * (the caller advances it after the step's attention).
