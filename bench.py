@@ -287,27 +287,25 @@ def run_ours(args, world, rank, local):
     flops_step = sum(2.0 * L["M"] * L["N"] * L["K"] for L in layers)
     from fp8_block_scaled_05_gb300.timing import L2Flush
     flush = L2Flush(dev, L2_FLUSH_BYTES)
-    launches_per_step = 3 * len(layers)
+    launches_per_step = 2 * len(layers)
 
     def step(events=None, pow2=False):
+        # per layer: the activation and weight quantisers in one launch, then the GEMM
         mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
         flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
         for i, L in enumerate(layers):
             if events is not None:
-                events[3 * i].record(stream)
-            ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], mode, stream)
+                events[2 * i].record(stream)
+            ops.fp8_quant_act_weight(L["a"], L["qa"], L["sa"], L["w"], L["qw"], L["sw"], mode, stream)
             if events is not None:
-                events[3 * i + 1].record(stream)
-            ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream)
-            if events is not None:
-                events[3 * i + 2].record(stream)
+                events[2 * i + 1].record(stream)
             ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags, L["ws"], stream)
         if events is not None:
-            events[3 * len(layers)].record(stream)
+            events[2 * len(layers)].record(stream)
 
     def timed(pow2, steps):
         """Runs `steps` flushed steps; returns (per-step ms, per-kernel mean ms)."""
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * len(layers) + 1)] for _ in range(steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers) + 1)] for _ in range(steps)]
         with torch.cuda.stream(stream):
             for k in range(steps):
                 flush()
@@ -316,8 +314,8 @@ def run_ours(args, world, rank, local):
         step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps)]
         kern = {}
         for i, L in enumerate(layers):
-            for j, kname in enumerate(("quant_act", "quant_weight", "gemm")):
-                ms = [evs[k][3 * i + j].elapsed_time(evs[k][3 * i + j + 1]) for k in range(steps)]
+            for j, kname in enumerate(("quant", "gemm")):
+                ms = [evs[k][2 * i + j].elapsed_time(evs[k][2 * i + j + 1]) for k in range(steps)]
                 kern[f"{L['name']}.{kname}"] = sum(ms) / len(ms)
         return step_ms, kern
 
@@ -350,20 +348,34 @@ def run_ours(args, world, rank, local):
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     traffic = traffic_for(f"gemm.{dom}")
     kernels_out = {}
+    qbytes = {}
     for L in layers:
         n = L["name"]
         qa_bytes = 2 * L["M"] * L["K"] + L["M"] * L["K"] + 4 * L["M"] * L["K"] // 128
         qw_bytes = 2 * L["N"] * L["K"] + L["N"] * L["K"] + 4 * (L["N"] // 128) * (L["K"] // 128)
-        kernels_out[f"{n}.quant_act"] = {"ms": kern[f"{n}.quant_act"],
-                                         "GB/s": qa_bytes / kern[f"{n}.quant_act"] / 1e6,
-                                         "frac_hbm": qa_bytes / kern[f"{n}.quant_act"] / 1e6 / peaks["hbm_gbs"]}
-        kernels_out[f"{n}.quant_weight"] = {"ms": kern[f"{n}.quant_weight"],
-                                            "GB/s": qw_bytes / kern[f"{n}.quant_weight"] / 1e6,
-                                            "frac_hbm": qw_bytes / kern[f"{n}.quant_weight"] / 1e6 / peaks["hbm_gbs"]}
+        qbytes[n] = (qa_bytes, qw_bytes)
+        q_ms = kern[f"{n}.quant"]
+        kernels_out[f"{n}.quant"] = {"what": "1x128 activations and 128x128 weights in one launch",
+                                     "ms": q_ms, "GB/s": (qa_bytes + qw_bytes) / q_ms / 1e6,
+                                     "frac_hbm": (qa_bytes + qw_bytes) / q_ms / 1e6 / peaks["hbm_gbs"]}
         gf = 2.0 * L["M"] * L["N"] * L["K"]
         kernels_out[f"{n}.gemm"] = {"ms": kern[f"{n}.gemm"], "TFLOP/s": gf / kern[f"{n}.gemm"] / 1e9,
                                     "frac_fp8": gf / kern[f"{n}.gemm"] / 1e9 / fp8_peak}
     gemm_ms = sum(kern[f"{L['name']}.gemm"] for L in layers)
+
+    # each quantiser alone (one launch each), for the per-kernel rooflines
+    qcalls = []
+    for L in layers:
+        qcalls += [lambda L=L: ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream),
+                   lambda L=L: ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)]
+    qper, _ = time_calls(args, stream, dev, flush, qcalls)
+    quantisers = {"what": "the two quantisers of each layer launched on their own (fp32 scales), flushed L2"}
+    for i, L in enumerate(layers):
+        n = L["name"]
+        for j, (kn, nbytes) in enumerate(zip(("quant_act", "quant_weight"), qbytes[n])):
+            ms = qper[2 * i + j]
+            quantisers[f"{n}.{kn}"] = {"ms": ms, "GB/s": nbytes / ms / 1e6,
+                                       "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
 
     # ---------------- end to end: pinned host buffers, copies inside the timed region
     e2e = None
@@ -395,8 +407,7 @@ def run_ours(args, world, rank, local):
                 stream.wait_event(e_in)
                 if prev_out[i] is not None:
                     stream.wait_event(prev_out[i])
-                ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], 0, stream)
-                ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], 0, stream)
+                ops.fp8_quant_act_weight(L["a"], L["qa"], L["sa"], L["w"], L["qw"], L["sw"], 0, stream)
                 ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], 0, L["ws"], stream)
                 e_k = ev()
                 e_k.record(stream)
@@ -565,6 +576,7 @@ def run_ours(args, world, rank, local):
                          "hbm_peak_gbs": peaks["hbm_gbs"]},
             "gemm_only_tflops": sum(g[1] for g in gemms.values()) / (gemm_ms / 1e3) / 1e12,
             "kernels": kernels_out,
+            "quantisers": quantisers,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "pow2": pow2,
@@ -700,25 +712,25 @@ def qwen_measure(args, ops, stream, dev, flush, fp8_peak):
         flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
         calls = []
         for L in layers:
-            calls += [lambda L=L: ops.fp8_quant_act_1x128(L["a"], L["qa"], L["sa"], mode, stream),
-                      lambda L=L: ops.fp8_quant_weight_128x128(L["w"], L["qw"], L["sw"], mode, stream),
+            calls += [lambda L=L: ops.fp8_quant_act_weight(L["a"], L["qa"], L["sa"], L["w"], L["qw"], L["sw"], mode,
+                                                           stream),
                       lambda L=L: ops.fp8_blockscaled_gemm(L["qa"], L["sa"], L["qw"], L["sw"], L["c"], flags,
                                                            L["ws"], stream)]
         per, total = time_calls(args, stream, dev, flush, calls)
         rows, gemm_ms = {}, 0.0
         for i, L in enumerate(layers):
-            qa_ms, qw_ms, g_ms = per[3 * i:3 * i + 3]
+            q_ms, g_ms = per[2 * i:2 * i + 2]
             gf = 2.0 * L["M"] * L["N"] * L["K"]
             gemm_ms += g_ms
-            rows[L["name"]] = {"quant_act_ms": qa_ms, "quant_weight_ms": qw_ms, "gemm_ms": g_ms,
-                               "quant_gemm_tflops": gf / ((qa_ms + qw_ms + g_ms) / 1e3) / 1e12,
+            rows[L["name"]] = {"quant_ms": q_ms, "gemm_ms": g_ms,
+                               "quant_gemm_tflops": gf / ((q_ms + g_ms) / 1e3) / 1e12,
                                "gemm_tflops": gf / (g_ms / 1e3) / 1e12,
                                "gemm_frac_fp8": gf / (g_ms / 1e3) / 1e12 / fp8_peak}
         out["modes"]["pow2" if pow2 else "fp32"] = {
             "gemm_kernel": "mx" if pow2 else "promote", "ms_per_step": total,
             "quant_gemm_tflops": flops / (total / 1e3) / 1e12, "gemm_only_tflops": flops / (gemm_ms / 1e3) / 1e12,
             "gemm_frac_fp8": flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, "layers": rows,
-            "gpu_launches": 3 * len(layers) * args.steps}
+            "gpu_launches": 2 * len(layers) * args.steps}
     return out
 
 
@@ -778,9 +790,10 @@ def moe_measure(args, ops, stream, dev, flush, fp8_peak, hbm_peak):
     experts with Zipf(1.1) popularity (seeded Gumbel-top-8), rows sorted by
     expert (65536 rows); expert gate+up (K 2048, N 1536) and down (K 768,
     N 2048).  Per projection: the 1x128 quantiser of the expert-sorted
-    activations, the 128x128 quantiser of all experts' weights (one launch on
-    the [G N, K] view; no tile straddles two experts since N % 128 == 0) and
-    the grouped GEMM with device-side offsets, in both scale modes.  FLOPs
+    activations and the 128x128 quantiser of all experts' weights in one
+    launch (the weights as the [G N, K] view; no tile straddles two experts
+    since N % 128 == 0), then the grouped GEMM with device-side offsets, in
+    both scale modes.  FLOPs
     are 2 sum(M_e) N K; the weight stream is G N K code bytes."""
     import numpy as np
     import torch
@@ -810,28 +823,27 @@ def moe_measure(args, ops, stream, dev, flush, fp8_peak, hbm_peak):
         flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
         calls = []
         for P in projs:
-            calls += [lambda P=P: ops.fp8_quant_act_1x128(P["a"], P["qa"], P["sa"], mode, stream),
-                      lambda P=P: ops.fp8_quant_weight_128x128(P["w"], P["qw"].view(-1, P["K"]),
-                                                               P["sw"].view(-1, P["K"] // 128), mode, stream),
+            calls += [lambda P=P: ops.fp8_quant_act_weight(P["a"], P["qa"], P["sa"], P["w"], P["qw"].view(-1, P["K"]),
+                                                           P["sw"].view(-1, P["K"] // 128), mode, stream),
                       lambda P=P: ops.fp8_blockscaled_grouped_gemm(P["qa"], P["sa"], offs, P["qw"], P["sw"], P["c"],
                                                                    flags, None, stream)]
         per, total = time_calls(args, stream, dev, flush, calls)
         rows = {}
         for i, P in enumerate(projs):
-            qa_ms, qw_ms, g_ms = per[3 * i:3 * i + 3]
+            q_ms, g_ms = per[2 * i:2 * i + 2]
             gf = 2.0 * P["M"] * P["N"] * P["K"]
             wbytes = G * P["N"] * P["K"]
-            rows[P["name"]] = {"quant_act_ms": qa_ms, "quant_weight_ms": qw_ms, "gemm_ms": g_ms,
+            rows[P["name"]] = {"quant_ms": q_ms, "gemm_ms": g_ms,
                                "gemm_tflops": gf / (g_ms / 1e3) / 1e12,
                                "gemm_frac_fp8": gf / (g_ms / 1e3) / 1e12 / fp8_peak,
                                "weight_stream_GB/s": wbytes / (g_ms / 1e3) / 1e9,
                                "weight_stream_frac_hbm": wbytes / (g_ms / 1e3) / 1e9 / hbm_peak,
-                               "quant_gemm_tflops": gf / ((qa_ms + qw_ms + g_ms) / 1e3) / 1e12}
+                               "quant_gemm_tflops": gf / ((q_ms + g_ms) / 1e3) / 1e12}
         flops = sum(2.0 * P["M"] * P["N"] * P["K"] for P in projs)
         out["modes"]["pow2" if pow2 else "fp32"] = {
             "gemm_kernel": "mx (grouped)" if pow2 else "promote (grouped)", "ms_per_step": total,
             "quant_gemm_tflops": flops / (total / 1e3) / 1e12, "projections": rows,
-            "gpu_launches": 3 * len(projs) * args.steps}
+            "gpu_launches": 2 * len(projs) * args.steps}
     out["wgrad"] = moe_wgrad_measure(args, ops, stream, dev, flush, fp8_peak, m, projs, offs)
     return out
 

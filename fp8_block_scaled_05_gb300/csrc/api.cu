@@ -237,6 +237,28 @@ fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fp8_status fp8_quant_act_weight(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qa, int64_t ldqa,
+                                float* sa, int64_t ldsa, const void* w, int64_t N, int64_t ldw, uint8_t* qw,
+                                int64_t ldqw, float* sw, fp8_scale_mode mode, fp8_stream_t stream) {
+    if (fp8_status e = check_mode(mode)) return e;
+    if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 31) - 1 || K > (1ll << 26)) return FP8_ERR_SHAPE;
+    if (N <= 0 || (N % 128) || N / 128 > 65535) return FP8_ERR_SHAPE;
+    const int64_t blocks = (N / 128) * (K / 128) + ((M + 15) / 16) * ((K / 128 + 7) / 8);
+    if (blocks > INT32_MAX) return FP8_ERR_SHAPE;
+    if (!w || !qw || !sw) return FP8_ERR_NULL;
+    if (M > 0 && (!x || !qa || !sa)) return FP8_ERR_NULL;
+    if (ldw < K || ldqw < K) return FP8_ERR_SHAPE;
+    if (M > 0 && (ldx < K || ldqa < K || ldsa < M)) return FP8_ERR_SHAPE;
+    if ((ldw % 8) || (ldqw % 16) || !aligned16(w) || !aligned16(qw) || (reinterpret_cast<uintptr_t>(sw) % 4))
+        return FP8_ERR_ALIGN;
+    if (M > 0 && ((ldx % 8) || (ldqa % 16) || (ldsa % 4) || !aligned16(x) || !aligned16(qa) || !aligned16(sa)))
+        return FP8_ERR_ALIGN;
+    DeviceInfo* d;
+    if (fp8_status e = current_device(&d)) return e;
+    return cuda_status(launch_quant_act_weight(x, M, K, ldx, qa, ldqa, sa, ldsa, w, N, ldw, qw, ldqw, sw,
+                                               mode == FP8_SCALE_POW2, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fp8_status fp8_quant_act_1x128_e8(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                   uint8_t* s, int64_t lds, fp8_stream_t stream) {
     if (M < 0 || K <= 0 || (K % 128) || M > (1ll << 31) - 1 || K > (1ll << 26)) return FP8_ERR_SHAPE;

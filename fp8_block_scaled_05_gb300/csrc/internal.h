@@ -69,6 +69,9 @@ struct DeviceInfo {
 // s8 != nullptr: power-of-two scales written as UE8M0 bytes there (s unused).
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                    float* s, int64_t lds, bool pow2, cudaStream_t st, uint8_t* s8 = nullptr);
+cudaError_t launch_quant_act_weight(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qa, int64_t ldqa,
+                                    float* sa, int64_t ldsa, const void* w, int64_t N, int64_t ldw, uint8_t* qw,
+                                    int64_t ldqw, float* sw, bool pow2, cudaStream_t st);
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                         int64_t ldq, float* s, bool pow2, cudaStream_t st, uint8_t* s8 = nullptr);
 

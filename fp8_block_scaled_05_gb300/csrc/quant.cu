@@ -38,18 +38,16 @@ constexpr int kActPairs = kActKB / 2;
 constexpr int kActItems = kActRowsPerWarp * kActPairs;   // blocks per half-warp
 static_assert(kActItems <= 16 && (kActItems & (kActItems - 1)) == 0, "items per half-warp");
 
-// POW2: power-of-two scales, cast by an exact multiply (no division, no check).
+// POW2: power-of-two scales (the exponent instead of the two divisions).
+// One CTA tile (bx, by) of 16 rows x 8 K-blocks; 256 threads.
 template <bool POW2>
-__global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
-                                                            int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
-                                                            float* __restrict__ s, int64_t lds,
-                                                            uint8_t* __restrict__ s8) {
+__device__ __forceinline__ void act_tile_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx,
+                                               uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
+                                               int64_t lds, uint8_t* __restrict__ s8, int64_t bx, int64_t by) {
     __shared__ float s_tile[kActKB][kActRows];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
-    const int64_t m0 = (int64_t)blockIdx.x * kActRows;
-    const int64_t kb0 = (int64_t)blockIdx.y * kActKB;
-    griddep_wait();                  // x may come from the previous kernel in the stream
-    griddep_launch_dependents();     // the GEMM that follows may start its prologue
+    const int64_t m0 = bx * kActRows;
+    const int64_t kb0 = by * kActKB;
 
     uint4 v[kActItems];
 #pragma unroll
@@ -118,6 +116,16 @@ __global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __re
     }
 }
 
+template <bool POW2>
+__global__ void __launch_bounds__(256, 4) k_quant_act_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t KB,
+                                                            int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
+                                                            float* __restrict__ s, int64_t lds,
+                                                            uint8_t* __restrict__ s8) {
+    griddep_wait();                  // x may come from the previous kernel in the stream
+    griddep_launch_dependents();     // the GEMM that follows may start its prologue
+    act_tile_1x128<POW2>(x, M, KB, ldx, q, ldq, s, lds, s8, blockIdx.x, blockIdx.y);
+}
+
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                                    float* s, int64_t lds, bool pow2, cudaStream_t st, uint8_t* s8) {
     if (M == 0) return cudaSuccess;
@@ -136,12 +144,11 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 // 16w..16w+15, one warp-wide load covering two rows (half-warp each).  Each
 // lane keeps its 64 values in registers across the CTA-wide amax reduction.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
-                                                         uint8_t* __restrict__ q, int64_t ldq,
-                                                         float* __restrict__ s, int pow2, uint8_t* __restrict__ s8) {
+__device__ __forceinline__ void weight_tile_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
+                                                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
+                                                    bool pow2, uint8_t* __restrict__ s8, int64_t kb, int64_t nb) {
     __shared__ float s_red[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
-    const int64_t kb = blockIdx.x, nb = blockIdx.y;
     const int64_t row0 = nb * 128 + warp * 16 + half;
     const int64_t col = kb * 128 + l16 * 8;
 
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restr
     amax = s_red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_red[i]);
-    const BlockScale bs = make_scale(amax, pow2 != 0);
+    const BlockScale bs = make_scale(amax, pow2);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         __stcs(reinterpret_cast<uint2*>(q + (row0 + 2 * i) * ldq + col), quant8(v[i], bs));
@@ -170,6 +177,46 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restr
         else
             s[nb * KB + kb] = bs.s;
     }
+}
+
+__global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int64_t KB, int64_t ldw,
+                                                         uint8_t* __restrict__ q, int64_t ldq,
+                                                         float* __restrict__ s, int pow2, uint8_t* __restrict__ s8) {
+    weight_tile_128x128(w, KB, ldw, q, ldq, s, pow2 != 0, s8, blockIdx.x, blockIdx.y);
+}
+
+// ---------------------------------------------------------------------------
+// A layer's activations (1x128) and weights (128x128) in one launch: CTAs
+// 0 .. NB*KB-1 take the weight tiles (kb fastest), the rest the activation
+// tiles (row tiles fastest), so neither quantiser's ramp and tail is paid
+// on its own.  Same tiles, same code as the two kernels above.
+// ---------------------------------------------------------------------------
+template <bool POW2>
+__global__ void __launch_bounds__(256, 4) k_quant_act_weight(const uint16_t* __restrict__ x, int64_t M, int64_t ldx,
+                                                             uint8_t* __restrict__ qa, int64_t ldqa,
+                                                             float* __restrict__ sa, int64_t ldsa,
+                                                             const uint16_t* __restrict__ w, int64_t NB, int64_t ldw,
+                                                             uint8_t* __restrict__ qw, int64_t ldqw,
+                                                             float* __restrict__ sw, int64_t KB, int64_t act_rows) {
+    const int64_t b = blockIdx.x, wt = NB * KB;
+    if (b < wt) {
+        weight_tile_128x128(w, KB, ldw, qw, ldqw, sw, POW2, nullptr, b % KB, b / KB);
+    } else {
+        const int64_t a = b - wt;
+        act_tile_1x128<POW2>(x, M, KB, ldx, qa, ldqa, sa, ldsa, nullptr, a % act_rows, a / act_rows);
+    }
+}
+
+cudaError_t launch_quant_act_weight(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qa, int64_t ldqa,
+                                    float* sa, int64_t ldsa, const void* w, int64_t N, int64_t ldw, uint8_t* qw,
+                                    int64_t ldqw, float* sw, bool pow2, cudaStream_t st) {
+    const int64_t KB = K / 128, NB = N / 128;
+    const int64_t act_rows = (M + kActRows - 1) / kActRows, act_kbs = (KB + kActKB - 1) / kActKB;
+    const int64_t blocks = NB * KB + act_rows * act_kbs;
+    auto kern = pow2 ? k_quant_act_weight<true> : k_quant_act_weight<false>;
+    kern<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, ldx, qa, ldqa, sa, ldsa,
+                                          static_cast<const uint16_t*>(w), NB, ldw, qw, ldqw, sw, KB, act_rows);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,

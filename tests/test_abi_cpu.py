@@ -448,3 +448,28 @@ def test_grouped_wgrad_validation(L):
         assert call() == 6
         assert call(flags=0x11) == 6              # promote path, pow2 scales
 
+
+def test_quant_act_weight_validation(L):
+    """The layer quantiser takes the union of the two quantisers' rules."""
+    f = L.fp8_quant_act_weight
+    ok = dict(x=A16, M=8, K=256, ldx=256, qa=A16b, ldqa=256, sa=A16c, ldsa=8, w=A16, N=128, ldw=256, qw=A16b,
+              ldqw=256, sw=A16c, mode=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["M"], a["K"], a["ldx"], a["qa"], a["ldqa"], a["sa"], a["ldsa"], a["w"], a["N"], a["ldw"],
+                 a["qw"], a["ldqw"], a["sw"], a["mode"], NULL)
+
+    assert call(w=NULL) == 1
+    assert call(x=NULL) == 1
+    assert call(x=NULL, M=0) in (0, 6)           # weights only: x is not needed
+    assert call(K=200) == 2
+    assert call(N=200) == 2
+    assert call(ldsa=4) == 2                     # ldsa < M
+    assert call(ldqw=128) == 2                   # ldqw < K
+    assert call(ldqa=264) == 3                   # row pitch not a multiple of 16 bytes
+    assert call(sw=A16c + 2) == 3
+    assert call(mode=5) == 4
+    if not _has_gpu():
+        assert call() == 6
+

@@ -145,3 +145,55 @@ def test_weight_llama_full_size_sampled_tiles(ops):
         qo, so = O.quant_weight_128x128(bf16_to_np(t))
         assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128].cpu().numpy(), qo)
         assert s[nb, kb].item() == float(so[0, 0])
+
+
+# ------------------------------------------------------------ one launch for a layer
+def _layer_gpu(ops, x, w, pow2):
+    """fp8_quant_act_weight on device copies of x [M, K] and w [N, K]; the
+    output buffers are pre-filled so that a missed write shows."""
+    M, K = x.shape
+    N = w.shape[0]
+    qa = torch.full((M, K), 0xAA, dtype=torch.uint8, device="cuda")
+    sa = torch.full((K // 128, ops.round_up(max(M, 1), 4)), -7.0, dtype=torch.float32, device="cuda")
+    qw = torch.full((N, K), 0xAA, dtype=torch.uint8, device="cuda")
+    sw = torch.full((N // 128, K // 128), -7.0, dtype=torch.float32, device="cuda")
+    ops.fp8_quant_act_weight(x.cuda(), qa, sa, w.cuda(), qw, sw, ops.FP8_SCALE_POW2 if pow2 else 0)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    return qa, sa, qw, sw
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 384, 640), (1, 128, 128), (0, 256, 256), (129, 1152, 384)])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_act_weight_one_launch_ragged(ops, M, N, K, pow2):
+    """The layer quantiser writes what the oracle's two quantisers give, and
+    nothing outside the activations' M rows."""
+    x = I.normal_bf16(I.stream(M + 3, 1), (max(M, 1), K))[:M].contiguous()
+    w = I.normal_bf16(I.stream(N + 5, 2), (N, K), std=0.02)
+    qa, sa, qw, sw = _layer_gpu(ops, x, w, pow2)
+    qw_o, sw_o = O.quant_weight_128x128(bf16_to_np(w), pow2)
+    assert np.array_equal(qw.cpu().numpy(), qw_o) and np.array_equal(sw.cpu().numpy(), sw_o)
+    if M:
+        qa_o, sa_o = O.quant_act_1x128(bf16_to_np(x), pow2)
+        assert np.array_equal(qa.cpu().numpy(), qa_o)
+        s = sa.cpu().numpy()
+        assert np.array_equal(s[:, :M].T, sa_o) and np.all(s[:, M:] == -7.0)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_act_weight_one_launch_equals_two_launches_llama(ops, pow2):
+    """All three Llama-3.1-8B layers at full size: codes and scales of the one
+    launch are bit-identical to the two separate quantisers' (which the
+    whole-output tests compare with the oracle)."""
+    mode = ops.FP8_SCALE_POW2 if pow2 else 0
+    for c in I.llama8b_layers(0):
+        x, w = c.a.cuda(), c.w.cuda()
+        qa, sa, qw, sw = _layer_gpu(ops, c.a, c.w, pow2)
+        qa2, sa2 = torch.empty_like(qa), torch.empty_like(sa)
+        qw2, sw2 = torch.empty_like(qw), torch.empty_like(sw)
+        ops.fp8_quant_act_1x128(x, qa2, sa2, mode)
+        ops.fp8_quant_weight_128x128(w, qw2, sw2, mode)
+        torch.cuda.synchronize()
+        M = x.shape[0]
+        assert torch.equal(qa, qa2) and torch.equal(sa[:, :M], sa2[:, :M]), c.name
+        assert torch.equal(qw, qw2) and torch.equal(sw, sw2), c.name
