@@ -15,7 +15,8 @@
 // Design (one CTA per SM, persistent over output tiles of 128 x BN, BN = 128
 // or 256):
 //   warp 0      TMA producer: qa tile 128x128 and qb tile BNx128 per K-block
-//               into a 192 KB shared-memory ring (128-byte swizzle).
+//               into a shared-memory ring (128-byte swizzle): 4 stages, 192 KB
+//               (3 stages for the weight-gradient form, see WHOLE_OUT).
 //   warps 1, 3  MMA issuers, one thread each, taking alternate K-blocks: four
 //               tcgen05.mma (M=128, N=BN, K=32) per K-block into one of
 //               512/BN BN-column TMEM buffers, the first with accumulate = 0.
@@ -55,28 +56,36 @@ constexpr int EPI_WARP0 = 4;                 // first promotion warp
 constexpr int SCALE_WARP = 2;
 constexpr int MAX_GROUPS = 1024;
 constexpr int SRING = 8;                     // scale ring slots
-constexpr int EPI_BUF_BYTES = 32 * 64;       // one 32 x 32 bf16 output block per promotion warp
+constexpr int EPI_BLK_BYTES = 32 * 64;       // one 32 x 32 bf16 output block
 
-template <int BN_>
+// WHOLE_OUT (BN 256 only): a 3-stage operand ring (144 KB) leaves room for
+// each promotion warp to stage its whole 32 x 128 output (8 KB), so its TMA
+// stores drain during the next tile instead of one 2 KB block at a time.
+// That pays where the output is large against the work (weight gradients:
+// 4-11% faster) and costs the long-K forward GEMMs the fourth stage (5-7%
+// slower), so only the per-row-scale (weight-gradient) instantiations use it.
+template <int BN_, bool WHOLE_OUT_ = false>
 struct Cfg {
     static constexpr int BN = BN_;
+    static constexpr bool WHOLE_OUT = WHOLE_OUT_ && BN_ == 256;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 4;                          // 192 KB (BN 256) or 128 KB (BN 128)
+    static constexpr int STAGES = WHOLE_OUT ? 3 : 4;          // 144 / 192 KB (BN 256) or 128 KB (BN 128)
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int NBUF = 512 / BN;                     // TMEM accumulator buffers
     static constexpr int EPI_WARPS = BN == 128 ? 16 : 8;
     static constexpr int SLICES = EPI_WARPS / 4;              // column slices per TMEM lane quarter
     static constexpr int EPI_COLS = BN / SLICES;              // columns per promotion warp
     static constexpr int CHUNKS = EPI_COLS / 32;
+    static constexpr int EPI_BUF_BYTES = (WHOLE_OUT ? CHUNKS : 1) * EPI_BLK_BYTES;   // per promotion warp
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr bool SPLIT_REGS = BN == 256;
     static constexpr int LAUNCH_REGS = 168;                   // 65536 / 384, rounded to 8 (BN 256)
     static constexpr int REGS_CTRL = 40;                      // warpgroup 0 after setmaxnreg.dec
     static constexpr int REGS_EPI = 232;                      // promotion warpgroups after .inc
     static constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
-    static_assert(STAGES % 2 == 0 && NBUF % 2 == 0, "each stage / buffer belongs to one MMA issuer");
+    static_assert(NBUF % 2 == 0, "each TMEM buffer belongs to one MMA issuer");
     static_assert(STAGES <= 8 && NBUF <= 4, "barrier arrays");
     static_assert(!SPLIT_REGS || (128 * REGS_CTRL + (THREADS - 128) * REGS_EPI <= THREADS * LAUNCH_REGS),
                   "register split exceeds the launch");
@@ -107,7 +116,8 @@ struct __align__(16) Ctrl {
 // group table.
 template <int BN, bool ROWB = false>
 constexpr size_t smem_bytes() {
-    return 1024 /*align slack*/ + (size_t)Cfg<BN>::RING_BYTES + (size_t)Cfg<BN>::EPI_WARPS * EPI_BUF_BYTES +
+    using C = Cfg<BN, ROWB>;
+    return 1024 /*align slack*/ + (size_t)C::RING_BYTES + (size_t)C::EPI_WARPS * C::EPI_BUF_BYTES +
            sizeof(Ctrl) + (size_t)(MAX_GROUPS + 4) * sizeof(int32_t) + (ROWB ? (size_t)SRING * BN * sizeof(float) : 0);
 }
 static_assert(smem_bytes<256, true>() <= 232448 && smem_bytes<128, true>() <= 232448, "shared memory per CTA");
@@ -126,18 +136,18 @@ __device__ __forceinline__ void record_timeout(int* status) {
 // run expert by expert; C_g is rows g M .. g M + M - 1 of the output (M %
 // 128 == 0); an expert without tokens gets zeros.
 template <int BN, bool GROUPED, bool ROWB, bool KGROUP = false>
-__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<BN, ROWB>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo,
                    uint64_t wait_ns, int skip_first_load, int kg_tokens) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, ROWB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)C::RING_BYTES;   // 1024-byte aligned
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)C::EPI_WARPS * EPI_BUF_BYTES);
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(epi_buf + (size_t)C::EPI_WARPS * C::EPI_BUF_BYTES);
     int32_t* cum = reinterpret_cast<int32_t*>(ctl + 1);
     float* sb_ring = reinterpret_cast<float*>(cum + MAX_GROUPS + 4);   // ROWB: [SRING][BN], 16-byte aligned
     static_assert(!(ROWB && GROUPED), "per-row B scales are dense only");
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                     const BlockScale bs = make_scale(absmax_pair_to_f32(m2), qo.pow2 != 0);
                     if (vrow) qo.s[(size_t)(col0 / 128) * qo.lds + m] = bs.s;
                     // two 32 x 64-byte halves through the warp's buffer (64-byte swizzle)
-                    uint8_t* qbuf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
+                    uint8_t* qbuf = epi_buf + (size_t)(warp - EPI_WARP0) * C::EPI_BUF_BYTES;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         if (lane == 0) bulk_wait_group_read<0>();
@@ -512,16 +522,13 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             }
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
-                // 32 x 32 blocks through this warp's 2 KB buffer and TMA stores:
-                // row `lane`, 16-byte piece k at lane*64 + ((k ^ ((lane >> 1) & 3))
-                // << 4), the 64-byte swizzle of the output tensor map.  (Stores
-                // straight from registers put one 16-byte piece of 32 rows in each
-                // instruction and held these warps for thousands of cycles.)
-                uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * EPI_BUF_BYTES;
-#pragma unroll
-                for (int cc = 0; cc < C::CHUNKS; ++cc) {
-                    if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
-                    __syncwarp();
+                uint8_t* buf = epi_buf + (size_t)(warp - EPI_WARP0) * C::EPI_BUF_BYTES;
+                // One 32 x 32 bf16 sub-block cc into shared memory: row `lane`,
+                // 16-byte piece k at lane*64 + ((k ^ ((lane >> 1) & 3)) << 4), the
+                // 64-byte swizzle of the output tensor map.  (Stores straight from
+                // registers put one 16-byte piece of 32 rows in each instruction
+                // and held these warps for thousands of cycles.)
+                auto stage_block = [&](uint8_t* dst, int cc) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint32_t p[4];
@@ -530,14 +537,39 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
                             const int col = 8 * k + 2 * e;
                             asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(p[e]) : "f"(acc[cc][col + 1]), "f"(acc[cc][col]));
                         }
-                        *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                        *reinterpret_cast<uint4*>(dst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
                             make_uint4(p[0], p[1], p[2], p[3]);
                     }
+                };
+                const int crow = (KGROUP ? tl.g * M : 0) + tl.m0 + q * 32;
+                if constexpr (C::WHOLE_OUT) {
+                    // all sub-blocks staged, then one TMA store each; they drain
+                    // while the warp promotes the next tile
+                    if (lane == 0) bulk_wait_group_read<0>();   // the previous tile's stores have read buf
+                    __syncwarp();
+#pragma unroll
+                    for (int cc = 0; cc < C::CHUNKS; ++cc) stage_block(buf + cc * EPI_BLK_BYTES, cc);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tm_c, buf, col0 + 32 * cc, (KGROUP ? tl.g * M : 0) + tl.m0 + q * 32);
+#pragma unroll
+                        for (int cc = 0; cc < C::CHUNKS; ++cc)
+                            tma_store_2d(&tm_c, buf + cc * EPI_BLK_BYTES, col0 + 32 * cc, crow);
                         bulk_commit_group();
+                    }
+                } else {
+                    // one sub-block at a time through the warp's 2 KB buffer
+#pragma unroll
+                    for (int cc = 0; cc < C::CHUNKS; ++cc) {
+                        if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read buf
+                        __syncwarp();
+                        stage_block(buf, cc);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_c, buf, col0 + 32 * cc, crow);
+                            bulk_commit_group();
+                        }
                     }
                 }
             } else if (vrow) {
@@ -576,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
 
 template <int BN, bool GROUPED, bool ROWB = false, bool KGROUP = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, ROWB>;
     static DeviceOnce attr_done;     // kernel attributes set on this device
     auto kern = k_gemm_promote<BN, GROUPED, ROWB, KGROUP>;
     int dev = 0;
