@@ -872,8 +872,9 @@ def moe_wgrad_measure(args, ops, stream, dev, flush, fp8_peak, m, projs, offs):
                       qx=torch.empty((K, 128 * nb), dtype=torch.uint8, device=dev),
                       sx=torch.empty((nb, ops.round_up(K, 4)), dtype=torch.float32, device=dev),
                       dw=torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)))
-    out = {"what": "per projection: grouped 128x1 quantiser of dY and of X, grouped wgrad GEMM (promote "
-                   "kernel, per-expert K ranges from device offsets); 3 launches for all experts",
+    out = {"what": "per projection: grouped 128x1 quantiser of dY and of X, grouped wgrad GEMM (per-expert K "
+                   "ranges from device offsets; promote kernel for fp32 scales, MX kernel for pow2 scales); "
+                   "3 launches for all experts",
            "modes": {}}
     for pow2 in (False, True):
         mode = ops.FP8_SCALE_POW2 if pow2 else ops.FP8_SCALE_FP32_AMAX
@@ -895,6 +896,7 @@ def moe_wgrad_measure(args, ops, stream, dev, flush, fp8_peak, m, projs, offs):
                                "quant_wgrad_tflops": gf / ((qg_ms + qx_ms + g_ms) / 1e3) / 1e12}
         flops = sum(2.0 * P["T"] * P["N"] * P["K"] for P in W)
         out["modes"]["pow2" if pow2 else "fp32"] = {
+            "wgrad_kernel": "mx (K-grouped)" if pow2 else "promote (K-grouped)",
             "ms_per_step": total, "quant_wgrad_tflops": flops / (total / 1e3) / 1e12, "projections": rows,
             "gpu_launches": 3 * len(W) * args.steps}
     return out

@@ -583,7 +583,10 @@ fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t* qa, int64_t lda, co
     if (flags & ~kKnownFlags) return FP8_ERR_SCALE_MODE;
     const uint32_t path = flags & FP8_GEMM_PATH_MASK;
     if (path > FP8_GEMM_PATH_SKINNY) return FP8_ERR_SCALE_MODE;
-    if (path == FP8_GEMM_PATH_MX || path == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    if (path == FP8_GEMM_PATH_MX && !(flags & FP8_GEMM_SCALES_POW2)) return FP8_ERR_SCALE_MODE;
+    if (path == FP8_GEMM_PATH_SKINNY) return FP8_ERR_NOT_IMPLEMENTED;
+    // power-of-two scales accumulate in TMEM with hardware scale factors (MX)
+    const bool mx = path == FP8_GEMM_PATH_MX || (path == FP8_GEMM_PATH_AUTO && (flags & FP8_GEMM_SCALES_POW2));
     if (M < 0 || N < 0 || (M % 128) || (N % 128) || M > (1ll << 24) || N > (1ll << 24)) return FP8_ERR_SHAPE;
     if (G < 1 || G > kMaxGroupedQuantExperts || T < 0 || T > INT32_MAX / 2) return FP8_ERR_SHAPE;
     if ((int64_t)G * M > INT32_MAX) return FP8_ERR_SHAPE;
@@ -615,7 +618,7 @@ fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t* qa, int64_t lda, co
     a.status = d->status;
     a.sm_count = d->sm_count;
     a.splits = 1;
-    a.bn = promote_tile_n(M, N, kcap, G);
+    a.bn = mx ? kMxTileN : promote_tile_n(M, N, kcap, G);
     if (fp8_status e = tensor_map(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, (uint64_t)G * M, ldc * 2, 32, 32,
                                   CU_TENSOR_MAP_SWIZZLE_64B, &a.tm_c))
         return e;
@@ -625,7 +628,8 @@ fp8_status fp8_blockscaled_grouped_gemm_wgrad(const uint8_t* qa, int64_t lda, co
     if (fp8_status e = tensor_map(qb, CU_TENSOR_MAP_DATA_TYPE_UINT8, kcap, N, ldb, 128, (uint32_t)a.bn,
                                   CU_TENSOR_MAP_SWIZZLE_128B, &a.tm_b))
         return e;
-    return cuda_status(launch_gemm_promote(a, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(mx ? launch_gemm_mx(a, st) : launch_gemm_promote(a, st));
 }
 
 fp8_status fp8_tensorscaled_gemm(const uint8_t* qa, int64_t lda, const float* sa, const uint8_t* qb, int64_t ldb,

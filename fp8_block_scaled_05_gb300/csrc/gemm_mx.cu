@@ -146,13 +146,19 @@ __device__ __forceinline__ float scale_at(const float* __restrict__ p, size_t i,
     return __uint_as_float(b == 0u ? 0x00400000u : b << 23);
 }
 
-template <bool GROUPED, bool PER_TENSOR = false>
+// KGROUP (mixture-of-experts weight gradients, per-row B scales): G GEMMs
+// C_g [M, N] = A_g B_g^T reducing over each expert's own padded token blocks
+// P_g .. P_{g+1}-1 (P_g = sum_{g' < g} ceil(M_g' / 128) over the device
+// offsets of kg_tokens tokens), the layout the grouped 128x1 quantiser
+// writes; C_g is rows g M .. of the output, zeros for an expert without
+// tokens (its tiles issue no MMA and never touch TMEM).
+template <bool GROUPED, bool PER_TENSOR = false, bool KGROUP = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
               const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
               uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K, const int32_t* __restrict__ offsets, int G,
-              int* status, SplitTail split, QuantOut qo, int e8) {
+              int* status, SplitTail split, QuantOut qo, int e8, int kg_tokens) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)RING_BYTES;   // 1024-byte aligned
@@ -190,6 +196,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (GROUPED) {
             const int total = build_group_table<BM>(offsets, G, M, NT, cum);
             if (lane == 0) ctl->n_tiles = total;
+        } else if (KGROUP) {
+            // cum[g]: the first padded token block of expert g
+            build_group_table<BM>(offsets, G, kg_tokens, 1, cum);
+            if (lane == 0) ctl->n_tiles = G * ((M + BM - 1) / BM) * NT;
         } else if (lane == 0) {
             ctl->n_tiles = ((M + BM - 1) / BM) * NT;
         }
@@ -200,6 +210,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const int n_tiles = ctl->n_tiles;
     const int n_items = work_items(n_tiles, split);
+    const int tiles_per_expert = ((M + BM - 1) / BM) * NT;   // KGROUP
+    // Work item t and its tile (with KGROUP: the expert's K range and tile).
+    auto item_at = [&](int t) -> Item {
+        Item w = decode_item(t, split, KB);
+        if constexpr (KGROUP) {
+            const int g = w.tile / tiles_per_expert;
+            w.kb0 = cum[g];
+            w.kb1 = cum[g + 1];
+        }
+        return w;
+    };
+    auto tile_at = [&](const Item& w) -> Tile {
+        if constexpr (KGROUP) {
+            Tile tl = decode_tile<BM, BN, false>(w.tile % tiles_per_expert, M, N, cum, offsets, G);
+            tl.g = w.tile / tiles_per_expert;
+            return tl;
+        } else {
+            return decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -207,8 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-                const Item w = decode_item(t, split, KB);
-                const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+                const Item w = item_at(t);
+                const Tile tl = tile_at(w);
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
                     if (!mbar_wait(&ctl->empty[s], ph ^ 1, kWaitLimitNs)) {
@@ -232,10 +262,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else if (warp == GATE_WARP) {
         // ------------------------------------------------ gatekeeper
-        uint32_t it = 0, gi = 0, tt = 0;
+        uint32_t it = 0, gi = 0, tt = 0;   // tt: items that use the accumulator (an empty K range does not)
         bool ok = true;
-        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tt) {
-            const Item w = decode_item(t, split, KB);
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+            const Item w = item_at(t);
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                 const uint32_t byte = (uint32_t)(kb - w.kb0) % KB_PER_SF;
                 if (lane == 0 && ok) {
@@ -250,12 +280,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 named_bar_sync(kIssueBar, 64);   // K-block `it` may be issued
                 if (byte == KB_PER_SF - 1 || kb == w.kb1 - 1) ++gi;
             }
+            if (w.kb1 > w.kb0) ++tt;
         }
     } else if (warp == ISSUE_WARP) {
         // ------------------------------------------------ MMA issuer
         uint32_t it = 0, gi = 0;
         for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
-            const Item w = decode_item(t, split, KB);
+            const Item w = item_at(t);
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t byte = (uint32_t)(kb - w.kb0) % KB_PER_SF;
@@ -293,8 +324,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t gi = 0;
         bool ok = true, bad = false;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item w = decode_item(t, split, KB);
-            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+            const Item w = item_at(t);
+            const Tile tl = tile_at(w);
             const int m = tl.m0 + q * 32 + lane;
             const bool vrow = m < tl.row_end;
             const int nb0 = tl.n0 / 128;
@@ -383,14 +414,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto scaled = [&](uint32_t v) -> uint32_t {
             return PER_TENSOR ? __float_as_uint(__uint_as_float(v) * ts) : v;
         };
-        uint32_t tt = 0;
+        uint32_t tt = 0;   // items that used the accumulator so far
         bool ok = true;
-        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tt) {
-            const Item w = decode_item(t, split, KB);
-            const Tile tl = decode_tile<BM, BN, GROUPED>(w.tile, M, N, cum, offsets, G);
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+            const Item w = item_at(t);
+            const Tile tl = tile_at(w);
             const int m = tl.m0 + q * 32 + lane;
             const int col0 = tl.n0 + h * 128;
+            const int crow = (KGROUP ? tl.g * M : 0) + tl.m0 + q * 32;   // first output row of this warp
+            if (KGROUP && w.kb1 == w.kb0) {
+                // an expert without tokens: its gradient is zero (no MMA, no TMEM)
+                if (col0 < N) {
+                    uint32_t z[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) z[jj] = 0u;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) store_block(z, col0 + 32 * cc, crow);
+                }
+                continue;
+            }
             bool got = mbar_wait_sleep(&ctl->tfull, tt & 1, kWaitLimitNs);
+            ++tt;
             got = __all_sync(0xFFFFFFFFu, got);
             if (!got) {
                 ok = false;
@@ -447,7 +491,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int jj = 0; jj < 16; ++jj)
                         pk[jj] = pack_bf16x2(scaled(__float_as_uint(sum[2 * jj])),
                                              scaled(__float_as_uint(sum[2 * jj + 1])));
-                    store_block(pk, col0 + 32 * cc, tl.m0 + q * 32);
+                    store_block(pk, col0 + 32 * cc, crow);
                 }
                 continue;
             }
@@ -503,7 +547,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tm_q, buf, col0 + 64 * hf, tl.m0 + q * 32);
+                        tma_store_2d(&tm_q, buf, col0 + 64 * hf, crow);
                         bulk_commit_group();
                     }
                 }
@@ -512,7 +556,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int rows_here = min(tl.row_end - (tl.m0 + q * 32), 32);
             if (!GROUPED || rows_here == 32) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) store_block(p + 16 * cc, col0 + 32 * cc, tl.m0 + q * 32);
+                for (int cc = 0; cc < 4; ++cc) store_block(p + 16 * cc, col0 + 32 * cc, crow);
             } else if (lane < rows_here) {
                 uint4* dst = reinterpret_cast<uint4*>(c + (size_t)m * ldc + col0);
 #pragma unroll
@@ -532,10 +576,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <bool GROUPED, bool PER_TENSOR = false>
+template <bool GROUPED, bool PER_TENSOR = false, bool KGROUP = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     static DeviceOnce attr_done;     // kernel attributes set on this device
-    auto kern = k_gemm_mx<GROUPED, PER_TENSOR>;
+    auto kern = k_gemm_mx<GROUPED, PER_TENSOR, KGROUP>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done.test(dev)) {
@@ -544,10 +588,11 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         attr_done.set(dev);
     }
     const int64_t NT = (a.N + BN - 1) / BN;
-    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT : ((a.M + BM - 1) / BM) * NT;
+    const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT
+                                  : ((a.M + BM - 1) / BM) * NT * (KGROUP ? a.G : 1);
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
-    if (!GROUPED && a.qout.q == nullptr) {   // the fused quantisation needs whole tiles
+    if (!GROUPED && !KGROUP && a.qout.q == nullptr) {   // the fused quantisation needs whole tiles
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kMxMaxParts);
         if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
             split.n_full = (int)tp.n_full;
@@ -558,7 +603,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     }
     kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, a.ldsb, static_cast<uint16_t*>(a.c), a.ldc,
                                             (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout,
-                                            a.scales_e8);
+                                            a.scales_e8, (int)a.kg_tokens);
     return cudaGetLastError();
 }
 
@@ -567,6 +612,10 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
 cudaError_t launch_gemm_mx(const GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;
     if (a.per_tensor) return a.offsets != nullptr ? cudaErrorInvalidValue : mx::launch<false, true>(a, st);
+    if (a.kgroup) {   // per-expert weight gradients over the experts' token blocks
+        if (a.offsets == nullptr || a.ldsb <= 0) return cudaErrorInvalidValue;
+        return mx::launch<false, false, true>(a, st);
+    }
     return a.offsets != nullptr ? mx::launch<true>(a, st) : mx::launch<false>(a, st);
 }
 

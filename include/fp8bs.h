@@ -309,9 +309,12 @@ FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const 
  *   c        device, bf16 [G * M, N] (row pitch ldc): dW_g at rows g M ..; an
  *            expert without tokens gets zeros
  *   M, N multiples of 128 (0: nothing to do); T and offsets as given to the quantiser;
- *   lda, ldb >= 128 * (ceil(T/128) + G).  flags: FP8_GEMM_SCALES_POW2 |
- *   FP8_GEMM_PATH_AUTO or _PROMOTE (the per-K-block promotion kernel);
- *   _MX, _SKINNY and FP8_GEMM_SCALES_E8 return FP8_ERR_NOT_IMPLEMENTED.
+ *   lda, ldb >= 128 * (ceil(T/128) + G).  flags: FP8_GEMM_PATH_AUTO runs
+ *   the per-K-block promotion kernel, or with FP8_GEMM_SCALES_POW2 (every
+ *   scale an exact power of two) the hardware block-scaled kernel, which
+ *   accumulates each expert's whole token range in TMEM; _PROMOTE and _MX
+ *   force one (_MX needs the pow2 promise: FP8_ERR_SCALE_MODE otherwise);
+ *   _SKINNY and FP8_GEMM_SCALES_E8 return FP8_ERR_NOT_IMPLEMENTED.
  */
 FP8BS_API fp8_status fp8_quant_act_128x1_grouped(const void *x, int64_t T, int64_t K, int64_t ldx,
                                                  const int32_t *offsets, int32_t G, uint8_t *qt, int64_t ldqt,

@@ -421,7 +421,8 @@ def test_quant_act_128x1_grouped_validation(L):
 
 
 def test_grouped_wgrad_validation(L):
-    """Grouped weight-gradient GEMM: fp32 scales on the promote path only."""
+    """Grouped weight-gradient GEMM: fp32 scales only (no UE8M0 bytes); the
+    MX path needs the power-of-two promise; no skinny path."""
     f = L.fp8_blockscaled_grouped_gemm_wgrad
     ok = dict(qa=A16, lda=768, sa=A16b, ldsa=256, qb=A16c, ldb=768, sb=A16, ldsb=128, offs=A16b, G=3, T=300,
               c=A16c, ldc=128, M=256, N=128, flags=0)
@@ -432,7 +433,7 @@ def test_grouped_wgrad_validation(L):
                  a["T"], a["c"], a["ldc"], a["M"], a["N"], a["flags"], NULL)
 
     assert call(flags=0x2) == 9                   # UE8M0 byte scales
-    assert call(flags=0x20) == 9                  # MX path
+    assert call(flags=0x20) == 4                  # MX path without the pow2 promise
     assert call(flags=0x30) == 9                  # skinny path
     assert call(M=200) == 2
     assert call(G=0) == 2
@@ -447,6 +448,7 @@ def test_grouped_wgrad_validation(L):
     if not _has_gpu():
         assert call() == 6
         assert call(flags=0x11) == 6              # promote path, pow2 scales
+        assert call(flags=0x21) == 6              # MX path, pow2 scales
 
 
 def test_quant_act_weight_validation(L):
