@@ -442,6 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t taddr = tacc;
+            uint32_t p[64];   // the warp's 32 x 128 block as bf16 pairs (row `lane`)
             if (w.parts > 1) {
                 // A K-split tile of the last wave (this CTA's last item): the fp32
                 // part goes straight from TMEM to the workspace, and the warp that
@@ -486,42 +487,40 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) sum[jj] += v[jj];
                     }
-                    uint32_t pk[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        pk[jj] = pack_bf16x2(scaled(__float_as_uint(sum[2 * jj])),
-                                             scaled(__float_as_uint(sum[2 * jj + 1])));
-                    store_block(pk, col0 + 32 * cc, crow);
+                        p[16 * cc + jj] = pack_bf16x2(scaled(__float_as_uint(sum[2 * jj])),
+                                                      scaled(__float_as_uint(sum[2 * jj + 1])));
                 }
-                continue;
-            }
-            // Three round trips (64, 32 and 32 columns), packed to bf16 pairs as
-            // they arrive so that at most 64 raw values are live; TMEM goes back
-            // before any store.
-            uint32_t p[64];
-            {
-                uint32_t v0[32], v1[32];
-                tmem_ld_x32(taddr, v0);
-                tmem_ld_x32(taddr + 32, v1);
-                tmem_ld_wait();
+                // the summed block goes on like a whole tile's (fused codes, C)
+            } else {
+                // Three round trips (64, 32 and 32 columns), packed to bf16 pairs as
+                // they arrive so that at most 64 raw values are live; TMEM goes back
+                // before any store.
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_x32(taddr, v0);
+                    tmem_ld_x32(taddr + 32, v1);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    p[jj] = pack_bf16x2(scaled(v0[2 * jj]), scaled(v0[2 * jj + 1]));
-                    p[16 + jj] = pack_bf16x2(scaled(v1[2 * jj]), scaled(v1[2 * jj + 1]));
+                    for (int jj = 0; jj < 16; ++jj) {
+                        p[jj] = pack_bf16x2(scaled(v0[2 * jj]), scaled(v0[2 * jj + 1]));
+                        p[16 + jj] = pack_bf16x2(scaled(v1[2 * jj]), scaled(v1[2 * jj + 1]));
+                    }
                 }
-            }
 #pragma unroll
-            for (int r = 2; r < 4; ++r) {
-                uint32_t v[32];
-                tmem_ld_x32(taddr + 32 * r, v);
-                tmem_ld_wait();
+                for (int r = 2; r < 4; ++r) {
+                    uint32_t v[32];
+                    tmem_ld_x32(taddr + 32 * r, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) p[16 * r + jj] = pack_bf16x2(scaled(v[2 * jj]), scaled(v[2 * jj + 1]));
+                    for (int jj = 0; jj < 16; ++jj) p[16 * r + jj] = pack_bf16x2(scaled(v[2 * jj]), scaled(v[2 * jj + 1]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty);
+                if (col0 >= N) continue;   // the half of a 256-wide tile past N
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tempty);
-            if (col0 >= N) continue;   // the half of a 256-wide tile past N
             if (!GROUPED && qo.q != nullptr) {
                 // Fused quantisation for the next layer: this warp holds, per row,
                 // the whole 128-column block col0 .. col0 + 127 as bf16 pairs, so
@@ -592,7 +591,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
                                   : ((a.M + BM - 1) / BM) * NT * (KGROUP ? a.G : 1);
     const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
-    if (!GROUPED && !KGROUP && a.qout.q == nullptr) {   // the fused quantisation needs whole tiles
+    if (!GROUPED && !KGROUP) {
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kMxMaxParts);
         if (tp.parts > 1 && a.workspace && a.ws_bytes >= tp.bytes) {
             split.n_full = (int)tp.n_full;
