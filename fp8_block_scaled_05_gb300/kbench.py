@@ -27,7 +27,7 @@ def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", required=True,
                    choices=["quant_act", "quant_weight", "gemm", "grouped", "quant_act_t", "quant_weight_t", "wgrad",
-                            "pt_gemm", "attention", "moe_wgrad"])
+                            "pt_gemm", "attention", "moe_wgrad", "quant_layer"])
     p.add_argument("--dual", action="store_true", help="quant_act_t / quant_weight_t: also the other layout")
     p.add_argument("--M", type=int, default=4096)
     p.add_argument("--N", type=int, default=4096)
@@ -58,6 +58,16 @@ def main(argv=None):
         s = torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev)
         run = lambda: ops.fp8_quant_act_1x128(x, q, s, mode)  # noqa: E731
         work, unit = 3.0 * M * K + 4.0 * M * (K // 128), "GB/s"
+    elif a.kernel == "quant_layer":
+        # activations x [M, K] (1x128) and weights w [N, K] (128x128) in one launch
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((K // 128, ops.round_up(M, 4)), dtype=torch.float32, device=dev)
+        qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+        run = lambda: ops.fp8_quant_act_weight(x, qa, sa, w, qw, sw, mode)  # noqa: E731
+        work, unit = 3.0 * (M + N) * K + 4.0 * M * (K // 128) + 4.0 * (N // 128) * (K // 128), "GB/s"
     elif a.kernel == "quant_weight":
         w = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
         q = torch.empty((N, K), dtype=torch.uint8, device=dev)
