@@ -176,23 +176,41 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle sample
-def oracle_sample(layers, rows_a=CPU_SAMPLE_ROWS_A, rows_w=CPU_SAMPLE_ROWS_W):
+def oracle_sample(layers, rows_a=CPU_SAMPLE_ROWS_A, rows_w=CPU_SAMPLE_ROWS_W, parts=None):
     """Time the CPU oracle on a bounded sample of each layer (first rows_a rows
     of A, first rows_w rows of W): quant A, quant W, GEMM.  Returns
-    (flops of the sample, seconds)."""
+    (flops of the sample, seconds); with a dict `parts`, also fills in each
+    step's own rate (quantisers in GB/s of 3 bytes per element, the GEMM in
+    GFLOP/s) over the sample."""
     import numpy as np
     import oracle.fp8_oracle as O
     flops = 0.0
+    tq = [0.0, 0.0, 0.0]
+    nq = [0.0, 0.0]
     t0 = time.perf_counter()
     for a, w in layers:
         xa = a[:rows_a].float().numpy()
         xw = w[:rows_w].float().numpy()
+        t1 = time.perf_counter()
         qa, sa = O.quant_act_1x128(xa)
+        t2 = time.perf_counter()
         qw, sw = O.quant_weight_128x128(xw)
+        t3 = time.perf_counter()
         c = O.gemm_ref(qa, sa, qw, sw)
+        t4 = time.perf_counter()
         assert np.isfinite(c).all()
+        tq[0] += t2 - t1
+        tq[1] += t3 - t2
+        tq[2] += t4 - t3
+        nq[0] += xa.size
+        nq[1] += xw.size
         flops += 2.0 * xa.shape[0] * xw.shape[0] * xa.shape[1]
-    return flops, time.perf_counter() - t0
+    secs = time.perf_counter() - t0
+    if parts is not None:
+        parts["quant_act"] = {"GB/s": 3.0 * nq[0] / tq[0] / 1e9, "seconds": tq[0]}
+        parts["quant_weight"] = {"GB/s": 3.0 * nq[1] / tq[1] / 1e9, "seconds": tq[1]}
+        parts["gemm"] = {"GFLOP/s": flops / tq[2] / 1e9, "seconds": tq[2]}
+    return flops, secs
 
 
 def blas_threads():
@@ -555,9 +573,10 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         layers_cpu = [(c.a, c.w) for c in cases]
-        f, s = oracle_sample(layers_cpu)
+        parts = {}
+        f, s = oracle_sample(layers_cpu, parts=parts)
         cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": sample_desc(), "seconds": s}
+               "sample": sample_desc(), "seconds": s, "per_step": parts}
 
     if rank == 0:
         line = {
