@@ -756,17 +756,19 @@ def qwen_measure(args, ops, stream, dev, flush, fp8_peak):
 def decode_measure(args, ops, stream, dev, flush, hbm_peak):
     """Decode-sized layers: M in {1, 8, 64, 256} tokens at (K, N) = (4096,
     6144) and (14336, 4096), weights pre-quantised 128x128 (fp32 scales).  A
-    decode step is the 1x128 quantiser of the bf16 activations and the skinny
-    GEMM; each is replayed from a CUDA graph with the L2 flushed before every
-    step.  Algorithmic bytes of the step: N K (weight codes) + 4 N K / 16384
+    decode step is the 1x128 quantiser of the bf16 activations and the GEMM on
+    the automatic path (the skinny kernel up to 128 tokens, the promote kernel
+    with every tile split along K above); each is replayed from a CUDA graph
+    with the L2 flushed before every step.  Algorithmic bytes of the step: N K (weight codes) + 4 N K / 16384
     (weight scales) + 2 M K (bf16 activations) + 2 M N (bf16 output); of the
     GEMM alone the activations count as M K codes + 4 M K / 128 scales."""
     import torch
 
     from fp8_block_scaled_05_gb300 import inputs as I
 
-    out = {"what": "quant_act (bf16 A -> E4M3 1x128) + skinny GEMM on pre-quantised weights, CUDA-graph replays, "
-                   "L2 flushed before each step", "points": {}}
+    out = {"what": "quant_act (bf16 A -> E4M3 1x128) + GEMM (automatic path) on pre-quantised weights, "
+                   "CUDA-graph replays, L2 flushed before each step", "points": {}}
+    path_name = {v: k for k, v in ops.PATHS.items()}
     fracs = []
     for K, N in I.DECODE_SHAPES:
         w = I.decode_case(1, K, N, args.seed).w.to(dev)
@@ -796,7 +798,8 @@ def decode_measure(args, ops, stream, dev, flush, hbm_peak):
                   "step_frac_hbm": step_bytes / (step_ms / 1e3) / 1e9 / hbm_peak,
                   "gemm_us": gemm_ms * 1e3, "gemm_GB/s": gemm_bytes / (gemm_ms / 1e3) / 1e9,
                   "gemm_frac_hbm": gemm_bytes / (gemm_ms / 1e3) / 1e9 / hbm_peak,
-                  "gemm_tflops": 2.0 * M * N * K / (gemm_ms / 1e3) / 1e12, "ctas": ctas}
+                  "gemm_tflops": 2.0 * M * N * K / (gemm_ms / 1e3) / 1e12, "path": path_name.get(path, path),
+                  "skinny_ctas": ctas if path == ops.FP8_GEMM_PATH_SKINNY else None}
             fracs.append(pt["step_frac_hbm"])
             out["points"][f"M{M}.K{K}.N{N}"] = pt
     out["min_step_frac_hbm"] = min(fracs)

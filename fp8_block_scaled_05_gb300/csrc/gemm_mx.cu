@@ -589,7 +589,6 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT
                                   : ((a.M + BM - 1) / BM) * NT * (KGROUP ? a.G : 1);
-    const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
     if (!GROUPED && !KGROUP) {
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kMxMaxParts);
@@ -600,6 +599,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
+    const int64_t items = work_items((int)tiles, split);
+    const int grid = (int)(items < a.sm_count ? items : a.sm_count);
     kern<<<grid, THREADS, SMEM_BYTES, st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb, a.ldsb, static_cast<uint16_t*>(a.c), a.ldc,
                                             (int)a.M, (int)a.N, (int)a.K, a.offsets, a.G, a.status, split, a.qout,
                                             a.scales_e8, (int)a.kg_tokens);

@@ -726,7 +726,6 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     const int64_t NT = (a.N + BN - 1) / BN;
     const int64_t tiles = GROUPED ? (((a.M + BM - 1) / BM) + a.G) * NT
                                   : ((a.M + BM - 1) / BM) * NT * (KGROUP ? a.G : 1);
-    const int grid = (int)(tiles < a.sm_count ? tiles : a.sm_count);
     SplitTail split{0, 1, nullptr, nullptr};
     if (!GROUPED && !KGROUP) {
         const TailPlan tp = tail_plan(a.M, a.N, a.K, a.sm_count, BN, kPromoteMaxParts);
@@ -737,6 +736,8 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
             split.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + tp.ticket_bytes);
         }
     }
+    const int64_t items = work_items((int)tiles, split);
+    const int grid = (int)(items < a.sm_count ? items : a.sm_count);
     kern<<<grid, C::THREADS, smem_bytes<BN, ROWB>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
                                                            a.ldsb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
                                                      (int)a.K, a.offsets, a.G, a.status, split, a.qout,
@@ -746,27 +747,38 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
 
 }  // namespace promote
 
-// Split of the last wave (dense): with `grid` = min(tiles, SMs) persistent
-// CTAs, the first (tiles / grid) * grid tiles fill whole waves; the L left
-// over are split along K into min(grid / L, KB / 8, max_parts) parts when
+// Split along K (dense).  With at least as many tiles as SMs, `grid` = SMs
+// persistent CTAs: the first (tiles / grid) * grid tiles fill whole waves and
+// the L left over are split into min(grid / L, KB / 8, max_parts) parts when
 // that is at least 2 (promote: 4; MX, whose single accumulator is held while
-// a part is written out: 2, and only when L >= grid / 4).
+// a part is written out: 2, and only when L >= grid / 4).  With fewer tiles
+// than SMs (small M) every tile is split, into min(SMs / tiles, KB / 8,
+// kSingleWaveMaxParts) parts, one per CTA, so that the parts fill the GPU.
 TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts) {
     TailPlan tp{0, 1, 0, 0};
     if (M <= 0 || bn <= 0 || sm_count <= 0) return tp;
     const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
-    const int64_t grid = tiles < sm_count ? tiles : sm_count;
-    const int64_t full = (tiles / grid) * grid, left = tiles - full;
-    if (left == 0 || full == 0) return tp;
-    // MX: a last wave under a quarter of the SMs measured slower split than
-    // whole (Llama qkv: 8 tiles left, 77 -> 80 us).
-    if (max_parts <= kMxMaxParts && left * 4 < grid) return tp;
-    // At least 8 K-blocks per part and at most max_parts parts: each extra part
-    // costs the warp that completes a tile another 16 KB read of fp32
-    // partials (8 parts of 4 K-blocks measured slower than no split).
-    int64_t parts = grid / left;
+    int64_t full, left, parts;
+    if (tiles < sm_count) {
+        full = 0;
+        left = tiles;
+        parts = sm_count / tiles;
+        if (parts > kSingleWaveMaxParts) parts = kSingleWaveMaxParts;
+    } else {
+        const int64_t grid = sm_count;
+        full = (tiles / grid) * grid;
+        left = tiles - full;
+        if (left == 0) return tp;
+        // MX: a last wave under a quarter of the SMs measured slower split than
+        // whole (Llama qkv: 8 tiles left, 77 -> 80 us).
+        if (max_parts <= kMxMaxParts && left * 4 < grid) return tp;
+        parts = grid / left;
+        if (parts > max_parts) parts = max_parts;
+    }
+    // At least 8 K-blocks per part: each extra part costs the warp that
+    // completes a tile another 16 KB read of fp32 partials (8 parts of 4
+    // K-blocks measured slower than no split).
     if (parts > (K / 128) / 8) parts = (K / 128) / 8;
-    if (parts > max_parts) parts = max_parts;
     if (parts < 2) return tp;
     const int epi_warps = bn == 128 ? 16 : 8;
     if (left * epi_warps > kMaxTickets) return tp;   // more tickets than the region holds: no split

@@ -555,7 +555,7 @@ def gemm(qa, sa, qb, sb, pow2: bool = False, path: str = "auto", out: torch.Tens
     N = qb.shape[0]
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
     flags = PATHS[path] | (FP8_GEMM_SCALES_POW2 if pow2 else 0)
-    # The size query follows the automatic plan: for M <= 256 the split-K
+    # The size query follows the automatic plan: for M <= 128 the split-K
     # skinny kernel, above it the large-M kernels' last-wave split (optional,
     # so a plan mismatch only costs that split).
     ws = workspace_for(M, N, K, 1, qa.device)

@@ -248,7 +248,7 @@ FP8BS_API fp8_status fp8_quant_weight_128x128_t(const void *w, int64_t N, int64_
  * with an exact evaluation to fp32 accumulation error plus bf16 output
  * rounding.
  *
- * Path choice with FP8_GEMM_PATH_AUTO: M <= 256 -> skinny; otherwise MX when
+ * Path choice with FP8_GEMM_PATH_AUTO: M <= 128 -> skinny; otherwise MX when
  * FP8_GEMM_SCALES_POW2 is set, else promote.  FP8_GEMM_PATH_MX without
  * FP8_GEMM_SCALES_POW2 returns FP8_ERR_SCALE_MODE.  On the MX path a scale that
  * is not a power of two in [2^-127, 2^127] breaks the promise: the output is
@@ -271,9 +271,10 @@ FP8BS_API fp8_status fp8_quant_weight_128x128_t(const void *w, int64_t N, int64_
  *       SM, so a tile may be computed in pieces whose fp32 partials are then
  *       added in CTA order); smaller or NULL returns FP8_ERR_WORKSPACE.
  *     - Promote and MX paths: optional.  With it, when the output tiles do
- *       not fill whole waves of the GPU's SMs, the tiles of the last wave are
- *       split along K and their fp32 parts added in a fixed order; without it
- *       (or if it is too small) every tile is computed whole.
+ *       not fill whole waves of the GPU's SMs, the tiles of the last wave (or,
+ *       with fewer tiles than SMs, every tile) are split along K and their
+ *       fp32 parts added in a fixed order; without it (or if it is too small)
+ *       every tile is computed whole.
  */
 FP8BS_API fp8_status fp8_blockscaled_gemm(const uint8_t *qa, int64_t lda, const float *sa, int64_t ldsa,
                                 const uint8_t *qb, int64_t ldb, const float *sb,
@@ -540,12 +541,13 @@ FP8BS_API fp8_status fp8_blockscaled_grouped_gemm(const uint8_t *qa, int64_t lda
  * - All calls share the array, and it keeps what the last call left in it.
  *   The call clears the ticket words on `stream` before its launch.  Calls
  *   that overlap on the GPU (unordered streams) race on the array: order them.
- * - The scratch needed is fp8_gemm_workspace_size(M, N, K, 1): 0 when every
- *   output tile is computed by one CTA, else 65536 bytes of tickets plus
+ * - The scratch needed is the skinny path's: 0 when every output tile is
+ *   computed by one CTA, else 65536 bytes of tickets plus
  *   (P + T - 1) * NT * 128 * 4 bytes of partials, where NT = M rounded up to
  *   16, 32, 64 or 128 (128 for M > 64), T = (N/128) * ceil(M / NT) output
  *   tiles (tokens beyond 128 run as further 128-token chunks), and P is the
- *   CTA count fp8_gemm_plan reports.  Sizes that need more than 8 MiB return
+ *   CTA count fp8_gemm_plan reports for FP8_GEMM_PATH_SKINNY (it is at most
+ *   fp8_gemm_workspace_size(M, N, K, 1)).  Sizes that need more than 8 MiB return
  *   FP8_ERR_WORKSPACE without launching.
  *   M > 256 returns FP8_ERR_SHAPE.
  * - flags: FP8_GEMM_PATH_AUTO or FP8_GEMM_PATH_SKINNY (plus FP8_GEMM_SCALES_POW2);
@@ -561,7 +563,8 @@ FP8BS_API fp8_status fp8_blockscaled_gemm_skinny_noalloc(const uint8_t *qa, int6
                                                          fp8_stream_t stream);
 
 /* Bytes of workspace fp8_blockscaled_gemm (G == 1) or
- * fp8_blockscaled_grouped_gemm (G > 1) needs for these sizes; 0 when none. */
+ * fp8_blockscaled_grouped_gemm (G > 1) needs for these sizes, whatever path
+ * the flags choose or force (the largest of the paths' needs); 0 when none. */
 FP8BS_API size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int32_t G);
 
 /* Static, human-readable name of a status code. */

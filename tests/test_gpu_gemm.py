@@ -94,6 +94,35 @@ def test_last_wave_split(ops, M, path):
     assert_gemm_close(bf16_to_np(c0), ref, f"{path} unsplit M={M}")
 
 
+@pytest.mark.parametrize("path,M,N,K", [("promote", 300, 1024, 4096), ("mx", 300, 1024, 4096),
+                                        ("promote", 64, 2048, 8192), ("mx", 200, 1536, 4096),
+                                        ("promote", 1, 768, 2048), ("mx", 8, 4096, 14336)])
+def test_single_wave_split(ops, path, M, N, K):
+    """Fewer output tiles than SMs: every tile is split along K, one part per
+    CTA (on 152 SMs: 12 tiles x 4 parts, 8 x 8, 12 x 4, 3 x 2 and 16 x 9,
+    the parts at least 8 K-blocks long).  Checked against the oracle,
+    bit-identical on a second call (parts added in part order), within
+    tolerance without a workspace (no split), and the tickets are left at
+    zero."""
+    pow2 = path == "mx"
+    qa, sa, qw, sw = _case(M, N, K, seed=M + 7 * N, pow2=pow2)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
+    flags = ops.PATHS[path] | (ops.FP8_GEMM_SCALES_POW2 if pow2 else 0)
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    outs = []
+    for w in (ws, ws, None):
+        c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ops.fp8_blockscaled_gemm(dqa, dsa, dqw, dsw, c, flags, w)
+        torch.cuda.synchronize()
+        assert ops.fp8_last_device_status() == 0
+        outs.append(c)
+    assert torch.equal(outs[0], outs[1])
+    assert_gemm_close(bf16_to_np(outs[0]), ref, f"{path} single-wave split {M}x{N}x{K}")
+    assert_gemm_close(bf16_to_np(outs[2]), ref, f"{path} unsplit {M}x{N}x{K}")
+    assert int(ws[:65536].view(torch.int32).abs().sum()) == 0
+
+
 def test_workspace_shared_across_shapes(ops):
     """One zero-initialised workspace reused, in sequence, by calls of several
     shapes and paths whose tickets and partials differ in size (split-K decode,

@@ -102,7 +102,7 @@ def test_qwen_prefill_whole_codes(ops, layer, pow2):
         assert_gemm_close_whole(y, par.gemm_ref(qa_o, sa_o, qw_o, sw_o), f"qwen o_proj pow2={pow2}")
 
 
-# ------------------------------------------------------------ decode, M <= 256
+# ------------------------------------------------------------ decode-sized, M <= 256
 _decode_w = {}
 
 
@@ -120,16 +120,19 @@ def _decode_weights(ops, K, N):
 
 
 @pytest.mark.parametrize("K,N", [(14336, 4096), (4096, 6144)])
-@pytest.mark.parametrize("M", [1, 8, 64, 256])
-def test_decode_whole_output(ops, M, K, N):
+@pytest.mark.parametrize("M,path", [(1, "auto"), (8, "auto"), (64, "auto"), (256, "auto"), (256, "skinny")])
+def test_decode_whole_output(ops, M, path, K, N):
+    # automatic path: the skinny kernel up to 128 rows, the promote kernel with
+    # every tile split along K at 256; the skinny kernel forced at 256 (two
+    # 128-token chunks per weight tile)
     qw, sw, qw_o, sw_o = _decode_weights(ops, K, N)
     a = I.decode_case(M, K, N).a
     qa, sa = ops.quant_act(a.cuda())
-    y = ops.gemm(qa, sa, qw, sw)
+    y = ops.gemm(qa, sa, qw, sw, path=path)
     _sync_ok(ops)
     qa_o, sa_o = O.quant_act_1x128(bf16_to_np(a))
     _same_act(qa, sa, qa_o, sa_o, f"decode M={M}")
-    assert_gemm_close_whole(y, O.gemm_ref(qa_o, sa_o, qw_o, sw_o), f"decode M={M} K={K} N={N}")
+    assert_gemm_close_whole(y, O.gemm_ref(qa_o, sa_o, qw_o, sw_o), f"decode M={M} K={K} N={N} path={path}")
 
 
 # ------------------------------------------------------------ Qwen3-30B-A3B experts

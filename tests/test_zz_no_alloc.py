@@ -39,6 +39,21 @@ def ops():
     return _ops
 
 
+def _skinny_scratch(ops, M, N, K):
+    """The skinny path's reduction scratch as the header states it: 0 when no
+    output tile is shared by two CTAs, else 64 KiB of tickets plus
+    (P + T - 1) * NT * 128 fp32 partials, with P the CTA count fp8_gemm_plan
+    reports for the skinny path on this GPU."""
+    path, P = ops.fp8_gemm_plan(M, N, K, ops.FP8_GEMM_PATH_SKINNY)
+    assert path == ops.FP8_GEMM_PATH_SKINNY
+    nt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+    KB = K // 128
+    T = (N // 128) * -(-M // nt)
+    U = T * KB
+    shared = any((c * U // P) % KB for c in range(1, P))
+    return 65536 + (P + T - 1) * nt * 128 * 4 if shared else 0
+
+
 def _operands(M, N, K, seed):
     """Oracle quantisation of seeded inputs, and the same codes and scales as
     device tensors in the library's layouts."""
@@ -62,8 +77,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(ops):
     # partials are used.
     cases = [(8, 6144, 4096, 1), (64, 4096, 14336, 2), (200, 256, 4096, 3), (8, 6144, 4096, 1)]
     for M, N, K, _ in cases:
-        need = ops.fp8_gemm_workspace_size(M, N, K, 1)
+        need = _skinny_scratch(ops, M, N, K)
         assert 0 < need <= SCRATCH_BYTES, (M, N, K, need)
+        assert need <= ops.fp8_gemm_workspace_size(M, N, K, 1)
     operands = {seed: _operands(M, N, K, seed) for M, N, K, seed in cases}
     outs = []
     for M, N, K, seed in cases:
@@ -83,11 +99,11 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(ops):
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch(ops):
-    # The first of these decode shapes whose reduction scratch, as the library
-    # reports it for this GPU, exceeds the fixed array: the call must refuse
-    # before launching.
+    # The first of these decode shapes whose reduction scratch, from the CTA
+    # count the library plans on this GPU, exceeds the fixed array: the call
+    # must refuse before launching.
     shapes = [(256, 4096, 14336), (256, 8192, 14336), (256, 16384, 16384), (256, 65536, 16384)]
-    big = [s for s in shapes if ops.fp8_gemm_workspace_size(*s, 1) > SCRATCH_BYTES]
+    big = [s for s in shapes if _skinny_scratch(ops, *s) > SCRATCH_BYTES]
     assert big, "no candidate shape needs more scratch than the array holds"
     M, N, K = big[0]
     qa = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
