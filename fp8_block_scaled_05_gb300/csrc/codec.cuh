@@ -135,7 +135,10 @@ __device__ __forceinline__ void mul2(float a, float b, float f, float &pa, float
 }
 
 // Codes of two elements: one packed multiply and one conversion per pair
-// (mode 2, a block whose reciprocal factor overflows, divides).
+// (mode 2, a block whose reciprocal factor overflows, divides).  The test of
+// the mode per pair is costly in a hot loop (in the GEMM's fused epilogue it
+// made the cast 3.5x slower): where the mode can be decided once, for a warp
+// (a vote) or a whole tile, callers take quant8_mul when it is 1.
 __device__ __forceinline__ uint32_t quant_pair(float xa, float xb, const BlockScale &bs) {
     if (bs.mode == 1) {
         float qa, qb;
@@ -157,7 +160,7 @@ __device__ __forceinline__ uint2 quant8(const uint4 &v, const BlockScale &bs) {
 // quant8 for a block in mode 1 (every power-of-two scale, and every fp32
 // scale whose factor r is finite): both elements of a pair in one packed
 // multiply, then one conversion.
-__device__ __forceinline__ uint2 quant8_pow2(const uint4 &v, float r) {
+__device__ __forceinline__ uint2 quant8_mul(const uint4 &v, float r) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t p[4];
 #pragma unroll

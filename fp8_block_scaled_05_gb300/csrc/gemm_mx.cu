@@ -531,6 +531,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int e = 0; e < 64; ++e) m2 = absmax_bf16x2(m2, p[e]);
                 const BlockScale bs = make_scale(absmax_pair_to_f32(m2), qo.pow2 != 0);
                 if (m < tl.row_end) qo.s[(size_t)(col0 / 128) * qo.lds + m] = bs.s;
+                // the product cast for the warp unless a row's factor overflows
+                // (a per-pair test of the mode made this cast several times slower)
+                const bool all_mul = __all_sync(0xFFFFFFFFu, bs.mode == 1);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     if (lane == 0) bulk_wait_group_read<0>();
@@ -538,8 +541,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int j0 = 32 * hf + 8 * k;
-                        const uint2 c0 = quant8(make_uint4(p[j0], p[j0 + 1], p[j0 + 2], p[j0 + 3]), bs);
-                        const uint2 c1 = quant8(make_uint4(p[j0 + 4], p[j0 + 5], p[j0 + 6], p[j0 + 7]), bs);
+                        const uint4 lo = make_uint4(p[j0], p[j0 + 1], p[j0 + 2], p[j0 + 3]);
+                        const uint4 hi = make_uint4(p[j0 + 4], p[j0 + 5], p[j0 + 6], p[j0 + 7]);
+                        const uint2 c0 = all_mul ? quant8_mul(lo, bs.r) : quant8(lo, bs);
+                        const uint2 c1 = all_mul ? quant8_mul(hi, bs.r) : quant8(hi, bs);
                         *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
                             make_uint4(c0.x, c0.y, c1.x, c1.y);
                     }

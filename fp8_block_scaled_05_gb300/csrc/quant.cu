@@ -83,6 +83,8 @@ __device__ __forceinline__ void act_tile_1x128(const uint16_t* __restrict__ x, i
     }
     // this lane's block: item (l16 mod kActItems) of half `half`
     const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
+    // every block of the warp is some lane's own: one vote picks the cast
+    const bool all_mul = POW2 || __all_sync(0xFFFFFFFFu, own.mode == 1);
     if (l16 < kActItems) {
         const int r = l16 / kActPairs, p = l16 % kActPairs;
         const int rl = warp * kActRowsPerWarp + r;
@@ -97,7 +99,7 @@ __device__ __forceinline__ void act_tile_1x128(const uint16_t* __restrict__ x, i
         const int64_t m = m0 + warp * kActRowsPerWarp + r;
         const int64_t kb = kb0 + 2 * p + half;
         if (m < M && kb < KB) {
-            const uint2 c = POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false));
+            const uint2 c = all_mul ? quant8_mul(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false));
             __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8), c);
         }
     }
@@ -168,9 +170,15 @@ __device__ __forceinline__ void weight_tile_128x128(const uint16_t* __restrict__
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_red[i]);
     const BlockScale bs = make_scale(amax, pow2);
+    if (bs.mode == 1) {   // one scale for the tile: a uniform choice of cast
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        __stcs(reinterpret_cast<uint2*>(q + (row0 + 2 * i) * ldq + col), quant8(v[i], bs));
+        for (int i = 0; i < 8; ++i)
+            __stcs(reinterpret_cast<uint2*>(q + (row0 + 2 * i) * ldq + col), quant8_mul(v[i], bs.r));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            __stcs(reinterpret_cast<uint2*>(q + (row0 + 2 * i) * ldq + col), quant8(v[i], bs));
+    }
     if (threadIdx.x == 0) {
         if (s8 != nullptr)
             s8[nb * KB + kb] = (uint8_t)(__float_as_uint(bs.s) >> 23);   // UE8M0 byte of a power of two

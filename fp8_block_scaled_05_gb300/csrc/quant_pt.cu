@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_quant_tensor(const uint16_t* 
     const float amax = __ldcg(scale_amax + 1);
     const BlockScale bs = make_scale(amax, POW2);
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_amax[0] = bs.s;
-    auto cast = [&](const uint4& v) { return POW2 ? quant8_pow2(v, bs.r) : quant8(v, bs); };
+    // one scale for the tensor: the warp-uniform choice of cast made once
+    const bool all_mul = POW2 || __all_sync(0xFFFFFFFFu, bs.mode == 1);
+    auto cast = [&](const uint4& v) { return all_mul ? quant8_mul(v, bs.r) : quant8(v, bs); };
     if (w.flat) {
         const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
         for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __
                                                              const float* __restrict__ scale) {
     const float sc = __ldg(scale);
     const BlockScale bs = scale_from_sr(sc, __frcp_rn(sc), false);
+    const bool all_mul = __all_sync(0xFFFFFFFFu, bs.mode == 1);   // one scale for the tensor
     if (w.flat) {
         const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
         for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __
 #pragma unroll
             for (int u = 0; u < kPtUnroll; ++u) {
                 const int64_t c = c0 + u * step;
-                if (c < total) __stcs(reinterpret_cast<uint2*>(q + c * 8), quant8(v[u], bs));
+                if (c < total)
+                    __stcs(reinterpret_cast<uint2*>(q + c * 8), all_mul ? quant8_mul(v[u], bs.r) : quant8(v[u], bs));
             }
         }
     } else {
@@ -161,7 +165,9 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __
 #pragma unroll
                 for (int u = 0; u < kPtUnroll; ++u) {
                     const int64_t c = c0 + (int64_t)u * kPtThreads;
-                    if (c < w.cpr) __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8), quant8(v[u], bs));
+                    if (c < w.cpr)
+                        __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8),
+                               all_mul ? quant8_mul(v[u], bs.r) : quant8(v[u], bs));
                 }
             }
         }

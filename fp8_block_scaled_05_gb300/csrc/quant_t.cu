@@ -50,6 +50,14 @@ __device__ __forceinline__ float elem(const uint4 (&v)[8], int i, int j) {
 template <bool POW2, typename ScaleOf>
 __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
                                                   ScaleOf scale_of) {
+    // the product cast for the whole warp unless one of its columns divides
+    bool all_mul = POW2;
+    if constexpr (!POW2) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine = mine && scale_of(j).mode == 1;
+        all_mul = __all_sync(0xFFFFFFFFu, mine);
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const BlockScale bs = scale_of(j);
@@ -57,7 +65,7 @@ __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, i
 #pragma unroll
         for (int p = 0; p < 4; ++p) {   // rows 2p (low byte) and 2p + 1
             uint32_t pair;
-            if constexpr (POW2) {
+            if (all_mul) {
                 float qa, qb;
                 mul2(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs.r, qa, qb);
                 pair = e4m3x2(qa, qb);
@@ -212,6 +220,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
         }
         const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
         if (cg < 8 && m0 + 8 * rg + cg < M) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
+        const bool all_mul = POW2 || __all_sync(0xFFFFFFFFu, own.mode == 1);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int src = (lane & 16) | i;
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
             const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
             if (m0 + 8 * rg + i < M)
                 __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
-                       POW2 ? quant8_pow2(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
+                       all_mul ? quant8_mul(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
         }
     }
     __syncthreads();
@@ -277,8 +286,13 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128_t(const uint16_t *__res
     // One scale for the whole tile: W's codes and W^T's are the same bytes,
     // computed once and transposed in registers.
     uint2 rc[8];
+    if (bs.mode == 1) {   // one scale for the tile: a uniform choice of cast
 #pragma unroll
-    for (int i = 0; i < 8; ++i) rc[i] = quant8(v[i], bs);
+        for (int i = 0; i < 8; ++i) rc[i] = quant8_mul(v[i], bs.r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rc[i] = quant8(v[i], bs);
+    }
     if (q != nullptr) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) __stcs(reinterpret_cast<uint2 *>(q + (n0 + 8 * rg + i) * ldq + k0 + 8 * cg), rc[i]);
