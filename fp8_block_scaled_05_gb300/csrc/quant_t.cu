@@ -44,20 +44,11 @@ __device__ __forceinline__ float elem(const uint4 (&v)[8], int i, int j) {
     return (j & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
 }
 
-// Codes of the thread's 8 columns (8 rows each) into the shared tile;
-// scale_of(j) gives column j's BlockScale (POW2: power-of-two scales, an
-// exact multiply).
-template <bool POW2, typename ScaleOf>
-__device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
-                                                  ScaleOf scale_of) {
-    // the product cast for the whole warp unless one of its columns divides
-    bool all_mul = POW2;
-    if constexpr (!POW2) {
-        bool mine = true;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mine = mine && scale_of(j).mode == 1;
-        all_mul = __all_sync(0xFFFFFFFFu, mine);
-    }
+// The column codes with one cast throughout: MUL, the product by each
+// column's factor r; otherwise the per-pair choice of quant_pair.
+template <bool MUL, typename ScaleOf>
+__device__ __forceinline__ void col_codes_to_smem_as(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
+                                                     ScaleOf scale_of) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const BlockScale bs = scale_of(j);
@@ -65,7 +56,7 @@ __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, i
 #pragma unroll
         for (int p = 0; p < 4; ++p) {   // rows 2p (low byte) and 2p + 1
             uint32_t pair;
-            if (all_mul) {
+            if constexpr (MUL) {
                 float qa, qb;
                 mul2(elem(v, 2 * p, j), elem(v, 2 * p + 1, j), bs.r, qa, qb);
                 pair = e4m3x2(qa, qb);
@@ -78,6 +69,26 @@ __device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, i
         *reinterpret_cast<uint2 *>(tcodes + R * kTT + ((((rg >> 1) ^ (cg & 7))) << 4) + ((rg & 1) << 3)) =
             make_uint2(part[0], part[1]);
     }
+}
+
+// Codes of the thread's 8 columns (8 rows each) into the shared tile;
+// scale_of(j) gives column j's BlockScale.  The product cast for the whole
+// warp unless one of its columns divides (POW2: power-of-two scales, always
+// an exact multiply); the choice is made once, outside the loops.
+template <bool POW2, typename ScaleOf>
+__device__ __forceinline__ void col_codes_to_smem(const uint4 (&v)[8], int rg, int cg, uint8_t *tcodes,
+                                                  ScaleOf scale_of) {
+    bool all_mul = POW2;
+    if constexpr (!POW2) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine = mine && scale_of(j).mode == 1;
+        all_mul = __all_sync(0xFFFFFFFFu, mine);
+    }
+    if (all_mul)
+        col_codes_to_smem_as<true>(v, rg, cg, tcodes, scale_of);
+    else
+        col_codes_to_smem_as<false>(v, rg, cg, tcodes, scale_of);
 }
 
 // 4 x 4 byte transpose: words a, b, c, d are rows (byte 0 = column 0); word
