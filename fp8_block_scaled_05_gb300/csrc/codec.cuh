@@ -172,6 +172,32 @@ __device__ __forceinline__ uint2 quant8_mul(const uint4 &v, float r) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
+// The cast of eight values with the choice fixed at compile time: MUL, the
+// product path (mode 1); otherwise the per-pair test.  with_cast(all_mul, f)
+// calls f with CastTag<true> or CastTag<false> once, so that a caller branches
+// on its warp-uniform choice outside its loops (a test inside them, even a
+// uniform one, cost 10-17% in the quantisers).
+template <bool MUL>
+struct CastTag {
+    static constexpr bool mul = MUL;
+};
+
+template <bool MUL>
+__device__ __forceinline__ uint2 quant8_as(const uint4 &v, const BlockScale &bs) {
+    if constexpr (MUL)
+        return quant8_mul(v, bs.r);
+    else
+        return quant8(v, bs);
+}
+
+template <typename F>
+__device__ __forceinline__ void with_cast(bool all_mul, F &&f) {
+    if (all_mul)
+        f(CastTag<true>{});
+    else
+        f(CastTag<false>{});
+}
+
 __device__ __forceinline__ uint32_t absmax8(uint32_t acc, const uint4 &v) {
     acc = absmax_bf16x2(acc, v.x);
     acc = absmax_bf16x2(acc, v.y);

@@ -605,16 +605,18 @@ __global__ void __launch_bounds__(Cfg<BN, ROWB>::THREADS, 1)
                     for (int hf = 0; hf < 2; ++hf) {
                         if (lane == 0) bulk_wait_group_read<0>();
                         __syncwarp();
+                        with_cast(all_mul, [&](auto cast) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int j0 = 32 * hf + 8 * k;   // first packed pair of this 16-byte piece
-                            const uint4 lo = make_uint4(pk[j0], pk[j0 + 1], pk[j0 + 2], pk[j0 + 3]);
-                            const uint4 hi = make_uint4(pk[j0 + 4], pk[j0 + 5], pk[j0 + 6], pk[j0 + 7]);
-                            const uint2 c0 = all_mul ? quant8_mul(lo, bs.r) : quant8(lo, bs);
-                            const uint2 c1 = all_mul ? quant8_mul(hi, bs.r) : quant8(hi, bs);
-                            *reinterpret_cast<uint4*>(qbuf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
-                                make_uint4(c0.x, c0.y, c1.x, c1.y);
-                        }
+                            for (int k = 0; k < 4; ++k) {
+                                const int j0 = 32 * hf + 8 * k;   // first packed pair of this 16-byte piece
+                                const uint2 c0 = quant8_as<decltype(cast)::mul>(
+                                    make_uint4(pk[j0], pk[j0 + 1], pk[j0 + 2], pk[j0 + 3]), bs);
+                                const uint2 c1 = quant8_as<decltype(cast)::mul>(
+                                    make_uint4(pk[j0 + 4], pk[j0 + 5], pk[j0 + 6], pk[j0 + 7]), bs);
+                                *reinterpret_cast<uint4*>(qbuf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                                    make_uint4(c0.x, c0.y, c1.x, c1.y);
+                            }
+                        });
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {

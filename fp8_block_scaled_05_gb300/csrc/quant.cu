@@ -90,19 +90,20 @@ __device__ __forceinline__ void act_tile_1x128(const uint16_t* __restrict__ x, i
         const int rl = warp * kActRowsPerWarp + r;
         if (m0 + rl < M && kb0 + 2 * p + half < KB) s_tile[2 * p + half][rl] = own.s;
     }
+    with_cast(all_mul, [&](auto cast) {
 #pragma unroll
-    for (int i = 0; i < kActItems; ++i) {
-        const int r = i / kActPairs, p = i % kActPairs;
-        const int src = (lane & 16) | i;
-        const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
-        const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
-        const int64_t m = m0 + warp * kActRowsPerWarp + r;
-        const int64_t kb = kb0 + 2 * p + half;
-        if (m < M && kb < KB) {
-            const uint2 c = all_mul ? quant8_mul(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false));
-            __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8), c);
+        for (int i = 0; i < kActItems; ++i) {
+            const int r = i / kActPairs, p = i % kActPairs;
+            const int src = (lane & 16) | i;
+            const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
+            const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
+            const int64_t m = m0 + warp * kActRowsPerWarp + r;
+            const int64_t kb = kb0 + 2 * p + half;
+            if (m < M && kb < KB)
+                __stcs(reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + l16 * 8),
+                       quant8_as<decltype(cast)::mul>(v[i], scale_from_sr(si, ri, false)));
         }
-    }
+    });
     __syncthreads();
     if (threadIdx.x < kActKB * kActRows) {
         const int kbl = threadIdx.x / kActRows, rl = threadIdx.x % kActRows;

@@ -232,15 +232,17 @@ __global__ void __launch_bounds__(256, ROWWISE ? 3 : 4) k_quant_act_128x1(const 
         const BlockScale own = make_scale(absmax_pair_to_f32(a[0]), POW2);
         if (cg < 8 && m0 + 8 * rg + cg < M) s[(size_t)blockIdx.x * lds + m0 + 8 * rg + cg] = own.s;
         const bool all_mul = POW2 || __all_sync(0xFFFFFFFFu, own.mode == 1);
+        with_cast(all_mul, [&](auto cast) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int src = (lane & 16) | i;
-            const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
-            const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
-            if (m0 + 8 * rg + i < M)
-                __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
-                       all_mul ? quant8_mul(v[i], ri) : quant8(v[i], scale_from_sr(si, ri, false)));
-        }
+            for (int i = 0; i < 8; ++i) {
+                const int src = (lane & 16) | i;
+                const float si = __shfl_sync(0xFFFFFFFFu, own.s, src);
+                const float ri = __shfl_sync(0xFFFFFFFFu, own.r, src);
+                if (m0 + 8 * rg + i < M)
+                    __stcs(reinterpret_cast<uint2 *>(q + (m0 + 8 * rg + i) * ldq + k0 + 8 * cg),
+                           quant8_as<decltype(cast)::mul>(v[i], scale_from_sr(si, ri, false)));
+            }
+        });
     }
     __syncthreads();
     if (threadIdx.x < kTT) {
