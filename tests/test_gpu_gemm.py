@@ -204,6 +204,41 @@ def test_gemm_quant_fused_exact_output(ops, path, out_pow2):
     assert np.array_equal(sc[:, :M].cpu().numpy(), s_o.T)
 
 
+@pytest.mark.parametrize("path", ["promote", "mx"])
+def test_gemm_quant_fused_rows_whose_factor_overflows(ops, path):
+    """The fused cast's rare path: rows whose bf16 outputs are so small that
+    448/amax overflows fp32 are cast by division (x / s), and a warp holding
+    one takes the per-pair choice for all its rows.  Exact operands as above;
+    rows 0-31 (a whole lane quarter) and every 37th row get sA = 2^-124 with
+    sB = 2^-2, so C there is an integer times 2^-126 (normal, exact in bf16)
+    and amax stays below 448 / FLT_MAX; the other rows keep ordinary scales.
+    Codes and scales must equal the oracle's quantiser on the oracle's C."""
+    rng = np.random.Generator(np.random.PCG64(35))
+    M, N, K = 300, 512, 256
+    lut = np.array([0x00, 0x38, 0xB8], np.uint8)
+    qa = lut[rng.integers(0, 3, (M, K))]
+    qw = lut[rng.integers(0, 3, (N, K))]
+    ea = rng.integers(-3, 3, (M, 1)).astype(np.float64)
+    tiny = np.zeros(M, bool)
+    tiny[:32] = True
+    tiny[::37] = True
+    ea[tiny] = -124
+    sa = np.repeat(2.0 ** ea, K // 128, axis=1).astype(np.float32)
+    sw = np.full((N // 128, K // 128), 0.25, np.float32)
+    ref = O.gemm_ref(qa, sa, qw, sw)
+    amax_tiny = np.abs(ref[tiny]).max()
+    assert 0 < amax_tiny < 448.0 / np.finfo(np.float32).max   # the division path is reached
+    dqa, dsa, dqw, dsw = _to_dev(qa, sa, qw, sw)
+    flags = (ops.FP8_GEMM_PATH_MX if path == "mx" else ops.FP8_GEMM_PATH_PROMOTE) | ops.FP8_GEMM_SCALES_POW2
+    c, qc, sc = _gemm_quant_path(ops, dqa, dsa, dqw, dsw, flags, False)
+    torch.cuda.synchronize()
+    assert ops.fp8_last_device_status() == 0
+    assert np.array_equal(bf16_to_np(c), ref)
+    q_o, s_o = O.quant_act_1x128(ref.astype(np.float32), False)
+    assert np.array_equal(qc.cpu().numpy(), q_o)
+    assert np.array_equal(sc[:, :M].cpu().numpy(), s_o.T)
+
+
 def _gemm_quant_path(ops, qa, sa, qw, sw, flags, out_pow2):
     M, N = qa.shape[0], qw.shape[0]
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
