@@ -115,17 +115,14 @@ struct __align__(16) Ctrl {
 };
 
 // ROWB (a scale per B row): a ring of SRING x BN column scales follows the
-// group table.  WHOLE: the whole-output staging (Cfg's WHOLE_OUT).
-template <int BN, bool ROWB = false, bool WHOLE = ROWB>
+// group table.
+template <int BN, bool ROWB = false>
 constexpr size_t smem_bytes() {
-    using C = Cfg<BN, WHOLE>;
+    using C = Cfg<BN, ROWB>;
     return 1024 /*align slack*/ + (size_t)C::RING_BYTES + (size_t)C::EPI_WARPS * C::EPI_BUF_BYTES +
            sizeof(Ctrl) + (size_t)(MAX_GROUPS + 4) * sizeof(int32_t) + (ROWB ? (size_t)SRING * BN * sizeof(float) : 0);
 }
-static_assert(smem_bytes<256, true>() <= 232448 && smem_bytes<128, true>() <= 232448 &&
-                  smem_bytes<256, false, true>() <= 232448,
-              "shared memory per CTA");
-constexpr int64_t kGroupedWholeMaxK = 2048;   // grouped forward: whole-output staging up to this K
+static_assert(smem_bytes<256, true>() <= 232448 && smem_bytes<128, true>() <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record_timeout(int* status) {
     if (status) atomicCAS(status, 0, kStatusTimeout);
@@ -140,15 +137,15 @@ __device__ __forceinline__ void record_timeout(int* status) {
 // kg_tokens tokens), the layout the grouped 128x1 quantiser writes.  Tiles
 // run expert by expert; C_g is rows g M .. g M + M - 1 of the output (M %
 // 128 == 0); an expert without tokens gets zeros.
-template <int BN, bool GROUPED, bool ROWB, bool KGROUP = false, bool WHOLE = ROWB>
-__global__ void __launch_bounds__(Cfg<BN, WHOLE>::THREADS, 1)
+template <int BN, bool GROUPED, bool ROWB, bool KGROUP = false>
+__global__ void __launch_bounds__(Cfg<BN, ROWB>::THREADS, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ sa, int64_t ldsa, const float* __restrict__ sb, int64_t ldsb,
                    uint16_t* __restrict__ c, int64_t ldc, int M, int N, int K,
                    const int32_t* __restrict__ offsets, int G, int* status, SplitTail split, QuantOut qo,
                    uint64_t wait_ns, int skip_first_load, int kg_tokens) {
-    using C = Cfg<BN, WHOLE>;
+    using C = Cfg<BN, ROWB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_buf = smem + (size_t)C::RING_BYTES;   // 1024-byte aligned
@@ -716,11 +713,11 @@ __global__ void __launch_bounds__(Cfg<BN, WHOLE>::THREADS, 1)
     }
 }
 
-template <int BN, bool GROUPED, bool ROWB = false, bool KGROUP = false, bool WHOLE = ROWB>
+template <int BN, bool GROUPED, bool ROWB = false, bool KGROUP = false>
 cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
-    using C = Cfg<BN, WHOLE>;
+    using C = Cfg<BN, ROWB>;
     static DeviceOnce attr_done;     // kernel attributes set on this device
-    auto kern = k_gemm_promote<BN, GROUPED, ROWB, KGROUP, WHOLE>;
+    auto kern = k_gemm_promote<BN, GROUPED, ROWB, KGROUP>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done.test(dev)) {
@@ -730,8 +727,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
         // The setmaxnreg split is only safe if the CTA really starts with
         // LAUNCH_REGS registers per thread; refuse to launch otherwise.
         if (C::SPLIT_REGS && fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes<BN, ROWB, WHOLE>());
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<BN, ROWB>());
         if (e != cudaSuccess) return e;
         attr_done.set(dev);
     }
@@ -750,7 +746,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t st) {
     }
     const int64_t items = work_items((int)tiles, split);
     const int grid = (int)(items < a.sm_count ? items : a.sm_count);
-    kern<<<grid, C::THREADS, smem_bytes<BN, ROWB, WHOLE>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
+    kern<<<grid, C::THREADS, smem_bytes<BN, ROWB>(), st>>>(a.tm_a, a.tm_b, a.tm_c, a.tm_q, a.sa, a.ldsa, a.sb,
                                                            a.ldsb, static_cast<uint16_t*>(a.c), a.ldc, (int)a.M, (int)a.N,
                                                      (int)a.K, a.offsets, a.G, a.status, split, a.qout,
                                                      wait_bound(a), a.skip_first_load, (int)a.kg_tokens);
@@ -825,14 +821,7 @@ cudaError_t launch_gemm_promote(const GemmArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     }
     if (a.bn == 128) return grouped ? promote::launch<128, true>(a, st) : promote::launch<128, false>(a, st);
-    if (a.bn == 256) {
-        if (!grouped) return promote::launch<256, false>(a, st);
-        // short experts' K: the whole-output staging (3-stage ring) pays for
-        // its missing stage (Qwen3-30B-A3B experts, K 2048 and 768: 1.5-4%
-        // faster; K 4096: 3% slower)
-        if (a.K <= promote::kGroupedWholeMaxK) return promote::launch<256, true, false, false, true>(a, st);
-        return promote::launch<256, true>(a, st);
-    }
+    if (a.bn == 256) return grouped ? promote::launch<256, true>(a, st) : promote::launch<256, false>(a, st);
     return cudaErrorInvalidValue;
 }
 
