@@ -369,6 +369,50 @@ def test_workspace_size_and_plan(L):
     path, splits = ops.fp8_gemm_plan(8, 4096, 14336)
     assert path == ops.FP8_GEMM_PATH_SKINNY and splits > 1
     assert ops.fp8_gemm_plan(4096, 4096, 4096)[0] == ops.FP8_GEMM_PATH_PROMOTE
+    # the automatic path: the skinny kernel up to 128 rows, the large-M kernels above
+    assert ops.fp8_gemm_plan(128, 4096, 14336)[0] == ops.FP8_GEMM_PATH_SKINNY
+    assert ops.fp8_gemm_plan(129, 4096, 14336)[0] == ops.FP8_GEMM_PATH_PROMOTE
+    assert ops.fp8_gemm_plan(256, 4096, 14336, ops.FP8_GEMM_SCALES_POW2)[0] == ops.FP8_GEMM_PATH_MX
+
+
+def _skinny_bytes(ops, M, N, K):
+    """The skinny path's scratch by the header's formula, with the CTA count P
+    the library plans for the forced skinny path."""
+    _, P = ops.fp8_gemm_plan(M, N, K, ops.FP8_GEMM_PATH_SKINNY)
+    nt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+    KB, T = K // 128, (N // 128) * -(-M // nt)
+    U = T * KB
+    return 65536 + (P + T - 1) * nt * 128 * 4 if any((c * U // P) % KB for c in range(1, P)) else 0
+
+
+def _large_m_bytes(M, N, K, sms=152):
+    """The large-M kernels' K split (256-wide tiles): every tile split when the
+    tiles do not fill the SMs, else the last wave's tiles."""
+    tiles = -(-M // 128) * (N // 256)
+    KB = K // 128
+    if tiles < sms:
+        left, parts = tiles, min(sms // tiles, 16)
+    else:
+        left = tiles % sms
+        if left == 0:
+            return 0
+        parts = min(sms // left, 4)
+    parts = min(parts, KB // 8)
+    return 65536 + left * parts * 128 * 256 * 4 if parts >= 2 else 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 6144, 4096), (64, 4096, 14336), (128, 4096, 14336), (200, 4096, 14336),
+                                   (256, 6144, 4096), (512, 4096, 4096), (4096, 6144, 4096)])
+def test_workspace_size_covers_every_path(L, M, N, K):
+    """fp8_gemm_workspace_size is the largest need of the paths these sizes
+    may take, automatic or forced (no device here: 152 SMs assumed): at least
+    the skinny kernel's scratch up to 256 rows and the large-M kernels' K
+    split, and equal to the larger of the two."""
+    from fp8_block_scaled_05_gb300 import ops
+    need = ops.fp8_gemm_workspace_size(M, N, K)
+    sk = _skinny_bytes(ops, M, N, K) if M <= 256 else 0
+    lm = _large_m_bytes(M, N, K)
+    assert need == max(sk, lm), (need, sk, lm)
 
 
 def _has_gpu():
