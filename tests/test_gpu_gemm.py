@@ -94,6 +94,23 @@ def test_last_wave_split(ops, M, path):
     assert_gemm_close(bf16_to_np(c0), ref, f"{path} unsplit M={M}")
 
 
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("M", [127, 128, 129, 130])
+def test_auto_path_at_the_row_threshold(ops, M, pow2):
+    """The automatic path takes the skinny kernel up to 128 rows and the
+    large-M kernels (every tile split along K here: 2 x 8 tiles on 152 SMs)
+    from 129: on both sides of the threshold the plan names the expected
+    kernel and the whole output is within tolerance of the oracle."""
+    N, K = 1024, 4096
+    flags = ops.FP8_GEMM_SCALES_POW2 if pow2 else 0
+    path, _ = ops.fp8_gemm_plan(M, N, K, flags)
+    want = ops.FP8_GEMM_PATH_SKINNY if M <= 128 else (ops.FP8_GEMM_PATH_MX if pow2 else ops.FP8_GEMM_PATH_PROMOTE)
+    assert path == want
+    qa, sa, qw, sw = _case(M, N, K, seed=3 * M + pow2, pow2=pow2)
+    c = _run(ops, qa, sa, qw, sw, "auto", pow2)
+    assert_gemm_close(c, O.gemm_ref(qa, sa, qw, sw), f"auto path M={M} pow2={pow2}")
+
+
 @pytest.mark.parametrize("path,M,N,K", [("promote", 300, 1024, 4096), ("mx", 300, 1024, 4096),
                                         ("promote", 64, 2048, 8192), ("mx", 200, 1536, 4096),
                                         ("promote", 1, 768, 2048), ("mx", 8, 4096, 14336)])
