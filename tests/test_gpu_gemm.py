@@ -168,7 +168,7 @@ def test_workspace_shared_across_shapes(ops):
 
 
 @pytest.mark.parametrize("M,N,K", [(200, 384, 512), (300, 1024, 1152), (129, 256, 128), (1, 512, 256),
-                                   (1280, 4096, 2048), (1536, 4096, 2048)])
+                                   (1280, 4096, 2048), (1536, 4096, 2048), (200, 1024, 4096)])
 @pytest.mark.parametrize("pow2,out_pow2", [(False, False), (True, True), (False, True), (True, False)])
 def test_gemm_quant_fused(ops, M, N, K, pow2, out_pow2):
     """GEMM with the next layer's 1x128 quantisation fused into the epilogue:
@@ -178,7 +178,8 @@ def test_gemm_quant_fused(ops, M, N, K, pow2, out_pow2):
     same.  Covers a half-empty last tile (N = 384), ragged M, K = 128, M = 1
     and the last-wave K split (M = 1280 and 1536, N = 4096: the promote
     kernel splits the 8 and 40 left-over tiles, the MX kernel the 40, the
-    codes coming from the summed parts).  Power-of-two input scales take the
+    codes coming from the summed parts), and fewer tiles than SMs (M = 200,
+    N = 1024, K = 4096: every tile split along K).  Power-of-two input scales take the
     MX kernel, the others the promote kernel."""
     qa, sa, qw, sw = _case(M, N, K, seed=M + K, pow2=pow2)
     ref = O.gemm_ref(qa, sa, qw, sw)
