@@ -178,8 +178,8 @@ struct TailPlan {
     size_t bytes;         // workspace needed for the split (0 when none)
 };
 constexpr int kPromoteMaxParts = 4, kMxMaxParts = 2;
-constexpr int kSingleWaveMaxParts = 16;
-constexpr int64_t kSkinnyAutoMaxM = 128;   // FP8_GEMM_PATH_AUTO: the skinny kernel up to this many rows   // fewer tiles than SMs: parts per tile at most
+constexpr int kSingleWaveMaxParts = 16;    // fewer tiles than SMs: parts per tile at most
+constexpr int64_t kSkinnyAutoMaxM = 128;   // FP8_GEMM_PATH_AUTO: the skinny kernel up to this many rows
 constexpr int kMxTileN = 256;   // MX kernel output tile width
 TailPlan tail_plan(int64_t M, int64_t N, int64_t K, int sm_count, int bn, int max_parts);
 size_t promote_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);

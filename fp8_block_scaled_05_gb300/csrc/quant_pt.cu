@@ -79,6 +79,47 @@ __global__ void __launch_bounds__(kPtThreads) k_amax_bf16(const uint16_t* __rest
     cta_amax_commit(m2, amax_bits);
 }
 
+// The cast walk shared by both kernels: every 16-byte chunk of x through
+// one cast (MUL: the product by bs.r; otherwise the per-pair test), chosen
+// once by the caller.
+template <bool MUL>
+__device__ __forceinline__ void cast_walk(const uint16_t* __restrict__ x, const ChunkWalk& w, uint8_t* __restrict__ q,
+                                          int64_t ldq, const BlockScale& bs) {
+    if (w.flat) {
+        const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
+        for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
+            uint4 v[kPtUnroll];
+#pragma unroll
+            for (int u = 0; u < kPtUnroll; ++u) {
+                const int64_t c = c0 + u * step;
+                v[u] = c < total ? __ldcs(reinterpret_cast<const uint4*>(x + c * 8)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kPtUnroll; ++u) {
+                const int64_t c = c0 + u * step;
+                if (c < total) __stcs(reinterpret_cast<uint2*>(q + c * 8), quant8_as<MUL>(v[u], bs));
+            }
+        }
+    } else {
+        for (int64_t r = blockIdx.x; r < w.M; r += gridDim.x) {
+            for (int64_t c0 = threadIdx.x; c0 < w.cpr; c0 += kPtThreads * kPtUnroll) {
+                uint4 v[kPtUnroll];
+#pragma unroll
+                for (int u = 0; u < kPtUnroll; ++u) {
+                    const int64_t c = c0 + (int64_t)u * kPtThreads;
+                    v[u] = c < w.cpr ? __ldcs(reinterpret_cast<const uint4*>(x + chunk_offset(w, r, c)))
+                                     : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kPtUnroll; ++u) {
+                    const int64_t c = c0 + (int64_t)u * kPtThreads;
+                    if (c < w.cpr) __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8), quant8_as<MUL>(v[u], bs));
+                }
+            }
+        }
+    }
+}
+
 // scale_amax[1] holds the amax (as written by k_amax_bf16); CTA 0 writes the
 // scale to scale_amax[0].  POW2: power-of-two scale, exact multiply.  The
 // flat walk needs ldq == ldx == K.
@@ -91,40 +132,7 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_quant_tensor(const uint16_t* 
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_amax[0] = bs.s;
     // one scale for the tensor: the warp-uniform choice of cast made once
     const bool all_mul = POW2 || __all_sync(0xFFFFFFFFu, bs.mode == 1);
-    auto cast = [&](const uint4& v) { return all_mul ? quant8_mul(v, bs.r) : quant8(v, bs); };
-    if (w.flat) {
-        const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
-        for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
-            uint4 v[kPtUnroll];
-#pragma unroll
-            for (int u = 0; u < kPtUnroll; ++u) {
-                const int64_t c = c0 + u * step;
-                v[u] = c < total ? __ldcs(reinterpret_cast<const uint4*>(x + c * 8)) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < kPtUnroll; ++u) {
-                const int64_t c = c0 + u * step;
-                if (c < total) __stcs(reinterpret_cast<uint2*>(q + c * 8), cast(v[u]));
-            }
-        }
-    } else {
-        for (int64_t r = blockIdx.x; r < w.M; r += gridDim.x) {
-            for (int64_t c0 = threadIdx.x; c0 < w.cpr; c0 += kPtThreads * kPtUnroll) {
-                uint4 v[kPtUnroll];
-#pragma unroll
-                for (int u = 0; u < kPtUnroll; ++u) {
-                    const int64_t c = c0 + (int64_t)u * kPtThreads;
-                    v[u] = c < w.cpr ? __ldcs(reinterpret_cast<const uint4*>(x + chunk_offset(w, r, c)))
-                                     : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < kPtUnroll; ++u) {
-                    const int64_t c = c0 + (int64_t)u * kPtThreads;
-                    if (c < w.cpr) __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8), cast(v[u]));
-                }
-            }
-        }
-    }
+    with_cast(all_mul, [&](auto cast) { cast_walk<decltype(cast)::mul>(x, w, q, ldq, bs); });
 }
 
 // Cast under a given scale (scale[0], a positive normal fp32 in device
@@ -136,42 +144,7 @@ __global__ void __launch_bounds__(kPtThreads, 4) k_cast_scale(const uint16_t* __
     const float sc = __ldg(scale);
     const BlockScale bs = scale_from_sr(sc, __frcp_rn(sc), false);
     const bool all_mul = __all_sync(0xFFFFFFFFu, bs.mode == 1);   // one scale for the tensor
-    if (w.flat) {
-        const int64_t total = w.M * w.cpr, step = (int64_t)gridDim.x * kPtThreads;
-        for (int64_t c0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x; c0 < total; c0 += step * kPtUnroll) {
-            uint4 v[kPtUnroll];
-#pragma unroll
-            for (int u = 0; u < kPtUnroll; ++u) {
-                const int64_t c = c0 + u * step;
-                v[u] = c < total ? __ldcs(reinterpret_cast<const uint4*>(x + c * 8)) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < kPtUnroll; ++u) {
-                const int64_t c = c0 + u * step;
-                if (c < total)
-                    __stcs(reinterpret_cast<uint2*>(q + c * 8), all_mul ? quant8_mul(v[u], bs.r) : quant8(v[u], bs));
-            }
-        }
-    } else {
-        for (int64_t r = blockIdx.x; r < w.M; r += gridDim.x) {
-            for (int64_t c0 = threadIdx.x; c0 < w.cpr; c0 += kPtThreads * kPtUnroll) {
-                uint4 v[kPtUnroll];
-#pragma unroll
-                for (int u = 0; u < kPtUnroll; ++u) {
-                    const int64_t c = c0 + (int64_t)u * kPtThreads;
-                    v[u] = c < w.cpr ? __ldcs(reinterpret_cast<const uint4*>(x + chunk_offset(w, r, c)))
-                                     : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < kPtUnroll; ++u) {
-                    const int64_t c = c0 + (int64_t)u * kPtThreads;
-                    if (c < w.cpr)
-                        __stcs(reinterpret_cast<uint2*>(q + r * ldq + c * 8),
-                               all_mul ? quant8_mul(v[u], bs.r) : quant8(v[u], bs));
-                }
-            }
-        }
-    }
+    with_cast(all_mul, [&](auto cast) { cast_walk<decltype(cast)::mul>(x, w, q, ldq, bs); });
 }
 
 cudaError_t launch_cast_with_scale(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
